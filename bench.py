@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Benchmark: FP32 C = A x B at M = N = K = 4096 on one GB300 (TFLOP/s).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one call of ``gemm_f32`` (the whole hot path: block-tile
+scheduling, shared-memory staging, register-tiled FFMA, epilogue) on the
+headline workload, operands resident in HBM, L2 flushed before every step by
+writing a buffer twice the L2 size.  Each step is timed with CUDA events on the
+launching stream; the JSON line reports the mean.  ``e2e`` repeats the
+measurement through the same C-ABI call with the operands in pinned host
+memory, the host-to-device copies of A and B and the device-to-host copy of C
+inside each timed step.
+
+Under torchrun (N > 1) every rank runs an independent replica of the product
+on its own GPU (the product has no exchange step); ``value`` is the FLOPs of
+all ranks over the slowest rank's time.
+
+``--impl reference`` times the CPU oracle instead (rank 0 only), each step a
+bounded sample of rows of the same product, on all host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from tiled_matrix_multiply_gb300 import inputs, tiling_model  # noqa: E402
+
+METRIC = "FP32 GEMM TFLOP/s at M=N=K=4096 on 1 GB300; % of FP32 (or tensor-pipe) roofline"
+UNIT = "TFLOP/s"
+FFMA_PER_CLK_PER_SM = 128          # 4 sub-partitions x 32 FP32 lanes
+FALLBACK_SM_MAX_MHZ = 2070.0
+
+
+# -- distributed plumbing ---------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def reduce_over_ranks(dist, local_ms: float, local_flops: float):
+    """(max time over ranks, summed FLOPs) -- the whole-job aggregate."""
+    if dist is None:
+        return local_ms, local_flops
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    f = torch.tensor([local_flops], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(f, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(f.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# -- clocks -------------------------------------------------------------------------------
+
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs."""
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self._thr = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={','.join(CLOCK_FIELDS)}",
+               "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._thr = threading.Thread(target=self._read, daemon=True)
+        self._thr.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._thr:
+            self._thr.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(CLOCK_FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(REASON_NAMES, parts[4:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -- peaks ----------------------------------------------------------------------------------
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f)
+    return {}
+
+
+def ffma_peak_tflops(sm_count: int, peaks: dict) -> tuple[float, str]:
+    """SMs x 128 FFMA/clk x 2 FLOP x maximum SM clock."""
+    mhz = peaks.get("sm_max_mhz")
+    src = "MEASURED_PEAKS.json sm_max_mhz"
+    if not mhz:
+        mhz, src = FALLBACK_SM_MAX_MHZ, "fallback 2070 MHz"
+    return sm_count * FFMA_PER_CLK_PER_SM * 2 * mhz * 1e6 / 1e12, \
+        f"{sm_count} SMs x 128 FFMA/clk x 2 FLOP x {mhz:.0f} MHz ({src})"
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it is for the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(f"{kernel}/{workload}")
+    if not rec:
+        return None
+    from tiled_matrix_multiply_gb300 import build
+    if rec.get("source_sha") != build.source_digest():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# -- the oracle as the CPU baseline / reference arm ---------------------------------------------
+
+def oracle_sample(A: np.ndarray, B: np.ndarray, rows: int, threads: int) -> float:
+    """Seconds the oracle takes for the first `rows` rows of C = A x B."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.gemm(A[:rows], B, threads=threads)
+    return time.perf_counter() - t0
+
+
+def calibrate_rows(A, B, threads: int, target_s: float) -> tuple[int, float]:
+    """Rows of C whose oracle time is about target_s (at least one row per thread)."""
+    M = A.shape[0]
+    rows = min(M, max(threads, 1))
+    t = oracle_sample(A, B, rows, threads)
+    while t < 0.2 * target_s and rows < M:
+        rows = min(M, rows * 4)
+        t = oracle_sample(A, B, rows, threads)
+    want = int(rows * target_s / max(t, 1e-9))
+    want = max(threads, (want // threads) * threads)
+    return min(M, want), t / rows
+
+
+def cpu_baseline(A, B, w, target_s=10.0) -> dict:
+    import oracle
+    threads = oracle.default_threads()
+    rows, _ = calibrate_rows(A, B, threads, min(2.0, target_s / 5))
+    rows = min(w.M, max(threads, int(rows * target_s / 2.0) // threads * threads))
+    t = oracle_sample(A, B, rows, threads)
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {rows} of {w.M} rows of C ({rows}x{w.N}x{w.K}, FP64 accumulation), "
+                      f"{t:.1f} s wall on {threads} OpenMP threads"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    w = inputs.WORKLOADS[args.workload]
+    A, B = inputs.workload_operands(w)
+    threads = oracle.default_threads()
+    total_steps = args.steps + args.warmup
+    per_step = max(0.05, min(5.0, 90.0 / total_steps))
+    rows, _ = calibrate_rows(A, B, threads, per_step)
+    for _ in range(args.warmup):
+        oracle_sample(A, B, rows, threads)
+    times = [oracle_sample(A, B, rows, threads) for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(times)
+    flops = 2.0 * rows * w.N * w.K
+    value = flops / (ms / 1e3) / 1e12
+    sample = (f"each step: first {rows} of {w.M} rows of C ({rows}x{w.N}x{w.K}), "
+              f"FP64 accumulation on {threads} OpenMP threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, "CPU oracle (row sample)"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, path: str) -> dict:
+    return {"workload": f"{w.name}: {w.describe()}", "M": w.M, "N": w.N, "K": w.K,
+            "layout": "row-major, lda=K, ldb=N, ldc=N", "path": path,
+            "l2": "flushed before every step (memset of 2x L2 bytes, outside the events)"}
+
+
+# -- the GPU arm ------------------------------------------------------------------------------
+
+def time_device(step_fn, flush_fn, steps: int, warmup: int, stream, dist) -> list[float]:
+    """Per-step device times (ms) of step_fn, L2 flushed before each step."""
+    import torch
+    for _ in range(warmup):
+        flush_fn()
+        step_fn()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush_fn()
+        starts[i].record(stream)
+        step_fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import tiled_matrix_multiply_gb300 as tmm
+    from tiled_matrix_multiply_gb300 import _abi, build
+
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}), flush=True)
+        return 1
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    build.build()
+    _abi.load()
+
+    w = inputs.WORKLOADS[args.workload]
+    A_h, B_h = inputs.workload_operands(w)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    stream = torch.cuda.current_stream(dev)
+    A = torch.from_numpy(A_h).to(dev)
+    B = torch.from_numpy(B_h).to(dev)
+    C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20) or (128 << 20))
+    flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    launches = {"n": 0}
+
+    def step():
+        _abi.check("gemm_f32", w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N,
+                   C.data_ptr(), w.N, stream.cuda_stream)
+        launches["n"] += 1
+
+    def flush():
+        flush_buf.zero_()
+
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid else None)
+    sampler.start()
+    time.sleep(0.3)
+    launches["n"] = 0
+    times = time_device(step, flush, args.steps, args.warmup, stream, dist)
+    timed_launches = launches["n"] - args.warmup
+    clocks = sampler.stop()
+    local_ms = statistics.mean(times)
+    ms, total_flops = reduce_over_ranks(dist, local_ms, float(w.flops))
+    value = total_flops / (ms / 1e3) / 1e12
+
+    # End to end through the same call: pinned host operands in, result out, per step.
+    A_pin = torch.from_numpy(A_h).pin_memory()
+    B_pin = torch.from_numpy(B_h).pin_memory()
+    C_pin = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        A.copy_(A_pin, non_blocking=True)
+        B.copy_(B_pin, non_blocking=True)
+        step()
+        C_pin.copy_(C, non_blocking=True)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 50))
+        e2e_times = time_device(e2e_step, flush, e2e_steps, args.warmup, stream, dist)
+        e2e_ms, e2e_flops = reduce_over_ranks(dist, statistics.mean(e2e_times), float(w.flops))
+        e2e = {"value": e2e_flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": A_h.nbytes + B_h.nbytes,
+               "d2h_bytes_per_step": w.M * w.N * 4, "ms_per_step": e2e_ms,
+               "steps": e2e_steps}
+
+    # Roofline of the one kernel a step launches.
+    peaks = measured_peaks()
+    peak, peak_src = ffma_peak_tflops(props.multi_processor_count, peaks)
+    achieved = w.flops / (local_ms / 1e3) / 1e12
+    roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "traffic": recorded_traffic("gemm_simt", w.name),
+                "peak_source": peak_src,
+                "algorithmic": f"2MNK = {w.flops:.4e} FLOP per launch",
+                "frac_at_measured_clock": (achieved / (peak * clocks["sm_mhz"] /
+                                                       (peaks.get("sm_max_mhz") or
+                                                        FALLBACK_SM_MAX_MHZ))
+                                           if clocks.get("sm_mhz") else None)}
+
+    extra = {}
+    if not args.no_contrast and rank == 0:
+        extra["contrast"] = contrast_paths(args, w, A, B, C, flush, stream, props, peaks)
+
+    if rank == 0:
+        cpu = (cpu_baseline(A_h, B_h, w, args.cpu_seconds)
+               if world == 1 and args.cpu_seconds > 0 else None)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": workload_config(w, "gemm_f32 (tiled SIMT FFMA)"),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": timed_launches,
+            "ms_per_step_min": min(times), "ms_per_step_max": max(times),
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def contrast_paths(args, w, A, B, C, flush, stream, props, peaks) -> dict:
+    """The naive kernel on the same workload (a few steps): the untiled contrast."""
+    import torch
+    from tiled_matrix_multiply_gb300 import _abi
+
+    def naive():
+        _abi.check("gemm_f32_naive", w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N,
+                   C.data_ptr(), w.N, stream.cuda_stream)
+    t = time_device(naive, flush, 3, 1, stream, None)
+    ms = statistics.mean(t)
+    return {"gemm_f32_naive": {"ms_per_step": ms, "value": w.flops / (ms / 1e3) / 1e12,
+                               "unit": UNIT,
+                               "logical_operand_bytes": 4 * tiling_model.q_naive(w.M, w.N, w.K)}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=inputs.HEADLINE, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="oracle CPU-baseline budget; 0 skips the CPU baseline")
+    ap.add_argument("--no-contrast", action="store_true", help="skip the naive-kernel contrast")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps, always
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

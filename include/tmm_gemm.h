@@ -1,0 +1,115 @@
+/*
+ * tmm_gemm.h -- C ABI of the GB300 (sm_103a) FP32 matrix-product library.
+ *
+ * Every entry point computes the matrix product of "Tiling Hierarchy on GPUs"
+ * (introduction and section "Inner Product"), C = A x B with A of M x K,
+ * B of K x N and C of M x N, all row-major:
+ *
+ *     C[i*ldc + j] = sum_{k=0}^{K-1} A[i*lda + k] * B[k*ldb + j]
+ *                                        for 0 <= i < M, 0 <= j < N.
+ *
+ * C is overwritten; it is never read (no alpha/beta scaling: the pages define
+ * none, and "CMU DLSys Lecture 12" section 5 counts no initial read of C).
+ * Elements of C outside the M x N window (the ldc - N gap of each row) are
+ * not touched.  Summation order inside the kernels is not specified; results
+ * agree with the exact product to FP32 rounding (each entry within about
+ * sqrt(K) units of FP32 rounding of the terms it sums), and are exact whenever
+ * every partial sum is exactly representable (for example small-integer
+ * inputs with sums below 2^24).
+ *
+ * Arguments (all entry points):
+ *   M, N, K      sizes, 0 <= size <= 2^31 - 1.  M == 0 or N == 0 is a no-op
+ *                (no CUDA call is made).  K == 0 writes zeros to the M x N
+ *                window of C (the empty sum).
+ *   A, B         DEVICE pointers (cudaMalloc'd or any device-accessible
+ *                memory of the current device) to FP32 row-major operands.
+ *                Caller-owned; read only.  Pointers must be 4-byte aligned
+ *                (natural float alignment); 16-byte aligned bases with lda,
+ *                ldb, K and N multiples of 4 take the vectorised load path.
+ *   lda, ldb     leading dimensions in elements: lda >= max(1, K),
+ *                ldb >= max(1, N).
+ *   C            DEVICE pointer to the FP32 row-major result, caller-owned,
+ *                written only.  The M x N window of C must not overlap A or B.
+ *   ldc          leading dimension of C in elements, ldc >= max(1, N).
+ *   stream       CUDA stream (cudaStream_t) the work is enqueued on; NULL is
+ *                the legacy default stream.  Every call is asynchronous: it
+ *                returns once the kernel is enqueued; the caller synchronises.
+ *
+ * The library allocates no device or host memory per call.  All entry points
+ * use the current CUDA device (cudaSetDevice) and are thread-safe.
+ *
+ * Return value: TMM_OK (0) when the work was enqueued, otherwise one of the
+ * negative TMM_ERR_* codes below, in which case nothing was launched.  No
+ * exception crosses the ABI and nothing is printed; tmm_last_error_string()
+ * gives a one-line description of the calling thread's last failure.
+ */
+#ifndef TMM_GEMM_H
+#define TMM_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream, declared here so that this header
+ * does not need the CUDA headers. */
+typedef struct CUstream_st *tmm_stream_t;
+
+#define TMM_OK 0
+/* A size is negative or above 2^31 - 1, a leading dimension is shorter than
+ * its row, a pointer is NULL while its matrix is non-empty or not 4-byte
+ * aligned, or a byte offset would overflow int64. */
+#define TMM_ERR_INVALID_ARG (-1)
+/* The byte range spanned by C's M x N window overlaps the range spanned by
+ * A's M x K window or B's K x N window. */
+#define TMM_ERR_ALIAS (-2)
+/* The current device is not a compute capability 10.3 (GB300-class) GPU. */
+#define TMM_ERR_UNSUPPORTED_DEVICE (-3)
+/* A CUDA runtime call or kernel launch failed (text in tmm_last_error_string). */
+#define TMM_ERR_CUDA (-4)
+
+/*
+ * gemm_f32 -- the tiled FP32 product on the CUDA cores (FFMA, IEEE single
+ * precision, one rounding per multiply-add).
+ *
+ * Follows the two-level tiling of "Tiling Strategies" sections 2-4 and "CMU
+ * DLSys Lecture 12" section 5: each thread block owns one block tile of C,
+ * stages K-slices of A and B in shared memory (double buffered, as in
+ * "Tiling Strategies" section 3), and each thread accumulates an 8 x 8 tile
+ * of C in registers as a sequence of outer products ("Tiling Hierarchy on
+ * GPUs", sections "Register Tiling" and "Register prefetching").  Tail tiles
+ * are handled with zero-filled masked loads and masked stores (DLSys section 5).
+ */
+int gemm_f32(int64_t M, int64_t N, int64_t K,
+             const float *A, int64_t lda,
+             const float *B, int64_t ldb,
+             float *C, int64_t ldc,
+             tmm_stream_t stream);
+
+/*
+ * gemm_f32_naive -- one output per thread, each walking a row of A and a
+ * column of B straight from global memory ("Tiling Strategies" section 2,
+ * "The Problem"; "CMU DLSys Lecture 12" section 1 for the bounds-checked
+ * one-thread-per-output launch).  Kept as the untiled contrast; the sum for
+ * each output is accumulated with fmaf in ascending k.
+ */
+int gemm_f32_naive(int64_t M, int64_t N, int64_t K,
+                   const float *A, int64_t lda,
+                   const float *B, int64_t ldb,
+                   float *C, int64_t ldc,
+                   tmm_stream_t stream);
+
+/* One-line description of the calling thread's last failed call ("" if none).
+ * The string is owned by the library and valid until the thread's next call. */
+const char *tmm_last_error_string(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int tmm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TMM_GEMM_H */

@@ -1,0 +1,68 @@
+"""Device-buffer helpers for the GPU parity tests (torch used for memory only).
+
+Operands are placed in flat device buffers at a chosen element offset and
+leading dimension, with every element outside the matrix window set to a
+canary NaN bit pattern; after a call the canaries of C are checked untouched,
+so a kernel that writes outside its M x N window (or into the ldc gaps) fails.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from tiled_matrix_multiply_gb300 import _abi
+
+CANARY_BITS = np.uint32(0x7FC0DEAD)   # a quiet NaN with a recognisable payload
+GUARD = 64                              # canary elements after each window
+
+
+class DevMatrix:
+    """A rows x cols float32 matrix inside a canary-filled flat device buffer.
+
+    Layout: ``offset`` canary elements, then ``rows`` rows of ``ld`` elements
+    (the first ``cols`` of each are the matrix), then ``GUARD`` canaries.
+    """
+
+    def __init__(self, host: np.ndarray | None, rows: int, cols: int, ld: int | None = None,
+                 offset: int = 0, device="cuda"):
+        self.rows, self.cols = rows, cols
+        self.ld = max(ld if ld is not None else cols, 1)
+        self.offset = offset
+        n = offset + rows * self.ld + GUARD
+        flat = np.full(n, CANARY_BITS, dtype=np.uint32).view(np.float32)
+        if host is not None and rows and cols:
+            self._rows_view(flat)[:, :cols] = host
+        self.buf = torch.from_numpy(flat).to(device)
+        self.ptr = self.buf.data_ptr() + 4 * offset
+
+    def _rows_view(self, flat):
+        return flat[self.offset:self.offset + self.rows * self.ld].reshape(self.rows, self.ld)
+
+    def window(self) -> np.ndarray:
+        flat = self.buf.cpu().numpy()
+        return self._rows_view(flat)[:, :self.cols].copy()
+
+    def outside_window_untouched(self) -> bool:
+        flat = self.buf.cpu().numpy().view(np.uint32)
+        ok = np.all(flat[:self.offset] == CANARY_BITS)
+        ok &= np.all(flat[self.offset + self.rows * self.ld:] == CANARY_BITS)
+        ok &= np.all(self._rows_view(flat)[:, self.cols:] == CANARY_BITS)
+        return bool(ok)
+
+
+def run_entry(entry: str, A: np.ndarray, B: np.ndarray, *, lda=None, ldb=None, ldc=None,
+              a_off=0, b_off=0, c_off=0, stream=None, check_canaries=True) -> np.ndarray:
+    """C = A x B through the C ABI on device buffers laid out as requested."""
+    M, K = A.shape
+    K2, N = B.shape
+    assert K == K2
+    dA = DevMatrix(A, M, K, lda, a_off)
+    dB = DevMatrix(B, K, N, ldb, b_off)
+    dC = DevMatrix(None, M, N, ldc, c_off)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = _abi.call(entry, M, N, K, dA.ptr, dA.ld, dB.ptr, dB.ld, dC.ptr, dC.ld, s.cuda_stream)
+    assert rc == _abi.TMM_OK, f"{entry} returned {rc}: {_abi.last_error()}"
+    torch.cuda.synchronize()
+    if check_canaries:
+        assert dC.outside_window_untouched(), f"{entry} wrote outside C's M x N window"
+    return dC.window()

@@ -1,0 +1,95 @@
+"""The C-ABI library on the host: it builds, loads, exports what the header
+declares, and rejects bad arguments before touching the GPU (CPU only; no
+compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tiled_matrix_multiply_gb300 import _abi, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _abi.load()
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_product_entry_points():
+    names = declared_functions()
+    for n in ("gemm_f32", "gemm_f32_naive", "tmm_last_error_string", "tmm_version"):
+        assert n in names
+    assert set(names) == set(_abi.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version(lib):
+    assert lib.tmm_version() >= 100
+
+
+FAKE = 0x7F0000001000  # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("entry", _abi.GEMM_ENTRY_POINTS)
+@pytest.mark.parametrize("args,status", [
+    ((-1, 4, 4, FAKE, 4, FAKE, 4, FAKE + (1 << 20), 4), _abi.TMM_ERR_INVALID_ARG),  # M < 0
+    ((4, -1, 4, FAKE, 4, FAKE, 4, FAKE, 4), _abi.TMM_ERR_INVALID_ARG),             # N < 0
+    ((4, 4, -2, FAKE, 4, FAKE, 4, FAKE, 4), _abi.TMM_ERR_INVALID_ARG),             # K < 0
+    ((4, 4, 8, FAKE, 7, FAKE, 4, FAKE, 4), _abi.TMM_ERR_INVALID_ARG),              # lda < K
+    ((4, 5, 8, FAKE, 8, FAKE, 4, FAKE, 5), _abi.TMM_ERR_INVALID_ARG),              # ldb < N
+    ((4, 5, 8, FAKE, 8, FAKE, 5, FAKE, 4), _abi.TMM_ERR_INVALID_ARG),              # ldc < N
+    ((4, 4, 4, 0, 4, FAKE, 4, FAKE, 4), _abi.TMM_ERR_INVALID_ARG),                 # A NULL
+    ((4, 4, 4, FAKE, 4, 0, 4, FAKE, 4), _abi.TMM_ERR_INVALID_ARG),                 # B NULL
+    ((4, 4, 4, FAKE, 4, FAKE, 4, 0, 4), _abi.TMM_ERR_INVALID_ARG),                 # C NULL
+    ((4, 4, 4, FAKE + 2, 4, FAKE, 4, FAKE + (1 << 20), 4), _abi.TMM_ERR_INVALID_ARG),  # misaligned
+    ((1 << 31, 4, 4, FAKE, 4, FAKE, 4, FAKE + (1 << 20), 4),
+     _abi.TMM_ERR_INVALID_ARG),                                                     # M >= 2^31
+    ((1 << 20, 1 << 30, 4, FAKE, 4, FAKE, 1 << 30, FAKE, (1 << 62)),
+     _abi.TMM_ERR_INVALID_ARG),                                                     # overflow
+    ((8, 8, 8, FAKE, 8, FAKE + (1 << 20), 8, FAKE + 64, 8), _abi.TMM_ERR_ALIAS),   # C inside A
+    ((8, 8, 8, FAKE, 8, FAKE + (1 << 20), 8, FAKE + (1 << 20) + 32, 8),
+     _abi.TMM_ERR_ALIAS),                                                           # C inside B
+])
+def test_invalid_arguments_are_rejected_without_a_launch(lib, entry, args, status):
+    rc = getattr(lib, entry)(*args, None)
+    assert rc == status
+    assert lib.tmm_last_error_string().decode()
+
+
+@pytest.mark.parametrize("entry", _abi.GEMM_ENTRY_POINTS)
+def test_empty_output_is_a_no_op(lib, entry):
+    # M == 0 or N == 0: nothing to compute, success without any CUDA call.
+    assert getattr(lib, entry)(0, 4, 4, 0, 4, 0, 4, 0, 4, None) == _abi.TMM_OK
+    assert getattr(lib, entry)(4, 0, 4, 0, 4, 0, 1, 0, 1, None) == _abi.TMM_OK
+
+
+def test_python_binding_rejects_host_tensors():
+    torch = pytest.importorskip("torch")
+    import tiled_matrix_multiply_gb300 as tmm
+    A = torch.zeros(4, 4)
+    with pytest.raises(ValueError):
+        tmm.gemm_f32(A, A)
+    with pytest.raises(TypeError):
+        tmm.gemm_f32(A.double(), A.double())

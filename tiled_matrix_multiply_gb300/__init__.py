@@ -1,1 +1,75 @@
-"""FP32 matrix product C = A x B on one GB300 (sm_103a), hand-written CUDA kernels."""
+"""FP32 matrix product C = A x B on one GB300 (sm_103a), hand-written CUDA kernels.
+
+The work is done by ``libtmm_gemm.so`` (C ABI in ``include/tmm_gemm.h``);
+this package marshals torch CUDA tensors to it.  PyTorch provides device
+memory and streams only.
+
+    import torch, tiled_matrix_multiply_gb300 as tmm
+    C = tmm.gemm_f32(A, B)            # A: (M, K), B: (K, N) float32 CUDA tensors
+
+``gemm_f32`` is the tiled FFMA path; ``gemm_f32_naive`` is the
+one-output-per-thread contrast kernel.  Both are asynchronous on the current
+torch stream of the operands' device.
+"""
+from __future__ import annotations
+
+from ._abi import (TMM_ERR_ALIAS, TMM_ERR_CUDA, TMM_ERR_INVALID_ARG,  # noqa: F401
+                   TMM_ERR_UNSUPPORTED_DEVICE, TMM_OK, TmmError)
+
+__all__ = ["gemm_f32", "gemm_f32_naive", "raw_call", "TmmError"]
+
+
+def _matrix(x, name):
+    import torch
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if x.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {x.dtype}")
+    if x.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(x.shape)}")
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    rows, cols = x.shape
+    if cols > 1 and x.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major (unit column stride)")
+    ld = x.stride(0) if rows > 1 else max(cols, 1)
+    if x.numel() and ld < cols:
+        raise ValueError(f"{name} has a row stride shorter than its rows")
+    return rows, cols, max(ld, cols, 1)
+
+
+def _product(entry: str, A, B, C=None, stream=None):
+    import torch
+    from . import _abi
+    M, K, lda = _matrix(A, "A")
+    K2, N, ldb = _matrix(B, "B")
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+    if A.device != B.device:
+        raise ValueError("A and B are on different devices")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    elif C.shape != (M, N) or C.device != A.device:
+        raise ValueError(f"C must be ({M}, {N}) on {A.device}")
+    _, _, ldc = _matrix(C, "C")
+    with torch.cuda.device(A.device):
+        s = stream if stream is not None else torch.cuda.current_stream(A.device)
+        _abi.check(entry, M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
+                   s.cuda_stream)
+    return C
+
+
+def gemm_f32(A, B, C=None, stream=None):
+    """C = A x B on the tiled FFMA path (C allocated when not given)."""
+    return _product("gemm_f32", A, B, C, stream)
+
+
+def gemm_f32_naive(A, B, C=None, stream=None):
+    """C = A x B, one output per thread, operands from global memory."""
+    return _product("gemm_f32_naive", A, B, C, stream)
+
+
+def raw_call(entry: str, M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, stream_ptr=0) -> int:
+    """Call a C-ABI entry point with plain integers; returns the status code."""
+    from . import _abi
+    return _abi.call(entry, M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, stream_ptr)

@@ -1,0 +1,165 @@
+// gemm_abi.cpp -- the extern "C" boundary: argument checks, device checks,
+// path selection and launch-status reporting.  No device memory is allocated.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/tmm_gemm.h"
+#include "tmm_internal.h"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+int fail(int code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+bool g_dev_known[kMaxDevices] = {};
+tmm::DeviceInfo g_dev_info[kMaxDevices];
+
+// Properties of the current device, queried once per device.
+int current_device(tmm::DeviceInfo *out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(TMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(TMM_ERR_UNSUPPORTED_DEVICE, "device ordinal %d out of range", dev);
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_dev_known[dev]) {
+      *out = g_dev_info[dev];
+      return TMM_OK;
+    }
+  }
+  tmm::DeviceInfo info = {};
+  info.id = dev;
+  if ((e = cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+      (e = cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+      (e = cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, dev)) ||
+      (e = cudaDeviceGetAttribute(&info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                  dev)))
+    return fail(TMM_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+  if (info.cc_major != 10 || info.cc_minor != 3)
+    return fail(TMM_ERR_UNSUPPORTED_DEVICE,
+                "device %d has compute capability %d.%d; this library is built for 10.3 (sm_103a)",
+                dev, info.cc_major, info.cc_minor);
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    g_dev_info[dev] = info;
+    g_dev_known[dev] = true;
+  }
+  *out = info;
+  return TMM_OK;
+}
+
+// a * b + c without int64 overflow; false when it would overflow.
+bool span_ok(int64_t rows, int64_t ld, int64_t cols) {
+  if (rows <= 0 || cols <= 0) return true;
+  const __int128 last = (__int128)(rows - 1) * ld + cols;
+  return last <= (__int128)(INT64_MAX / 4);
+}
+
+// Byte range [lo, hi) spanned by the rows x cols window of a row-major matrix.
+void byte_span(const void *p, int64_t rows, int64_t ld, int64_t cols, uintptr_t *lo,
+               uintptr_t *hi) {
+  *lo = reinterpret_cast<uintptr_t>(p);
+  *hi = *lo + uintptr_t(((rows - 1) * ld + cols) * int64_t(sizeof(float)));
+}
+
+bool overlaps(uintptr_t a_lo, uintptr_t a_hi, uintptr_t b_lo, uintptr_t b_hi) {
+  return a_lo < b_hi && b_lo < a_hi;
+}
+
+// Checks shared by every entry point; on success *nothing_to_do tells whether
+// the call is a no-op (M == 0 or N == 0).
+int check_args(const char *who, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+               const float *B, int64_t ldb, const float *C, int64_t ldc, bool *nothing_to_do) {
+  *nothing_to_do = false;
+  if (M < 0 || N < 0 || K < 0)
+    return fail(TMM_ERR_INVALID_ARG, "%s: negative size (M=%lld N=%lld K=%lld)", who,
+                (long long)M, (long long)N, (long long)K);
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+    return fail(TMM_ERR_INVALID_ARG, "%s: sizes above 2^31-1 are not supported", who);
+  const int64_t min_lda = K > 1 ? K : 1, min_ldn = N > 1 ? N : 1;
+  if (lda < min_lda || ldb < min_ldn || ldc < min_ldn)
+    return fail(TMM_ERR_INVALID_ARG,
+                "%s: leading dimension too small (lda=%lld ldb=%lld ldc=%lld for K=%lld N=%lld)",
+                who, (long long)lda, (long long)ldb, (long long)ldc, (long long)K, (long long)N);
+  if (M == 0 || N == 0) {
+    *nothing_to_do = true;
+    return TMM_OK;
+  }
+  if (C == nullptr) return fail(TMM_ERR_INVALID_ARG, "%s: C is NULL", who);
+  if (K > 0 && (A == nullptr || B == nullptr))
+    return fail(TMM_ERR_INVALID_ARG, "%s: A or B is NULL", who);
+  if (!span_ok(M, lda, K) || !span_ok(K, ldb, N) || !span_ok(M, ldc, N))
+    return fail(TMM_ERR_INVALID_ARG, "%s: matrix extent overflows 64-bit byte offsets", who);
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(C)) & 3u)
+    return fail(TMM_ERR_INVALID_ARG, "%s: pointers must be 4-byte aligned", who);
+  if (K > 0) {
+    uintptr_t c_lo, c_hi, a_lo, a_hi, b_lo, b_hi;
+    byte_span(C, M, ldc, N, &c_lo, &c_hi);
+    byte_span(A, M, lda, K, &a_lo, &a_hi);
+    byte_span(B, K, ldb, N, &b_lo, &b_hi);
+    if (overlaps(c_lo, c_hi, a_lo, a_hi) || overlaps(c_lo, c_hi, b_lo, b_hi))
+      return fail(TMM_ERR_ALIAS, "%s: the byte range of C overlaps A or B", who);
+  }
+  return TMM_OK;
+}
+
+using Launcher = cudaError_t (*)(const tmm::GemmProblem &, const tmm::DeviceInfo &, cudaStream_t);
+
+int run(const char *who, Launcher launch, int64_t M, int64_t N, int64_t K, const float *A,
+        int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc, tmm_stream_t stream) {
+  bool noop = false;
+  int rc = check_args(who, M, N, K, A, lda, B, ldb, C, ldc, &noop);
+  if (rc != TMM_OK || noop) return rc;
+  tmm::DeviceInfo dev;
+  if ((rc = current_device(&dev)) != TMM_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (K == 0) {
+    // The empty sum: zero the M x N window of C, leaving the row gaps alone.
+    e = cudaMemset2DAsync(C, size_t(ldc) * sizeof(float), 0, size_t(N) * sizeof(float),
+                          size_t(M), s);
+    if (e != cudaSuccess)
+      return fail(TMM_ERR_CUDA, "%s: cudaMemset2DAsync: %s", who, cudaGetErrorString(e));
+    return TMM_OK;
+  }
+  const tmm::GemmProblem p = {M, N, K, A, lda, B, ldb, C, ldc};
+  e = launch(p, dev, s);
+  if (e != cudaSuccess) return fail(TMM_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
+  return TMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+             int64_t ldb, float *C, int64_t ldc, tmm_stream_t stream) {
+  return run("gemm_f32", tmm::launch_simt, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+int gemm_f32_naive(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                   int64_t ldb, float *C, int64_t ldc, tmm_stream_t stream) {
+  return run("gemm_f32_naive", tmm::launch_naive, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+const char *tmm_last_error_string(void) { return g_last_error; }
+
+int tmm_version(void) { return 100; }
+
+}  // extern "C"
