@@ -1,35 +1,45 @@
 // gemm_simt.cu -- two-level tiled FP32 product on the CUDA cores (FFMA).
 //
 // Tiling ("Tiling Strategies" sections 2-4, "CMU DLSys Lecture 12" section 5):
-//   * block tile: each 256-thread block owns a BM x BN = 128 x 128 tile of C;
-//   * K-slices of BK = 8: the block stages the BM x BK slab of A and the
-//     BK x BN slab of B in shared memory, double buffered ("Tiling
-//     Strategies" section 3): the global loads of slice t+1 are in flight
-//     (held in registers) while slice t is consumed, and are written to the
-//     other buffer just before it is needed, so one barrier per slice suffices;
-//   * thread tile: each thread owns an 8 x 8 tile of C in 64 accumulators and
-//     performs one outer product per k (8 + 8 operands, 64 FFMA), with the
+//   * block tile: each 128-thread block (4 warps, 2 x 2) owns a 128 x 128 tile
+//     of C; two blocks are resident per SM;
+//   * K-slices of BK = 16 flow through a ring of kStages shared-memory stages
+//     filled by asynchronous copies (cp.async).  This generalises the double
+//     buffer of "Tiling Strategies" section 3: the copies of the next
+//     kStages - 1 slices are in flight while one slice is consumed, and no
+//     register holds staged data;
+//   * thread tile: each thread owns a 16 x 8 tile of C (128 accumulators) and
+//     performs one outer product per k, 16 + 8 operands for 128 FFMA, with the
 //     operands of step k+1 loaded from shared memory while step k's FFMAs
 //     issue ("Tiling Hierarchy on GPUs", "Register Tiling", "Register
-//     prefetching").
+//     prefetching", "Reducing Overhead Slots").
 //
 // Shared-memory layout.  The A slab is stored transposed, a[k][m], so a
-// thread's 8 rows of A at one k are two 16-byte vectors; the row length is
-// padded to BM + 4 floats, which makes the transposing stores conflict-free
-// (each warp writes 16 rows x 2 k-quads that land in 32 distinct banks).  The
-// B slab keeps its global layout b[k][n].  A warp covers a 32 x 64 region of
-// C with its lanes as 4 (rows) x 8 (columns), each lane's 8 x 8 tile split
-// into 4 x 4 quadrants 16 rows / 32 columns apart: every fragment load of a
-// warp then reads 4 (A) or 8 (B) distinct 16-byte vectors of one 128-byte
-// line -- one shared-memory wavefront, the other lanes served by broadcast.
+// thread's rows of A at one k are 16-byte vectors; it is filled by 4-byte
+// copies, each warp copying 4 rows x 8 consecutive k (four 32-byte global
+// sectors) into 32 distinct banks (row length BM + 4 floats).  The B slab
+// keeps its global layout b[k][n] and is filled by 16-byte copies of whole
+// 512-byte row segments when B is 16-byte aligned (4-byte copies otherwise).
 //
-// Tails ("CMU DLSys Lecture 12" section 5, single-buffer schedule): loads
-// outside M, N or K are replaced by zeros, which add nothing to the sums, and
-// only entries inside M x N are stored.
+// Warp tiling ("Tiling Hierarchy on GPUs", "Warp Tiling"): each warp covers a
+// 64 x 64 region of C; lane (lm, ln), lm in 0..3, ln in 0..7, owns rows
+// lm*4 + 16t + i and columns ln*4 + 32c + j (t < 4, c < 2, i, j < 4).  A
+// 128-bit shared load is served at most 16 lanes per wavefront, and the two
+// quarter-warps of a half-warp share a wavefront only when they read disjoint
+// words with lanes that share a word paired up.  With quarter q = lane / 8,
+//     lm = lane % 2 + 2 (q % 2),
+//     ln = (lane / 2) % 4 + 4 ((q % 2) xor (q / 2)),
+// every fragment load, of A or of B, takes two wavefronts, the minimum.
+//
+// Tails ("CMU DLSys Lecture 12" section 5): copies outside M, N or K are
+// zero-filled (source size 0), which adds nothing to the sums, and only
+// entries inside M x N are stored.
 //
 // Scheduling: tiles are numbered along a grouped raster -- kGroupM tile-rows
 // are walked column by column -- so blocks resident at the same time share
 // the A row-panels and B column-panels they read through L2.
+#include <atomic>
+
 #include "tmm_internal.h"
 
 namespace tmm {
@@ -37,22 +47,50 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int BK = 8;
-constexpr int TM = 8;
-constexpr int TN = 8;
-constexpr int kThreads = (BM / TM) * (BN / TN);  // 256
-constexpr int kAsLd = BM + 4;                    // padded row of the transposed A slab
+constexpr int BK = 16;
+constexpr int kStages = 4;
+constexpr int TM = 16;                       // thread tile rows
+constexpr int TN = 8;                        // thread tile columns
+constexpr int kWarpsM = 2, kWarpsN = 2;
+constexpr int kThreads = 32 * kWarpsM * kWarpsN;  // 128
+constexpr int kAsLd = BM + 4;                // row of the transposed A slab (floats)
 constexpr int kBsLd = BN;
+constexpr int kStageFloats = BK * kAsLd + BK * kBsLd;
+constexpr int kSmemBytes = kStages * kStageFloats * 4;
 constexpr int kGroupM = 16;
+constexpr int kKUnroll = 4;                  // k steps per iteration of the inner loop
 
-static_assert(kThreads == 256, "thread mapping below assumes 256 threads");
-static_assert(BM * BK == kThreads * 4 && BN * BK == kThreads * 4,
-              "each thread stages one 4-element vector of A and of B per slice");
+static_assert(BM == kWarpsM * 4 * TM && BN == kWarpsN * 8 * TN, "warp tile is 4 x 8 lanes");
+static_assert(BM * BK == kThreads * 16, "each thread copies 16 elements of the A slab");
+static_assert(BK * BN == kThreads * 16, "each thread copies 16 elements of the B slab");
+static_assert(BK % kKUnroll == 0 && kKUnroll % 2 == 0, "inner loop ping-pongs fragments");
 
-struct __align__(16) SimtSmem {
-  float a[2][BK][kAsLd];
-  float b[2][BK][kBsLd];
-};
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Asynchronous global->shared copies; a false predicate copies zero bytes and
+// zero-fills the destination.  The source is then not read, and is replaced by
+// `safe` (an address inside the operand) all the same.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const float *src, bool pred,
+                                           const float *safe) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst),
+               "l"(pred ? src : safe), "r"(pred ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const float *src, bool pred,
+                                            const float *safe) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
+               "l"(pred ? src : safe), "r"(pred ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &tm,
                                             int &tn) {
@@ -65,16 +103,15 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
   tn = in_group / rows;
 }
 
-// kVecLoad: A and B are 16-byte aligned, lda, ldb, K and N are multiples of 4,
-//           so every staged 4-vector is either wholly inside or wholly outside.
+// kVecB:     B is 16-byte aligned and ldb, N are multiples of 4 (16-byte copies).
 // kVecStore: C is 16-byte aligned and ldc, N are multiples of 4.
-template <bool kVecLoad, bool kVecStore>
+template <bool kVecB, bool kVecStore>
 __global__ void __launch_bounds__(kThreads, 2)
 gemm_simt_kernel(int M, int N, int K,
                  const float *__restrict__ A, int64_t lda,
                  const float *__restrict__ B, int64_t ldb,
                  float *__restrict__ C, int64_t ldc, int tiles_m, int tiles_n) {
-  __shared__ SimtSmem sm;
+  extern __shared__ __align__(16) float smem[];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -85,24 +122,64 @@ gemm_simt_kernel(int M, int N, int K,
   const int m0 = tm * BM;
   const int n0 = tn * BN;
 
-  // Staging assignment: A vector = row a_row, k offset a_k (4 consecutive k);
-  // B vector = k row b_k, columns b_n..b_n+3.
-  const int a_row = tid >> 1;
-  const int a_k = (tid & 1) * 4;
-  const int b_k = tid >> 5;
-  const int b_n = (tid & 31) * 4;
-  const bool a_row_ok = m0 + a_row < M;
-  const int b_col = n0 + b_n;
-  const float *a_src = A + int64_t(a_row_ok ? m0 + a_row : 0) * lda + a_k;
-  const float *b_src = B + int64_t(b_k) * ldb + (b_col < N ? b_col : 0);
-  const int64_t b_step = int64_t(BK) * ldb;
+  // ---- copy assignment -------------------------------------------------------
+  // A: element `it` (0..15) of this thread is row a_r0 + 16 (it/2), k a_k0 + 8 (it%2).
+  const int a_r0 = (lane >> 3) + 4 * warp;
+  const int a_k0 = lane & 7;
+  uint32_t a_rows_ok = 0;                      // bit r: row a_r0 + 16 r inside M
+#pragma unroll
+  for (int r = 0; r < 8; ++r) a_rows_ok |= uint32_t(m0 + a_r0 + 16 * r < M) << r;
+  const float *a_src = A + int64_t(min(m0 + a_r0, M - 1)) * lda + a_k0;
+  const int64_t a_row_step = 16 * lda;
+  const uint32_t a_dst0 = smem_addr(smem) + 4u * (a_k0 * kAsLd + a_r0);
 
-  // Fragment assignment: warp (wm, wn) covers rows wm*32.., columns wn*64..;
-  // lane (lm, ln) reads A at rows a_off, a_off+16 and B at columns b_off, b_off+32.
-  const int wm = warp >> 1, wn = warp & 1;
-  const int lm = lane >> 3, ln = lane & 7;
-  const int a_off = wm * 32 + lm * 4;
-  const int b_off = wn * 64 + ln * 4;
+  // B: vectorised, vector v (0..3) is k row b_k0 + 4v, columns b_n0..b_n0+3;
+  //    scalar, element it (0..15) is k row b_k0 + 4 (it/4), column lane + 32 (it%4).
+  const int b_k0 = tid >> 5;
+  const int b_n0 = kVecB ? (tid & 31) * 4 : lane;
+  const float *b_src = B + int64_t(b_k0) * ldb + min(n0 + b_n0, N - 1);
+  const int64_t b_row4_step = 4 * ldb;
+  const uint32_t b_dst0 = smem_addr(smem) + 4u * (BK * kAsLd + b_k0 * kBsLd + b_n0);
+
+  const int num_slices = (K + BK - 1) / BK;
+
+  auto issue_slice = [&](int s, int stage) {
+    const int k0 = s * BK;
+    const uint32_t st_off = 4u * stage * kStageFloats;
+    const float *a = a_src + k0;
+#pragma unroll
+    for (int it = 0; it < 16; ++it) {
+      const int r = it >> 1, h = it & 1;
+      const bool ok = ((a_rows_ok >> r) & 1u) && (k0 + a_k0 + 8 * h < K);
+      cp_async_4(a_dst0 + st_off + 4u * (8 * h * kAsLd + 16 * r), a + r * a_row_step + 8 * h,
+                 ok, A);
+    }
+    const float *b = b_src + int64_t(k0) * ldb;
+    if (kVecB) {
+      const bool col_ok = n0 + b_n0 < N;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const bool ok = col_ok && (k0 + b_k0 + 4 * v < K);
+        cp_async_16(b_dst0 + st_off + 4u * (4 * v * kBsLd), b + v * b_row4_step, ok, B);
+      }
+    } else {
+#pragma unroll
+      for (int it = 0; it < 16; ++it) {
+        const int v = it >> 2, c = it & 3;
+        const bool ok = (n0 + b_n0 + 32 * c < N) && (k0 + b_k0 + 4 * v < K);
+        cp_async_4(b_dst0 + st_off + 4u * (4 * v * kBsLd + 32 * c), b + v * b_row4_step + 32 * c,
+                   ok, B);
+      }
+    }
+  };
+
+  // ---- fragment placement ----------------------------------------------------
+  const int q = lane >> 3;
+  const int lm = (lane & 1) + 2 * (q & 1);
+  const int ln = ((lane >> 1) & 3) + 4 * ((q & 1) ^ (q >> 1));
+  const int wm = warp / kWarpsN, wn = warp % kWarpsN;
+  const int a_off = wm * (4 * TM) + lm * 4;   // + 16 t
+  const int b_off = wn * (8 * TN) + ln * 4;   // + 32 c
 
   float acc[TM][TN];
 #pragma unroll
@@ -110,127 +187,131 @@ gemm_simt_kernel(int M, int N, int K,
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
 
-  float4 a_st, b_st;
-
-  // Stage the slice starting at k0 into registers; a_src/b_src point at it.
-  auto load_slice = [&](int k0) {
-    if (kVecLoad) {
-      const bool a_ok = a_row_ok && (k0 + a_k < K);
-      const bool b_ok = (b_col < N) && (k0 + b_k < K);
-      a_st = a_ok ? *reinterpret_cast<const float4 *>(a_src) : make_float4(0, 0, 0, 0);
-      b_st = b_ok ? *reinterpret_cast<const float4 *>(b_src) : make_float4(0, 0, 0, 0);
-    } else {
-      float av[4], bv[4];
-      const bool b_k_ok = k0 + b_k < K;
+  auto load_frag = [&](const float *st, int k, float (&af)[TM], float (&bf)[TN]) {
+    const float *as = st + k * kAsLd + a_off;
+    const float *bs = st + BK * kAsLd + k * kBsLd + b_off;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        av[j] = (a_row_ok && k0 + a_k + j < K) ? a_src[j] : 0.0f;
-        bv[j] = (b_k_ok && b_col + j < N) ? b_src[j] : 0.0f;
-      }
-      a_st = make_float4(av[0], av[1], av[2], av[3]);
-      b_st = make_float4(bv[0], bv[1], bv[2], bv[3]);
+    for (int t = 0; t < TM / 4; ++t) {
+      const float4 v = *reinterpret_cast<const float4 *>(as + 16 * t);
+      af[4 * t + 0] = v.x; af[4 * t + 1] = v.y; af[4 * t + 2] = v.z; af[4 * t + 3] = v.w;
+    }
+#pragma unroll
+    for (int c = 0; c < TN / 4; ++c) {
+      const float4 v = *reinterpret_cast<const float4 *>(bs + 32 * c);
+      bf[4 * c + 0] = v.x; bf[4 * c + 1] = v.y; bf[4 * c + 2] = v.z; bf[4 * c + 3] = v.w;
     }
   };
-  auto store_slice = [&](int buf) {
-    sm.a[buf][a_k + 0][a_row] = a_st.x;
-    sm.a[buf][a_k + 1][a_row] = a_st.y;
-    sm.a[buf][a_k + 2][a_row] = a_st.z;
-    sm.a[buf][a_k + 3][a_row] = a_st.w;
-    *reinterpret_cast<float4 *>(&sm.b[buf][b_k][b_n]) = b_st;
-  };
-  auto load_frag = [&](int buf, int k, float (&af)[TM], float (&bf)[TN]) {
-    const float4 a0 = *reinterpret_cast<const float4 *>(&sm.a[buf][k][a_off]);
-    const float4 a1 = *reinterpret_cast<const float4 *>(&sm.a[buf][k][a_off + 16]);
-    const float4 b0 = *reinterpret_cast<const float4 *>(&sm.b[buf][k][b_off]);
-    const float4 b1 = *reinterpret_cast<const float4 *>(&sm.b[buf][k][b_off + 32]);
-    af[0] = a0.x; af[1] = a0.y; af[2] = a0.z; af[3] = a0.w;
-    af[4] = a1.x; af[5] = a1.y; af[6] = a1.z; af[7] = a1.w;
-    bf[0] = b0.x; bf[1] = b0.y; bf[2] = b0.z; bf[3] = b0.w;
-    bf[4] = b1.x; bf[5] = b1.y; bf[6] = b1.z; bf[7] = b1.w;
+  auto outer_product = [&](const float (&af)[TM], const float (&bf)[TN]) {
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(af[i], bf[j], acc[i][j]);
   };
 
-  load_slice(0);
-  store_slice(0);
-  __syncthreads();
-
-  float af[TM], bf[TN];
-  int cur = 0;
-  for (int k0 = 0; k0 < K; k0 += BK) {
-    const bool has_next = k0 + BK < K;
-    if (has_next) {
-      a_src += BK;
-      b_src += b_step;
-      load_slice(k0 + BK);
-    }
+  // ---- pipeline ----------------------------------------------------------------
 #pragma unroll
-    for (int k = 0; k < BK; ++k) {
-      load_frag(cur, k, af, bf);
-#pragma unroll
-      for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(af[i], bf[j], acc[i][j]);
-    }
-    if (has_next) {
-      store_slice(cur ^ 1);
-      __syncthreads();
-    }
-    cur ^= 1;
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < num_slices) issue_slice(s, s);
+    cp_async_commit();
   }
 
-  // Epilogue: row i of the thread tile is m0 + a_off + (i/4)*16 + i%4,
-  // column j is n0 + b_off + (j/4)*32 + j%4.
+  float af[2][TM], bf[2][TN];
+  int stage = 0;
+  for (int s = 0; s < num_slices; ++s) {
+    cp_async_wait<kStages - 2>();   // slice s has landed (this thread's copies) ...
+    __syncthreads();                // ... and everyone's; slice s-1's stage is free
+    {
+      const int sn = s + kStages - 1;
+      int stage_n = stage + kStages - 1;
+      if (stage_n >= kStages) stage_n -= kStages;
+      if (sn < num_slices) issue_slice(sn, stage_n);
+      cp_async_commit();
+    }
+    const float *st = smem + stage * kStageFloats;
+    load_frag(st, 0, af[0], bf[0]);
+#pragma unroll 1
+    for (int kk = 0; kk < BK; kk += kKUnroll) {
+#pragma unroll
+      for (int u = 0; u < kKUnroll; ++u) {
+        const int k = kk + u;
+        if (u + 1 < kKUnroll || k + 1 < BK) load_frag(st, k + 1, af[(u + 1) & 1], bf[(u + 1) & 1]);
+        outer_product(af[u & 1], bf[u & 1]);
+      }
+    }
+    if (++stage == kStages) stage = 0;
+  }
+  cp_async_wait<0>();
+
+  // ---- epilogue: accumulator (4t + i, 4c + j) is C[m0 + a_off + 16t + i][n0 + b_off + 32c + j]
   const int row0 = m0 + a_off;
   const int col0 = n0 + b_off;
   float *c_base = C + int64_t(row0) * ldc + col0;
 #pragma unroll
-  for (int i = 0; i < TM; ++i) {
-    const int dr = (i >> 2) * 16 + (i & 3);
-    if (row0 + dr >= M) continue;
-    float *c_row = c_base + int64_t(dr) * ldc;
+  for (int t = 0; t < TM / 4; ++t) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int dc = h * 32;
-      if (kVecStore) {
-        if (col0 + dc < N)
-          *reinterpret_cast<float4 *>(c_row + dc) =
-              make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
-      } else {
+    for (int i = 0; i < 4; ++i) {
+      const int dr = 16 * t + i;
+      if (row0 + dr >= M) continue;
+      float *c_row = c_base + int64_t(dr) * ldc;
+      const float *a = acc[4 * t + i];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (col0 + dc + j < N) c_row[dc + j] = acc[i][4 * h + j];
+      for (int c = 0; c < TN / 4; ++c) {
+        const int dc = 32 * c;
+        if (kVecStore) {
+          if (col0 + dc < N)
+            *reinterpret_cast<float4 *>(c_row + dc) =
+                make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (col0 + dc + j < N) c_row[dc + j] = a[4 * c + j];
+        }
       }
     }
   }
 }
 
-template <bool kVecLoad, bool kVecStore>
-cudaError_t launch_variant(const GemmProblem &p, cudaStream_t stream) {
+// Dynamic shared memory above 48 KiB needs an opt-in per kernel and device.
+std::atomic<uint64_t> g_smem_configured[4];
+
+template <bool kVecB, bool kVecStore>
+cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
+  auto kernel = gemm_simt_kernel<kVecB, kVecStore>;
+  const int variant = (kVecB ? 2 : 0) + (kVecStore ? 1 : 0);
+  const uint64_t bit = uint64_t(1) << (dev.id & 63);
+  if (!(g_smem_configured[variant].load(std::memory_order_acquire) & bit)) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    g_smem_configured[variant].fetch_or(bit, std::memory_order_release);
+  }
   const int64_t tiles_m = (p.M + BM - 1) / BM;
   const int64_t tiles_n = (p.N + BN - 1) / BN;
   if (tiles_m * tiles_n > 0x7fffffff) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(tiles_m * tiles_n), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, gemm_simt_kernel<kVecLoad, kVecStore>, int(p.M), int(p.N),
-                            int(p.K), p.A, p.lda, p.B, p.ldb, p.C, p.ldc, int(tiles_m),
-                            int(tiles_n));
+  return cudaLaunchKernelEx(&cfg, kernel, int(p.M), int(p.N), int(p.K), p.A, p.lda, p.B, p.ldb,
+                            p.C, p.ldc, int(tiles_m), int(tiles_n));
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
-cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &, cudaStream_t stream) {
-  const bool vec_load = aligned16(p.A) && aligned16(p.B) && p.lda % 4 == 0 &&
-                        p.ldb % 4 == 0 && p.K % 4 == 0 && p.N % 4 == 0;
+cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
+  const bool vec_b = aligned16(p.B) && p.ldb % 4 == 0 && p.N % 4 == 0;
   const bool vec_store = aligned16(p.C) && p.ldc % 4 == 0 && p.N % 4 == 0;
-  if (vec_load)
-    return vec_store ? launch_variant<true, true>(p, stream)
-                     : launch_variant<true, false>(p, stream);
-  return vec_store ? launch_variant<false, true>(p, stream)
-                   : launch_variant<false, false>(p, stream);
+  if (vec_b)
+    return vec_store ? launch_variant<true, true>(p, dev, stream)
+                     : launch_variant<true, false>(p, dev, stream);
+  return vec_store ? launch_variant<false, true>(p, dev, stream)
+                   : launch_variant<false, false>(p, dev, stream);
 }
 
 }  // namespace tmm
