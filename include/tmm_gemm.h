@@ -69,6 +69,9 @@ typedef struct CUstream_st *tmm_stream_t;
 #define TMM_ERR_UNSUPPORTED_DEVICE (-3)
 /* A CUDA runtime call or kernel launch failed (text in tmm_last_error_string). */
 #define TMM_ERR_CUDA (-4)
+/* Reported by tmm_check_device: a bounded wait inside a kernel ran out of
+ * time, and results written since the last check are not valid. */
+#define TMM_ERR_DEVICE_TIMEOUT (-5)
 
 /*
  * gemm_f32 -- the tiled FP32 product on the CUDA cores (FFMA, IEEE single
@@ -81,6 +84,13 @@ typedef struct CUstream_st *tmm_stream_t;
  * of C in registers as a sequence of outer products ("Tiling Hierarchy on
  * GPUs", sections "Register Tiling" and "Register prefetching").  Tail tiles
  * are handled with zero-filled masked loads and masked stores (DLSys section 5).
+ *
+ * When the tile count leaves the last wave of blocks partly empty, the call
+ * runs persistent and cooperative (one block per resident slot) and splits
+ * the K range of the last tiles between pairs of blocks; the pair meets
+ * through a flag in library-owned device memory, with a bounded wait (see
+ * tmm_check_device).  Up to 16 such calls may be in flight at once (for
+ * example on different streams); results are deterministic either way.
  */
 int gemm_f32(int64_t M, int64_t N, int64_t K,
              const float *A, int64_t lda,
@@ -100,6 +110,26 @@ int gemm_f32_naive(int64_t M, int64_t N, int64_t K,
                    const float *B, int64_t ldb,
                    float *C, int64_t ldc,
                    tmm_stream_t stream);
+
+/*
+ * tmm_check_device -- synchronise `stream`, then read and clear the current
+ * device's status word.  Returns TMM_OK, or TMM_ERR_DEVICE_TIMEOUT when a
+ * bounded wait inside gemm_f32 (between the two blocks sharing a split tile)
+ * ran out of time since the last check; results written since then are not
+ * valid.  The pages have no counterpart: this is the library's failure
+ * detection ("CMU DLSys Lecture 12" section 2 only asks that API and launch
+ * errors be checked).  TMM_ERR_CUDA if the synchronisation itself failed.
+ */
+int tmm_check_device(tmm_stream_t stream);
+
+/*
+ * tmm_testing_set_wait_hooks -- testing only; no counterpart in the pages.
+ * drop_signal_block >= 0 makes that block of later stream-K launches skip
+ * raising its flag, so the block waiting on it runs into the time limit;
+ * wait_limit_ns > 0 sets that limit (default, and for values <= 0, 10 s).
+ * Process-wide; pass (-1, 0) to restore the defaults.  Always TMM_OK.
+ */
+int tmm_testing_set_wait_hooks(int drop_signal_block, int64_t wait_limit_ns);
 
 /* One-line description of the calling thread's last failed call ("" if none).
  * The string is owned by the library and valid until the thread's next call. */

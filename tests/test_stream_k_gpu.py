@@ -1,0 +1,88 @@
+"""GPU tests of the persistent stream-K schedule of gemm_f32 and of its bounded waits.
+
+Shapes are chosen so that the tile count (128 x 128 tiles) leaves a partial
+last wave on a 152-SM GB300 with two resident blocks per SM, which sends
+gemm_f32 down the persistent stream-K path: split tiles are summed by two
+blocks that meet through a flag.  The timeout test makes one block skip its
+flag (a testing hook of the library) with a 2 ms limit: the waiting block
+must give up, the library must report TMM_ERR_DEVICE_TIMEOUT through
+tmm_check_device, and the next call must be correct again.  No kernel faults
+or hangs: every wait is bounded and the kernel always runs to completion.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import parity  # noqa: E402
+from tiled_matrix_multiply_gb300 import _abi, build  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    _abi.load()
+
+
+def _run(*a, **k):
+    from gpu_util import run_entry
+    return run_entry(*a, **k)
+
+
+# (M, N, K): all tiles split (400 tiles); data-parallel waves plus split tiles
+# (1089 tiles); ragged K; ragged M and N with odd leading dimensions.
+SK_SHAPES = [(2560, 2560, 1000), (4224, 4224, 256), (2600, 2700, 1001), (3001, 2999, 777)]
+
+
+@pytest.mark.parametrize("shape", SK_SHAPES)
+def test_stream_k_shapes_float(shape):
+    M, N, K = shape
+    rng = np.random.default_rng(40)
+    A = rng.random((M, K), dtype=np.float32) * 2 - 1
+    B = rng.random((K, N), dtype=np.float32) * 2 - 1
+    C = _run("gemm_f32", A, B, check_canaries=False)
+    parity.assert_close(C, oracle.gemm(A, B), K, f"stream-K {shape}")
+    assert _abi.load().tmm_check_device(torch.cuda.current_stream().cuda_stream) == _abi.TMM_OK
+
+
+@pytest.mark.parametrize("shape", SK_SHAPES)
+def test_stream_k_shapes_integer_exact_and_deterministic(shape):
+    M, N, K = shape
+    rng = np.random.default_rng(41)
+    A = rng.integers(-4, 5, (M, K)).astype(np.float32)
+    B = rng.integers(-4, 5, (K, N)).astype(np.float32)
+    C1 = _run("gemm_f32", A, B, check_canaries=False)
+    parity.assert_bit_exact(C1, oracle.gemm(A, B), f"stream-K {shape}")
+    Af = rng.standard_normal((M, K), dtype=np.float32)
+    Bf = rng.standard_normal((K, N), dtype=np.float32)
+    D1 = _run("gemm_f32", Af, Bf, check_canaries=False)
+    D2 = _run("gemm_f32", Af, Bf, check_canaries=False)
+    assert np.array_equal(D1.view(np.uint32), D2.view(np.uint32))
+
+
+def test_stream_k_wait_timeout_is_reported_and_recovers():
+    lib = _abi.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    M, N, K = 2560, 2560, 256
+    rng = np.random.default_rng(42)
+    A = rng.integers(-4, 5, (M, K)).astype(np.float32)
+    B = rng.integers(-4, 5, (K, N)).astype(np.float32)
+    assert lib.tmm_check_device(stream) == _abi.TMM_OK      # clean slate
+    try:
+        assert lib.tmm_testing_set_wait_hooks(1, 2_000_000) == _abi.TMM_OK
+        _run("gemm_f32", A, B, check_canaries=False)
+        rc = lib.tmm_check_device(stream)
+        assert rc == _abi.TMM_ERR_DEVICE_TIMEOUT, rc
+        assert "ran out of time" in _abi.last_error()
+    finally:
+        lib.tmm_testing_set_wait_hooks(-1, 0)
+    # The status was cleared by the check and the context is usable.
+    assert lib.tmm_check_device(stream) == _abi.TMM_OK
+    C = _run("gemm_f32", A, B, check_canaries=False)
+    parity.assert_bit_exact(C, oracle.gemm(A, B), "after timeout")
+    assert lib.tmm_check_device(stream) == _abi.TMM_OK

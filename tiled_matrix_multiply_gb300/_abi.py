@@ -17,6 +17,7 @@ TMM_ERR_INVALID_ARG = -1
 TMM_ERR_ALIAS = -2
 TMM_ERR_UNSUPPORTED_DEVICE = -3
 TMM_ERR_CUDA = -4
+TMM_ERR_DEVICE_TIMEOUT = -5
 
 STATUS_NAMES = {
     TMM_OK: "TMM_OK",
@@ -24,13 +25,15 @@ STATUS_NAMES = {
     TMM_ERR_ALIAS: "TMM_ERR_ALIAS",
     TMM_ERR_UNSUPPORTED_DEVICE: "TMM_ERR_UNSUPPORTED_DEVICE",
     TMM_ERR_CUDA: "TMM_ERR_CUDA",
+    TMM_ERR_DEVICE_TIMEOUT: "TMM_ERR_DEVICE_TIMEOUT",
 }
 
 # Entry points with the common product signature
 # (M, N, K, A, lda, B, ldb, C, ldc, stream) -> int.
 GEMM_ENTRY_POINTS = ("gemm_f32", "gemm_f32_naive")
 # Every symbol include/tmm_gemm.h declares.
-EXPORTED = GEMM_ENTRY_POINTS + ("tmm_last_error_string", "tmm_version")
+EXPORTED = GEMM_ENTRY_POINTS + ("tmm_check_device", "tmm_testing_set_wait_hooks",
+                                 "tmm_last_error_string", "tmm_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +68,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = [i64, i64, i64, ptr, i64, ptr, i64, ptr, i64, ptr]
             fn.restype = ctypes.c_int
+        lib.tmm_check_device.argtypes = [ptr]
+        lib.tmm_check_device.restype = ctypes.c_int
+        lib.tmm_testing_set_wait_hooks.argtypes = [ctypes.c_int, i64]
+        lib.tmm_testing_set_wait_hooks.restype = ctypes.c_int
         lib.tmm_last_error_string.argtypes = []
         lib.tmm_last_error_string.restype = ctypes.c_char_p
         lib.tmm_version.argtypes = []

@@ -8,7 +8,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/tmm_gemm.h"
+#include "tmm_gemm.h"
 #include "tmm_internal.h"
 
 namespace {
@@ -156,6 +156,26 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const
 int gemm_f32_naive(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
                    int64_t ldb, float *C, int64_t ldc, tmm_stream_t stream) {
   return run("gemm_f32_naive", tmm::launch_naive, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+int tmm_check_device(tmm_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(TMM_ERR_CUDA, "tmm_check_device: cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  unsigned int status = 0;
+  e = tmm::simt_device_status(&status, true);
+  if (e != cudaSuccess)
+    return fail(TMM_ERR_CUDA, "tmm_check_device: status read: %s", cudaGetErrorString(e));
+  if (status & 1u)
+    return fail(TMM_ERR_DEVICE_TIMEOUT,
+                "tmm_check_device: a bounded wait inside gemm_f32 ran out of time; the "
+                "affected results are not valid");
+  return TMM_OK;
+}
+
+int tmm_testing_set_wait_hooks(int drop_signal_block, int64_t wait_limit_ns) {
+  tmm::simt_set_test_hooks(drop_signal_block, wait_limit_ns);
+  return TMM_OK;
 }
 
 const char *tmm_last_error_string(void) { return g_last_error; }

@@ -1,16 +1,16 @@
 // gemm_simt.cu -- two-level tiled FP32 product on the CUDA cores (FFMA).
 //
 // Tiling ("Tiling Strategies" sections 2-4, "CMU DLSys Lecture 12" section 5):
-//   * block tile: each 128-thread block (4 warps, 2 x 2) owns a 128 x 128 tile
-//     of C; two blocks are resident per SM;
-//   * K-slices of BK = 16 flow through a ring of kStages shared-memory stages
+//   * block tile: each block owns a BM x BN tile of C (128 x 128 with four
+//     warps in the default configuration; two blocks resident per SM);
+//   * K-slices of BK flow through a ring of kStages shared-memory stages
 //     filled by asynchronous copies (cp.async).  This generalises the double
 //     buffer of "Tiling Strategies" section 3: the copies of the next
 //     kStages - 1 slices are in flight while one slice is consumed, and no
 //     register holds staged data;
-//   * thread tile: each thread owns a 16 x 8 tile of C (128 accumulators) and
-//     performs one outer product per k, 16 + 8 operands for 128 FFMA, with the
-//     operands of step k+1 loaded from shared memory while step k's FFMAs
+//   * thread tile: each thread owns a TM x TN tile of C in registers and
+//     performs one outer product per k (TM + TN operands, TM*TN FFMA), with
+//     the operands of step k+1 loaded from shared memory while step k's FFMAs
 //     issue ("Tiling Hierarchy on GPUs", "Register Tiling", "Register
 //     prefetching", "Reducing Overhead Slots").
 //
@@ -19,51 +19,92 @@
 // copies, each warp copying 4 rows x 8 consecutive k (four 32-byte global
 // sectors) into 32 distinct banks (row length BM + 4 floats).  The B slab
 // keeps its global layout b[k][n] and is filled by 16-byte copies of whole
-// 512-byte row segments when B is 16-byte aligned (4-byte copies otherwise).
+// row segments when B is 16-byte aligned (4-byte copies otherwise).
 //
-// Warp tiling ("Tiling Hierarchy on GPUs", "Warp Tiling"): each warp covers a
-// 64 x 64 region of C; lane (lm, ln), lm in 0..3, ln in 0..7, owns rows
-// lm*4 + 16t + i and columns ln*4 + 32c + j (t < 4, c < 2, i, j < 4).  A
+// Warp tiling ("Tiling Hierarchy on GPUs", "Warp Tiling"): the 32 lanes of a
+// warp form an LM x LN grid (4 x 8 or 8 x 4); lane (lm, ln) owns rows
+// lm*4 + 4*LM*t + i and columns ln*4 + 4*LN*c + j of the warp's region.  A
 // 128-bit shared load is served at most 16 lanes per wavefront, and the two
 // quarter-warps of a half-warp share a wavefront only when they read disjoint
 // words with lanes that share a word paired up.  With quarter q = lane / 8,
-//     lm = lane % 2 + 2 (q % 2),
-//     ln = (lane / 2) % 4 + 4 ((q % 2) xor (q / 2)),
-// every fragment load, of A or of B, takes two wavefronts, the minimum.
+// the 4-valued coordinate is  lane % 2 + 2 (q % 2)  and the 8-valued one is
+// (lane / 2) % 4 + 4 ((q % 2) xor (q / 2)),  so every fragment load, of A or
+// of B, takes two wavefronts, the minimum.
 //
 // Tails ("CMU DLSys Lecture 12" section 5): copies outside M, N or K are
 // zero-filled (source size 0), which adds nothing to the sums, and only
 // entries inside M x N are stored.
 //
-// Scheduling: tiles are numbered along a grouped raster -- kGroupM tile-rows
+// Scheduling.  Tiles are numbered along a grouped raster -- kGroupM tile-rows
 // are walked column by column -- so blocks resident at the same time share
-// the A row-panels and B column-panels they read through L2.
+// the A row-panels and B column-panels they read through L2.  When the tile
+// count leaves a partial last wave, the kernel runs persistent (one block per
+// resident slot, launched cooperatively so that all are resident at once):
+// all but the last full wave of tiles are processed whole ("data-parallel"),
+// and the remaining tiles' K-slices are divided evenly among all blocks
+// ("stream-K").  Every block then does the same amount of work.  Each block's
+// share is at least one whole tile, so a split tile has exactly two
+// contributors: the block holding slices [x, S) stores its partial sums into
+// C and raises a flag; the block holding slices [0, x) -- which reaches the
+// tile last -- waits for the flag, adds the partial to its own sums and
+// stores the total.  The order of that addition is fixed, so results are
+// deterministic.  The wait is bounded: past the time limit the block records
+// a timeout in the device status word and finishes.
 #include <atomic>
+#include <cstdint>
 
 #include "tmm_internal.h"
 
 namespace tmm {
+
+// Flags of split tiles: kFlagRegions rings of kMaxPersistentBlocks words; a
+// call uses region epoch % kFlagRegions and raises flags to its epoch, so no
+// reset is needed between calls and calls in flight together use distinct
+// regions (up to kFlagRegions of them).
+constexpr int kFlagRegions = 16;
+constexpr int kMaxPersistentBlocks = 4096;
+__device__ unsigned int g_simt_flags[kFlagRegions * kMaxPersistentBlocks];
+// Device status word (bit 0: a stream-K wait ran out of time).
+__device__ unsigned int g_simt_status;
+
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int BK = 16;
-constexpr int kStages = 4;
-constexpr int TM = 16;                       // thread tile rows
-constexpr int TN = 8;                        // thread tile columns
-constexpr int kWarpsM = 2, kWarpsN = 2;
-constexpr int kThreads = 32 * kWarpsM * kWarpsN;  // 128
-constexpr int kAsLd = BM + 4;                // row of the transposed A slab (floats)
-constexpr int kBsLd = BN;
-constexpr int kStageFloats = BK * kAsLd + BK * kBsLd;
-constexpr int kSmemBytes = kStages * kStageFloats * 4;
 constexpr int kGroupM = 16;
-constexpr int kKUnroll = 4;                  // k steps per iteration of the inner loop
 
-static_assert(BM == kWarpsM * 4 * TM && BN == kWarpsN * 8 * TN, "warp tile is 4 x 8 lanes");
-static_assert(BM * BK == kThreads * 16, "each thread copies 16 elements of the A slab");
-static_assert(BK * BN == kThreads * 16, "each thread copies 16 elements of the B slab");
-static_assert(BK % kKUnroll == 0 && kKUnroll % 2 == 0, "inner loop ping-pongs fragments");
+template <int TM_, int TN_, int kWarpsM_, int kWarpsN_, int BK_, int kStages_, int kMinBlocks_>
+struct SimtConfig {
+  static constexpr int TM = TM_, TN = TN_;
+  static constexpr int kWarpsM = kWarpsM_, kWarpsN = kWarpsN_;
+  static constexpr int LM = (TM >= TN) ? 4 : 8;     // lane grid rows
+  static constexpr int LN = 32 / LM;                // lane grid columns
+  static constexpr int BM = kWarpsM * LM * TM;
+  static constexpr int BN = kWarpsN * LN * TN;
+  static constexpr int BK = BK_;
+  static constexpr int kStages = kStages_;
+  static constexpr int kThreads = 32 * kWarpsM * kWarpsN;
+  static constexpr int kWarps = kWarpsM * kWarpsN;
+  static constexpr int kMinBlocks = kMinBlocks_;
+  static constexpr int kAsLd = BM + 4;
+  static constexpr int kBsLd = BN;
+  static constexpr int kStageFloats = BK * kAsLd + BK * kBsLd;
+  static constexpr int kSmemBytes = kStages * kStageFloats * 4;
+  // A copies: groups of 4 rows x 8 k per warp instruction.
+  static constexpr int kARowGroups = BM / 4;
+  static constexpr int kARowGroupsPerWarp = kARowGroups / kWarps;
+  static constexpr int kACopies = kARowGroupsPerWarp * (BK / 8);
+  // B copies.
+  static constexpr int kBVecPerRow = BN / 4;
+  static constexpr int kBVecCopies = BK * BN / 4 / kThreads;
+  static constexpr int kBScalarCopies = BK * BN / kThreads;
+  static constexpr int kKUnroll = 4;
+
+  static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tiles are made of 4 x 4 quadrants");
+  static_assert(BK % 8 == 0 && BK % kKUnroll == 0, "slice depth");
+  static_assert(kARowGroups % kWarps == 0, "A copy groups divide among warps");
+  static_assert(kThreads % kBVecPerRow == 0, "B vector copies cover whole rows");
+  static_assert((BK * BN) % (4 * kThreads) == 0 && (BK * BN) % kThreads == 0, "B copies");
+  static_assert(BN % 32 == 0, "scalar B copies: a warp copies 32 consecutive columns");
+};
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -92,6 +133,37 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// Two FP32 values in one 64-bit register pair (lo = first).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// Two IEEE single-precision fused multiply-adds in one instruction: each half
+// is rounded once, exactly as fmaf; the pair costs one issue slot.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ unsigned int load_acquire(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void store_release(unsigned int *p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &tm,
                                             int &tn) {
   const int per_group = kGroupM * tiles_n;
@@ -103,201 +175,346 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
   tn = in_group / rows;
 }
 
-// kVecB:     B is 16-byte aligned and ldb, N are multiples of 4 (16-byte copies).
-// kVecStore: C is 16-byte aligned and ldc, N are multiples of 4.
-template <bool kVecB, bool kVecStore>
-__global__ void __launch_bounds__(kThreads, 2)
-gemm_simt_kernel(int M, int N, int K,
-                 const float *__restrict__ A, int64_t lda,
-                 const float *__restrict__ B, int64_t ldb,
-                 float *__restrict__ C, int64_t ldc, int tiles_m, int tiles_n) {
-  extern __shared__ __align__(16) float smem[];
+struct SimtParams {
+  int M, N, K;
+  const float *A;
+  int64_t lda;
+  const float *B;
+  int64_t ldb;
+  float *C;
+  int64_t ldc;
+  int tiles_m, tiles_n;
+  int slices;            // K-slices per tile
+  int dp_tiles;          // tiles [0, dp_tiles) are processed whole, striding by gridDim.x
+  int64_t sk_iters;      // (tiles - dp_tiles) * slices, divided evenly among the blocks
+  unsigned int epoch;    // this call's flag value (never 0)
+  int64_t wait_limit_ns; // bound on a stream-K wait
+  int drop_signal_block; // testing hook: this block never raises its flag (-1: none)
+};
 
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
+// One block's work on tile `tile`, K-slices [s_begin, s_end).
+template <class Cf, bool kVecB, bool kVecStore>
+struct SimtBlock {
+  // Accumulators in pairs along N: acc[i][jp] holds columns 2 jp (lo), 2 jp + 1 (hi).
+  uint64_t acc[Cf::TM][Cf::TN / 2];
+  int lane, warp, tid;
+  int a_off, b_off;
 
-  int tm, tn;
-  tile_coords(blockIdx.x, tiles_m, tiles_n, tm, tn);
-  const int m0 = tm * BM;
-  const int n0 = tn * BN;
-
-  // ---- copy assignment -------------------------------------------------------
-  // A: element `it` (0..15) of this thread is row a_r0 + 16 (it/2), k a_k0 + 8 (it%2).
-  const int a_r0 = (lane >> 3) + 4 * warp;
-  const int a_k0 = lane & 7;
-  uint32_t a_rows_ok = 0;                      // bit r: row a_r0 + 16 r inside M
-#pragma unroll
-  for (int r = 0; r < 8; ++r) a_rows_ok |= uint32_t(m0 + a_r0 + 16 * r < M) << r;
-  const float *a_src = A + int64_t(min(m0 + a_r0, M - 1)) * lda + a_k0;
-  const int64_t a_row_step = 16 * lda;
-  const uint32_t a_dst0 = smem_addr(smem) + 4u * (a_k0 * kAsLd + a_r0);
-
-  // B: vectorised, vector v (0..3) is k row b_k0 + 4v, columns b_n0..b_n0+3;
-  //    scalar, element it (0..15) is k row b_k0 + 4 (it/4), column lane + 32 (it%4).
-  const int b_k0 = tid >> 5;
-  const int b_n0 = kVecB ? (tid & 31) * 4 : lane;
-  const float *b_src = B + int64_t(b_k0) * ldb + min(n0 + b_n0, N - 1);
-  const int64_t b_row4_step = 4 * ldb;
-  const uint32_t b_dst0 = smem_addr(smem) + 4u * (BK * kAsLd + b_k0 * kBsLd + b_n0);
-
-  const int num_slices = (K + BK - 1) / BK;
-
-  auto issue_slice = [&](int s, int stage) {
-    const int k0 = s * BK;
-    const uint32_t st_off = 4u * stage * kStageFloats;
-    const float *a = a_src + k0;
-#pragma unroll
-    for (int it = 0; it < 16; ++it) {
-      const int r = it >> 1, h = it & 1;
-      const bool ok = ((a_rows_ok >> r) & 1u) && (k0 + a_k0 + 8 * h < K);
-      cp_async_4(a_dst0 + st_off + 4u * (8 * h * kAsLd + 16 * r), a + r * a_row_step + 8 * h,
-                 ok, A);
-    }
-    const float *b = b_src + int64_t(k0) * ldb;
-    if (kVecB) {
-      const bool col_ok = n0 + b_n0 < N;
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const bool ok = col_ok && (k0 + b_k0 + 4 * v < K);
-        cp_async_16(b_dst0 + st_off + 4u * (4 * v * kBsLd), b + v * b_row4_step, ok, B);
-      }
-    } else {
-#pragma unroll
-      for (int it = 0; it < 16; ++it) {
-        const int v = it >> 2, c = it & 3;
-        const bool ok = (n0 + b_n0 + 32 * c < N) && (k0 + b_k0 + 4 * v < K);
-        cp_async_4(b_dst0 + st_off + 4u * (4 * v * kBsLd + 32 * c), b + v * b_row4_step + 32 * c,
-                   ok, B);
-      }
-    }
-  };
-
-  // ---- fragment placement ----------------------------------------------------
-  const int q = lane >> 3;
-  const int lm = (lane & 1) + 2 * (q & 1);
-  const int ln = ((lane >> 1) & 3) + 4 * ((q & 1) ^ (q >> 1));
-  const int wm = warp / kWarpsN, wn = warp % kWarpsN;
-  const int a_off = wm * (4 * TM) + lm * 4;   // + 16 t
-  const int b_off = wn * (8 * TN) + ln * 4;   // + 32 c
-
-  float acc[TM][TN];
-#pragma unroll
-  for (int i = 0; i < TM; ++i)
-#pragma unroll
-    for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
-
-  auto load_frag = [&](const float *st, int k, float (&af)[TM], float (&bf)[TN]) {
-    const float *as = st + k * kAsLd + a_off;
-    const float *bs = st + BK * kAsLd + k * kBsLd + b_off;
-#pragma unroll
-    for (int t = 0; t < TM / 4; ++t) {
-      const float4 v = *reinterpret_cast<const float4 *>(as + 16 * t);
-      af[4 * t + 0] = v.x; af[4 * t + 1] = v.y; af[4 * t + 2] = v.z; af[4 * t + 3] = v.w;
-    }
-#pragma unroll
-    for (int c = 0; c < TN / 4; ++c) {
-      const float4 v = *reinterpret_cast<const float4 *>(bs + 32 * c);
-      bf[4 * c + 0] = v.x; bf[4 * c + 1] = v.y; bf[4 * c + 2] = v.z; bf[4 * c + 3] = v.w;
-    }
-  };
-  auto outer_product = [&](const float (&af)[TM], const float (&bf)[TN]) {
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-      for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(af[i], bf[j], acc[i][j]);
-  };
-
-  // ---- pipeline ----------------------------------------------------------------
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < num_slices) issue_slice(s, s);
-    cp_async_commit();
+  __device__ __forceinline__ void init_lanes() {
+    tid = threadIdx.x;
+    warp = tid >> 5;
+    lane = tid & 31;
+    const int q = lane >> 3;
+    const int four = (lane & 1) + 2 * (q & 1);
+    const int eight = ((lane >> 1) & 3) + 4 * ((q & 1) ^ (q >> 1));
+    const int lm = (Cf::LM == 4) ? four : eight;
+    const int ln = (Cf::LM == 4) ? eight : four;
+    const int wm = warp / Cf::kWarpsN, wn = warp % Cf::kWarpsN;
+    a_off = wm * (Cf::LM * Cf::TM) + lm * 4;
+    b_off = wn * (Cf::LN * Cf::TN) + ln * 4;
   }
 
-  float af[2][TM], bf[2][TN];
-  int stage = 0;
-  for (int s = 0; s < num_slices; ++s) {
-    cp_async_wait<kStages - 2>();   // slice s has landed (this thread's copies) ...
-    __syncthreads();                // ... and everyone's; slice s-1's stage is free
-    {
-      const int sn = s + kStages - 1;
-      int stage_n = stage + kStages - 1;
-      if (stage_n >= kStages) stage_n -= kStages;
-      if (sn < num_slices) issue_slice(sn, stage_n);
+  __device__ __forceinline__ void mainloop(const SimtParams &p, float *smem, int m0, int n0,
+                                           int s_begin, int s_end) {
+    constexpr int BK = Cf::BK, kAsLd = Cf::kAsLd, kBsLd = Cf::kBsLd;
+    constexpr int kStageFloats = Cf::kStageFloats, kStages = Cf::kStages;
+
+    // A copies: warp instruction (r, h) copies rows 4 (warp + kWarps r) + lane/8,
+    // k 8 h + lane % 8.
+    const int a_row = (lane >> 3) + 4 * warp;
+    const int a_k = lane & 7;
+    uint32_t a_rows_ok = 0;
+#pragma unroll
+    for (int r = 0; r < Cf::kARowGroupsPerWarp; ++r)
+      a_rows_ok |= uint32_t(m0 + a_row + 4 * Cf::kWarps * r < p.M) << r;
+    const float *a_src = p.A + int64_t(min(m0 + a_row, p.M - 1)) * p.lda + a_k;
+    const int64_t a_row_step = int64_t(4 * Cf::kWarps) * p.lda;
+    const uint32_t a_dst0 = smem_addr(smem) + 4u * (a_k * kAsLd + a_row);
+
+    // B copies: vector v is k row tid / (BN/4) + v * (threads / (BN/4)), columns 4 (tid % (BN/4));
+    // scalar it is k row warp + kWarps (it / (BN/32)), column lane + 32 (it % (BN/32)).
+    constexpr int kBRowsPerPass = Cf::kThreads / Cf::kBVecPerRow;
+    const int b_k = kVecB ? tid / Cf::kBVecPerRow : warp;
+    const int b_n = kVecB ? (tid % Cf::kBVecPerRow) * 4 : lane;
+    const float *b_src = p.B + int64_t(b_k) * p.ldb + min(n0 + b_n, p.N - 1);
+    const uint32_t b_dst0 = smem_addr(smem) + 4u * (BK * kAsLd + b_k * kBsLd + b_n);
+
+    auto issue_slice = [&](int s, int stage) {
+      const int k0 = s * BK;
+      const uint32_t st_off = 4u * stage * kStageFloats;
+      const float *a = a_src + k0;
+#pragma unroll
+      for (int it = 0; it < Cf::kACopies; ++it) {
+        const int r = it % Cf::kARowGroupsPerWarp, h = it / Cf::kARowGroupsPerWarp;
+        const bool ok = ((a_rows_ok >> r) & 1u) && (k0 + a_k + 8 * h < p.K);
+        cp_async_4(a_dst0 + st_off + 4u * (8 * h * kAsLd + 4 * Cf::kWarps * r),
+                   a + r * a_row_step + 8 * h, ok, p.A);
+      }
+      const float *b = b_src + int64_t(k0) * p.ldb;
+      if (kVecB) {
+        const bool col_ok = n0 + b_n < p.N;
+#pragma unroll
+        for (int v = 0; v < Cf::kBVecCopies; ++v) {
+          const int kr = b_k + kBRowsPerPass * v;
+          const bool ok = col_ok && (k0 + kr < p.K);
+          cp_async_16(b_dst0 + st_off + 4u * (kBRowsPerPass * v * kBsLd),
+                      b + int64_t(kBRowsPerPass * v) * p.ldb, ok, p.B);
+        }
+      } else {
+        constexpr int kColPasses = Cf::BN / 32;
+#pragma unroll
+        for (int it = 0; it < Cf::kBScalarCopies; ++it) {
+          const int kr = Cf::kWarps * (it / kColPasses), c = it % kColPasses;
+          const bool ok = (n0 + b_n + 32 * c < p.N) && (k0 + b_k + kr < p.K);
+          cp_async_4(b_dst0 + st_off + 4u * (kr * kBsLd + 32 * c),
+                     b + int64_t(kr) * p.ldb + 32 * c, ok, p.B);
+        }
+      }
+    };
+
+    auto load_frag = [&](const float *st, int k, float (&af)[Cf::TM],
+                         uint64_t (&bf)[Cf::TN / 2]) {
+      const float *as = st + k * kAsLd + a_off;
+      const float *bs = st + BK * kAsLd + k * kBsLd + b_off;
+#pragma unroll
+      for (int t = 0; t < Cf::TM / 4; ++t) {
+        const float4 v = *reinterpret_cast<const float4 *>(as + 4 * Cf::LM * t);
+        af[4 * t + 0] = v.x; af[4 * t + 1] = v.y; af[4 * t + 2] = v.z; af[4 * t + 3] = v.w;
+      }
+#pragma unroll
+      for (int c = 0; c < Cf::TN / 4; ++c) {
+        const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(bs + 4 * Cf::LN * c);
+        bf[2 * c + 0] = v.x; bf[2 * c + 1] = v.y;
+      }
+    };
+
+#pragma unroll
+    for (int i = 0; i < Cf::TM; ++i)
+#pragma unroll
+      for (int j = 0; j < Cf::TN / 2; ++j) acc[i][j] = 0;   // +0.0f in both halves
+
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+      if (s_begin + s < s_end) issue_slice(s_begin + s, s);
       cp_async_commit();
     }
-    const float *st = smem + stage * kStageFloats;
-    load_frag(st, 0, af[0], bf[0]);
-#pragma unroll 1
-    for (int kk = 0; kk < BK; kk += kKUnroll) {
-#pragma unroll
-      for (int u = 0; u < kKUnroll; ++u) {
-        const int k = kk + u;
-        if (u + 1 < kKUnroll || k + 1 < BK) load_frag(st, k + 1, af[(u + 1) & 1], bf[(u + 1) & 1]);
-        outer_product(af[u & 1], bf[u & 1]);
-      }
-    }
-    if (++stage == kStages) stage = 0;
-  }
-  cp_async_wait<0>();
 
-  // ---- epilogue: accumulator (4t + i, 4c + j) is C[m0 + a_off + 16t + i][n0 + b_off + 32c + j]
-  const int row0 = m0 + a_off;
-  const int col0 = n0 + b_off;
-  float *c_base = C + int64_t(row0) * ldc + col0;
+    float af[2][Cf::TM];
+    uint64_t bf[2][Cf::TN / 2];
+    int stage = 0;
+    for (int s = s_begin; s < s_end; ++s) {
+      cp_async_wait<kStages - 2>();   // slice s has landed (this thread's copies) ...
+      __syncthreads();                // ... and everyone's; slice s-1's stage is free
+      {
+        const int sn = s + kStages - 1;
+        int stage_n = stage + kStages - 1;
+        if (stage_n >= kStages) stage_n -= kStages;
+        if (sn < s_end) issue_slice(sn, stage_n);
+        cp_async_commit();
+      }
+      const float *st = smem + stage * kStageFloats;
+      load_frag(st, 0, af[0], bf[0]);
+#pragma unroll 1
+      for (int kk = 0; kk < BK; kk += Cf::kKUnroll) {
 #pragma unroll
-  for (int t = 0; t < TM / 4; ++t) {
+        for (int u = 0; u < Cf::kKUnroll; ++u) {
+          const int k = kk + u;
+          if (u + 1 < Cf::kKUnroll || k + 1 < BK)
+            load_frag(st, k + 1, af[(u + 1) & 1], bf[(u + 1) & 1]);
+          // Outer product: acc[i][j] += a[i] * b[j], two columns per instruction.
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int dr = 16 * t + i;
-      if (row0 + dr >= M) continue;
-      float *c_row = c_base + int64_t(dr) * ldc;
-      const float *a = acc[4 * t + i];
+          for (int i = 0; i < Cf::TM; ++i) {
+            const uint64_t ai = pack2(af[u & 1][i], af[u & 1][i]);
 #pragma unroll
-      for (int c = 0; c < TN / 4; ++c) {
-        const int dc = 32 * c;
-        if (kVecStore) {
-          if (col0 + dc < N)
-            *reinterpret_cast<float4 *>(c_row + dc) =
-                make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
-        } else {
+            for (int j = 0; j < Cf::TN / 2; ++j) acc[i][j] = ffma2(ai, bf[u & 1][j], acc[i][j]);
+          }
+        }
+      }
+      if (++stage == kStages) stage = 0;
+    }
+    cp_async_wait<0>();
+    __syncthreads();   // the next tile's copies may overwrite any stage
+  }
+
+  // Accumulator (4t + i, 4c + j) is C[m0 + a_off + 4 LM t + i][n0 + b_off + 4 LN c + j].
+  // kAdd: add the partial sums already in C (loaded through L2) before storing.
+  template <bool kAdd>
+  __device__ __forceinline__ void epilogue(const SimtParams &p, int m0, int n0) {
+    const int row0 = m0 + a_off;
+    const int col0 = n0 + b_off;
+    float *c_base = p.C + int64_t(row0) * p.ldc + col0;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (col0 + dc + j < N) c_row[dc + j] = a[4 * c + j];
+    for (int t = 0; t < Cf::TM / 4; ++t) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int dr = 4 * Cf::LM * t + i;
+        if (row0 + dr >= p.M) continue;
+        float *c_row = c_base + int64_t(dr) * p.ldc;
+        float a[Cf::TN];
+#pragma unroll
+        for (int j = 0; j < Cf::TN / 2; ++j) unpack2(acc[4 * t + i][j], a[2 * j], a[2 * j + 1]);
+#pragma unroll
+        for (int c = 0; c < Cf::TN / 4; ++c) {
+          const int dc = 4 * Cf::LN * c;
+          if (kVecStore) {
+            if (col0 + dc < p.N) {
+              float4 v = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+              if (kAdd) {
+                const float4 w = __ldcg(reinterpret_cast<const float4 *>(c_row + dc));
+                v.x = w.x + v.x; v.y = w.y + v.y; v.z = w.z + v.z; v.w = w.w + v.w;
+              }
+              *reinterpret_cast<float4 *>(c_row + dc) = v;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (col0 + dc + j < p.N) {
+                float v = a[4 * c + j];
+                if (kAdd) v = __ldcg(c_row + dc + j) + v;
+                c_row[dc + j] = v;
+              }
+          }
         }
       }
     }
   }
+};
+
+template <class Cf, bool kVecB, bool kVecStore>
+__global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
+gemm_simt_kernel(const SimtParams p) {
+  extern __shared__ __align__(16) float smem[];
+  SimtBlock<Cf, kVecB, kVecStore> blk;
+  blk.init_lanes();
+
+  // Whole tiles.
+  for (int tile = blockIdx.x; tile < p.dp_tiles; tile += gridDim.x) {
+    int tm, tn;
+    tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+    blk.mainloop(p, smem, tm * Cf::BM, tn * Cf::BN, 0, p.slices);
+    blk.template epilogue<false>(p, tm * Cf::BM, tn * Cf::BN);
+  }
+  if (p.sk_iters == 0) return;
+
+  // This block's share of the split tiles' K-slices.
+  const int64_t g = gridDim.x, b = blockIdx.x;
+  const int64_t it_end = (b + 1) * p.sk_iters / g;
+  unsigned int *flags = g_simt_flags + (p.epoch % kFlagRegions) * kMaxPersistentBlocks;
+  for (int64_t it = b * p.sk_iters / g; it < it_end;) {
+    const int tile = p.dp_tiles + int(it / p.slices);
+    const int s_begin = int(it % p.slices);
+    const int64_t rest = it_end - it;
+    const int s_end = rest < int64_t(p.slices - s_begin) ? s_begin + int(rest) : p.slices;
+    int tm, tn;
+    tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+    const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
+    blk.mainloop(p, smem, m0, n0, s_begin, s_end);
+    if (s_begin == 0 && s_end == p.slices) {
+      blk.template epilogue<false>(p, m0, n0);
+    } else if (s_begin > 0) {
+      // Slices [s_begin, S): store the partial sums, then raise this block's flag.
+      blk.template epilogue<false>(p, m0, n0);
+      __syncthreads();
+      if (threadIdx.x == 0 && int(b) != p.drop_signal_block) {
+        __threadfence();
+        store_release(&flags[b], p.epoch);
+      }
+    } else {
+      // Slices [0, s_end): the next block holds [s_end, S); wait for its partial.
+      if (threadIdx.x == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (load_acquire(&flags[b + 1]) != p.epoch) {
+          if (int64_t(global_timer_ns() - t0) > p.wait_limit_ns) {
+            atomicOr(&g_simt_status, 1u);
+            break;
+          }
+          __nanosleep(128);
+        }
+      }
+      __syncthreads();
+      blk.template epilogue<true>(p, m0, n0);
+    }
+    it += s_end - s_begin;
+  }
 }
 
-// Dynamic shared memory above 48 KiB needs an opt-in per kernel and device.
-std::atomic<uint64_t> g_smem_configured[4];
+// ---- host side ------------------------------------------------------------------
 
-template <bool kVecB, bool kVecStore>
+using DefaultConfig = SimtConfig<8, 16, 2, 2, 16, 4, 2>;
+
+struct LaunchState {
+  std::atomic<uint64_t> configured{0};   // bit per device: smem opt-in done
+  std::atomic<int> blocks_per_sm[64];
+};
+
+std::atomic<unsigned int> g_epoch{0};
+std::atomic<int64_t> g_wait_limit_ns{int64_t(10) * 1000 * 1000 * 1000};
+std::atomic<int> g_drop_signal_block{-1};
+
+template <class Cf, bool kVecB, bool kVecStore>
 cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
-  auto kernel = gemm_simt_kernel<kVecB, kVecStore>;
-  const int variant = (kVecB ? 2 : 0) + (kVecStore ? 1 : 0);
+  static LaunchState state;
+  auto kernel = gemm_simt_kernel<Cf, kVecB, kVecStore>;
   const uint64_t bit = uint64_t(1) << (dev.id & 63);
-  if (!(g_smem_configured[variant].load(std::memory_order_acquire) & bit)) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (!(state.configured.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cf::kSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    g_smem_configured[variant].fetch_or(bit, std::memory_order_release);
+    int nb = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, Cf::kThreads, Cf::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    state.blocks_per_sm[dev.id & 63].store(nb, std::memory_order_relaxed);
+    state.configured.fetch_or(bit, std::memory_order_release);
   }
-  const int64_t tiles_m = (p.M + BM - 1) / BM;
-  const int64_t tiles_n = (p.N + BN - 1) / BN;
-  if (tiles_m * tiles_n > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  const int blocks_per_sm = state.blocks_per_sm[dev.id & 63].load(std::memory_order_relaxed);
+
+  const int64_t tiles_m = (p.M + Cf::BM - 1) / Cf::BM;
+  const int64_t tiles_n = (p.N + Cf::BN - 1) / Cf::BN;
+  const int64_t tiles = tiles_m * tiles_n;
+  if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  const int slices = int((p.K + Cf::BK - 1) / Cf::BK);
+
+  SimtParams prm = {};
+  prm.M = int(p.M); prm.N = int(p.N); prm.K = int(p.K);
+  prm.A = p.A; prm.lda = p.lda; prm.B = p.B; prm.ldb = p.ldb; prm.C = p.C; prm.ldc = p.ldc;
+  prm.tiles_m = int(tiles_m); prm.tiles_n = int(tiles_n);
+  prm.slices = slices;
+  prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  prm.drop_signal_block = g_drop_signal_block.load(std::memory_order_relaxed);
+
+  // Stream-K when the last wave would be partly empty: one block per resident
+  // slot, the last full wave plus the remainder split over K.
+  const int64_t slots = int64_t(blocks_per_sm) * dev.sm_count;
+  const int64_t rem = slots > 0 ? tiles % slots : 0;
+  const bool stream_k = slots > 0 && slots <= kMaxPersistentBlocks && tiles > slots &&
+                        rem != 0 && rem * 10 < slots * 9 && slices >= 4;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(tiles_m * tiles_n), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(Cf::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cf::kSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kernel, int(p.M), int(p.N), int(p.K), p.A, p.lda, p.B, p.ldb,
-                            p.C, p.ldc, int(tiles_m), int(tiles_n));
+  if (stream_k) {
+    const int64_t sk_tiles = rem + slots;
+    prm.dp_tiles = int(tiles - sk_tiles);
+    prm.sk_iters = sk_tiles * slices;
+    unsigned int e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    prm.epoch = e;
+    cfg.gridDim = dim3(unsigned(slots), 1, 1);
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  } else {
+    prm.dp_tiles = int(tiles);
+    prm.sk_iters = 0;
+    prm.epoch = 0;
+    cfg.gridDim = dim3(unsigned(tiles), 1, 1);
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, prm);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -305,13 +522,27 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 
 cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
+  using Cf = DefaultConfig;
   const bool vec_b = aligned16(p.B) && p.ldb % 4 == 0 && p.N % 4 == 0;
   const bool vec_store = aligned16(p.C) && p.ldc % 4 == 0 && p.N % 4 == 0;
   if (vec_b)
-    return vec_store ? launch_variant<true, true>(p, dev, stream)
-                     : launch_variant<true, false>(p, dev, stream);
-  return vec_store ? launch_variant<false, true>(p, dev, stream)
-                   : launch_variant<false, false>(p, dev, stream);
+    return vec_store ? launch_variant<Cf, true, true>(p, dev, stream)
+                     : launch_variant<Cf, true, false>(p, dev, stream);
+  return vec_store ? launch_variant<Cf, false, true>(p, dev, stream)
+                   : launch_variant<Cf, false, false>(p, dev, stream);
+}
+
+cudaError_t simt_device_status(unsigned int *status, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, g_simt_status, sizeof(unsigned int));
+  if (e != cudaSuccess || !clear) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_simt_status, &zero, sizeof(unsigned int));
+}
+
+void simt_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns) {
+  g_drop_signal_block.store(drop_signal_block, std::memory_order_relaxed);
+  g_wait_limit_ns.store(wait_limit_ns > 0 ? wait_limit_ns : int64_t(10) * 1000 * 1000 * 1000,
+                        std::memory_order_relaxed);
 }
 
 }  // namespace tmm

@@ -31,4 +31,10 @@ struct DeviceInfo {
 cudaError_t launch_naive(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream);
 cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream);
 
+// Device status word of the tiled kernel (bit 0: a bounded wait ran out of
+// time); read from the current device, optionally cleared.
+cudaError_t simt_device_status(unsigned int *status, bool clear);
+// Testing hooks of the tiled kernel's stream-K waits (see tmm_gemm.h).
+void simt_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns);
+
 }  // namespace tmm
