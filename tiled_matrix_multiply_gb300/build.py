@@ -43,11 +43,19 @@ def _inputs():
     return files
 
 
-def source_digest() -> str:
-    """SHA-256 over the CUDA/C++ sources and headers (identifies a kernel build)."""
+def source_digest(names: list[str] | None = None) -> str:
+    """SHA-256 over CUDA/C++ sources (default: all sources and headers).
+
+    ``names`` restricts it to the given files of ``csrc/`` -- the files one
+    kernel is built from -- so a recorded measurement of that kernel stays
+    valid while other kernels change.
+    """
     import hashlib
     h = hashlib.sha256()
-    files = sorted(f for f in _inputs() if not f.endswith(".py"))
+    if names:
+        files = sorted(os.path.join(CSRC, n) for n in names)
+    else:
+        files = sorted(f for f in _inputs() if not f.endswith(".py"))
     for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:

@@ -96,7 +96,7 @@ struct SimtConfig {
   static constexpr int kBVecPerRow = BN / 4;
   static constexpr int kBVecCopies = BK * BN / 4 / kThreads;
   static constexpr int kBScalarCopies = BK * BN / kThreads;
-  static constexpr int kKUnroll = 4;
+  static constexpr int kKUnroll = BK;   // the whole slice unrolled (fits the instruction cache)
 
   static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tiles are made of 4 x 4 quadrants");
   static_assert(BK % 8 == 0 && BK % kKUnroll == 0, "slice depth");
@@ -440,7 +440,7 @@ gemm_simt_kernel(const SimtParams p) {
 
 // ---- host side ------------------------------------------------------------------
 
-using DefaultConfig = SimtConfig<8, 16, 2, 2, 16, 4, 2>;
+using DefaultConfig = SimtConfig<8, 16, 1, 4, 16, 4, 2>;
 
 struct LaunchState {
   std::atomic<uint64_t> configured{0};   // bit per device: smem opt-in done
