@@ -364,6 +364,8 @@ def run_ours(args, world, rank, local):
                                            if clocks.get("sm_mhz") else None)}
 
     extra = {}
+    if not args.no_tc3 and rank == 0:
+        extra["tc3"] = tc3_leg(args, w, A, B, C, flush, stream, peaks)
     if not args.no_contrast and rank == 0:
         extra["contrast"] = contrast_paths(args, w, A, B, C, flush, stream, props, peaks)
 
@@ -389,6 +391,48 @@ def run_ours(args, world, rank, local):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+TF32_PER_BF16 = 1.1 / 2.25       # nominal dense TF32 / BF16 tensor rates of the part
+
+
+def tc3_leg(args, w, A, B, C, flush, stream, peaks) -> dict:
+    """gemm_f32_tc3 on the same workload: three TF32 tensor-core products per
+    output term; reported as effective FP32 TFLOP/s and against the TF32 pipe."""
+    import torch
+    from tiled_matrix_multiply_gb300 import _abi
+    lib = _abi.load()
+    need = int(lib.gemm_f32_tc3_workspace_size(w.M, w.N, w.K))
+    ws = torch.empty(need + 256, dtype=torch.uint8, device=A.device)
+    wptr = (ws.data_ptr() + 255) // 256 * 256
+    launches = {"n": 0}
+
+    def step():
+        rc = lib.gemm_f32_tc3(w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N, C.data_ptr(),
+                              w.N, wptr, need, stream.cuda_stream)
+        if rc != _abi.TMM_OK:
+            raise _abi.TmmError("gemm_f32_tc3", rc, _abi.last_error())
+        launches["n"] += 3   # split of A, split of B, product kernel
+
+    steps = max(3, min(args.steps, 200))
+    times = time_device(step, flush, steps, args.warmup, stream, None)
+    if lib.tmm_check_device(stream.cuda_stream) != _abi.TMM_OK:
+        raise _abi.TmmError("tmm_check_device", _abi.TMM_ERR_DEVICE_TIMEOUT, _abi.last_error())
+    ms = statistics.mean(times)
+    bf16 = peaks.get("bf16_tflops")
+    peak = bf16 * TF32_PER_BF16 if bf16 else 1900.0 * TF32_PER_BF16
+    tensor_tflops = 3 * w.flops / (ms / 1e3) / 1e12
+    return {"path": "gemm_f32_tc3 (tcgen05, 3 x TF32 split products, FP32 accumulation)",
+            "value": w.flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "steps": steps, "gpu_launches": launches["n"] - 3 * args.warmup,
+            "workspace_bytes": need,
+            "roofline": {"bound": "tensor", "achieved": tensor_tflops, "peak": peak, "unit": UNIT,
+                         "frac": tensor_tflops / peak, "traffic": None,
+                         "peak_source": ("MEASURED_PEAKS.json bf16_tflops x 1.1/2.25 (nominal "
+                                         "TF32/BF16 dense ratio)" if bf16 else
+                                         "fallback 1.9 PFLOP/s bf16 x 1.1/2.25"),
+                         "algorithmic": f"3 x 2MNK = {3 * w.flops:.4e} tensor FLOP per step "
+                                        "(split pre-pass included in the step time)"}}
 
 
 def contrast_paths(args, w, A, B, C, flush, stream, props, peaks) -> dict:
@@ -417,6 +461,7 @@ def main(argv=None):
                     help="oracle CPU-baseline budget; 0 skips the CPU baseline")
     ap.add_argument("--no-contrast", action="store_true", help="skip the naive-kernel contrast")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-tc3", action="store_true", help="skip the tensor-core (3xTF32) leg")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps, always
     world, rank, local = dist_env()

@@ -112,11 +112,43 @@ int gemm_f32_naive(int64_t M, int64_t N, int64_t K,
                    tmm_stream_t stream);
 
 /*
+ * gemm_f32_tc3 -- the same product on the tcgen05 tensor cores, with each FP32
+ * operand split into two TF32 values, x = hi + lo (hi: x with its low 13
+ * mantissa bits cleared; lo: the exact remainder rounded to TF32), and
+ *     A B ~ A_hi B_hi + A_hi B_lo + A_lo B_hi
+ * accumulated in FP32 tensor memory (the dropped A_lo B_lo term is about
+ * 2^-22 of each product).  The pages do not go beyond FP32 FMA units ("CMU
+ * DLSys Lecture 12" section 6 notes that tensor instructions change the
+ * implementation); the tiling is that of section 5 with the register tile
+ * replaced by a tensor-memory accumulator.  Same contract as gemm_f32, plus:
+ *   workspace        DEVICE pointer, 256-byte aligned, caller-owned, at least
+ *                    gemm_f32_tc3_workspace_size(M, N, K) bytes; holds the
+ *                    split operands (its contents are scratch, not preserved);
+ *                    it must not overlap A, B or C.
+ *   workspace_bytes  its size.
+ * TMM_ERR_INVALID_ARG if the workspace is missing, short or misaligned,
+ * TMM_ERR_ALIAS if it overlaps an operand.  Calls sharing one workspace must
+ * not overlap on the GPU.
+ */
+int gemm_f32_tc3(int64_t M, int64_t N, int64_t K,
+                 const float *A, int64_t lda,
+                 const float *B, int64_t ldb,
+                 float *C, int64_t ldc,
+                 void *workspace, size_t workspace_bytes,
+                 tmm_stream_t stream);
+
+/* Workspace bytes gemm_f32_tc3 needs for an M x N x K product (0 for an empty
+ * product or sizes out of range):  4 Kp (2M + 2N) rounded to 256-byte
+ * sections, Kp = K rounded up to a multiple of 32. */
+size_t gemm_f32_tc3_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
  * tmm_check_device -- synchronise `stream`, then read and clear the current
  * device's status word.  Returns TMM_OK, or TMM_ERR_DEVICE_TIMEOUT when a
  * bounded wait inside gemm_f32 (between the two blocks sharing a split tile)
- * ran out of time since the last check; results written since then are not
- * valid.  The pages have no counterpart: this is the library's failure
+ * or gemm_f32_tc3 (between the copy, tensor-core and epilogue roles of a
+ * block) ran out of time since the last check; results written since then are
+ * not valid.  The pages have no counterpart: this is the library's failure
  * detection ("CMU DLSys Lecture 12" section 2 only asks that API and launch
  * errors be checked).  TMM_ERR_CUDA if the synchronisation itself failed.
  */
@@ -126,7 +158,8 @@ int tmm_check_device(tmm_stream_t stream);
  * tmm_testing_set_wait_hooks -- testing only; no counterpart in the pages.
  * drop_signal_block >= 0 makes that block of later stream-K launches skip
  * raising its flag, so the block waiting on it runs into the time limit;
- * wait_limit_ns > 0 sets that limit (default, and for values <= 0, 10 s).
+ * wait_limit_ns > 0 sets the limit of every bounded wait of both kernels
+ * (default, and for values <= 0, 10 s).
  * Process-wide; pass (-1, 0) to restore the defaults.  Always TMM_OK.
  */
 int tmm_testing_set_wait_hooks(int drop_signal_block, int64_t wait_limit_ns);

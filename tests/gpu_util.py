@@ -51,7 +51,8 @@ class DevMatrix:
 
 
 def run_entry(entry: str, A: np.ndarray, B: np.ndarray, *, lda=None, ldb=None, ldc=None,
-              a_off=0, b_off=0, c_off=0, stream=None, check_canaries=True) -> np.ndarray:
+              a_off=0, b_off=0, c_off=0, stream=None, check_canaries=True,
+              check_status=True) -> np.ndarray:
     """C = A x B through the C ABI on device buffers laid out as requested."""
     M, K = A.shape
     K2, N = B.shape
@@ -60,9 +61,20 @@ def run_entry(entry: str, A: np.ndarray, B: np.ndarray, *, lda=None, ldb=None, l
     dB = DevMatrix(B, K, N, ldb, b_off)
     dC = DevMatrix(None, M, N, ldc, c_off)
     s = stream if stream is not None else torch.cuda.current_stream()
-    rc = _abi.call(entry, M, N, K, dA.ptr, dA.ld, dB.ptr, dB.ld, dC.ptr, dC.ld, s.cuda_stream)
+    if entry == "gemm_f32_tc3":
+        lib = _abi.load()
+        need = int(lib.gemm_f32_tc3_workspace_size(M, N, K))
+        ws = torch.empty(max(need, 1) + 256, dtype=torch.uint8, device=dC.buf.device)
+        wptr = (ws.data_ptr() + 255) // 256 * 256
+        rc = lib.gemm_f32_tc3(M, N, K, dA.ptr, dA.ld, dB.ptr, dB.ld, dC.ptr, dC.ld, wptr, need,
+                              s.cuda_stream)
+    else:
+        rc = _abi.call(entry, M, N, K, dA.ptr, dA.ld, dB.ptr, dB.ld, dC.ptr, dC.ld,
+                       s.cuda_stream)
     assert rc == _abi.TMM_OK, f"{entry} returned {rc}: {_abi.last_error()}"
     torch.cuda.synchronize()
+    if check_status:
+        assert _abi.load().tmm_check_device(s.cuda_stream) == _abi.TMM_OK, _abi.last_error()
     if check_canaries:
         assert dC.outside_window_untouched(), f"{entry} wrote outside C's M x N window"
     return dC.window()

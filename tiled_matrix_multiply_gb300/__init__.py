@@ -8,7 +8,9 @@ memory and streams only.
     C = tmm.gemm_f32(A, B)            # A: (M, K), B: (K, N) float32 CUDA tensors
 
 ``gemm_f32`` is the tiled FFMA path; ``gemm_f32_naive`` is the
-one-output-per-thread contrast kernel.  Both are asynchronous on the current
+one-output-per-thread contrast kernel; ``gemm_f32_tc3`` runs the product on the
+tensor cores with split-TF32 operands (it needs a workspace, allocated here
+through torch unless one is passed).  All are asynchronous on the current
 torch stream of the operands' device.
 """
 from __future__ import annotations
@@ -16,7 +18,8 @@ from __future__ import annotations
 from ._abi import (TMM_ERR_ALIAS, TMM_ERR_CUDA, TMM_ERR_INVALID_ARG,  # noqa: F401
                    TMM_ERR_UNSUPPORTED_DEVICE, TMM_OK, TmmError)
 
-__all__ = ["gemm_f32", "gemm_f32_naive", "raw_call", "TmmError"]
+__all__ = ["gemm_f32", "gemm_f32_naive", "gemm_f32_tc3", "tc3_workspace_bytes",
+           "check_device", "raw_call", "TmmError"]
 
 
 def _matrix(x, name):
@@ -67,6 +70,56 @@ def gemm_f32(A, B, C=None, stream=None):
 def gemm_f32_naive(A, B, C=None, stream=None):
     """C = A x B, one output per thread, operands from global memory."""
     return _product("gemm_f32_naive", A, B, C, stream)
+
+
+def tc3_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Bytes of workspace gemm_f32_tc3 needs for an M x N x K product."""
+    from . import _abi
+    return int(_abi.load().gemm_f32_tc3_workspace_size(M, N, K))
+
+
+def gemm_f32_tc3(A, B, C=None, workspace=None, stream=None):
+    """C = A x B on the tensor cores (3 x TF32 split products, FP32 accumulation).
+
+    ``workspace``: a CUDA tensor of at least ``tc3_workspace_bytes(M, N, K)``
+    bytes whose storage starts 256-byte aligned (torch allocations do); one is
+    allocated when not given.
+    """
+    import torch
+    from . import _abi
+    M, K, lda = _matrix(A, "A")
+    K2, N, ldb = _matrix(B, "B")
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+    if A.device != B.device:
+        raise ValueError("A and B are on different devices")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    elif C.shape != (M, N) or C.device != A.device:
+        raise ValueError(f"C must be ({M}, {N}) on {A.device}")
+    _, _, ldc = _matrix(C, "C")
+    need = tc3_workspace_bytes(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(A.device):
+        s = stream if stream is not None else torch.cuda.current_stream(A.device)
+        rc = _abi.load().gemm_f32_tc3(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
+                                      C.data_ptr(), ldc, workspace.data_ptr(), ws_bytes,
+                                      s.cuda_stream)
+        if rc != _abi.TMM_OK:
+            raise _abi.TmmError("gemm_f32_tc3", rc, _abi.last_error())
+    return C
+
+
+def check_device(stream=None) -> None:
+    """Synchronise the stream and raise TmmError if a bounded wait in a kernel ran out."""
+    import torch
+    from . import _abi
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = _abi.load().tmm_check_device(s.cuda_stream)
+    if rc != _abi.TMM_OK:
+        raise _abi.TmmError("tmm_check_device", rc, _abi.last_error())
 
 
 def raw_call(entry: str, M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, stream_ptr=0) -> int:

@@ -32,7 +32,8 @@ STATUS_NAMES = {
 # (M, N, K, A, lda, B, ldb, C, ldc, stream) -> int.
 GEMM_ENTRY_POINTS = ("gemm_f32", "gemm_f32_naive")
 # Every symbol include/tmm_gemm.h declares.
-EXPORTED = GEMM_ENTRY_POINTS + ("tmm_check_device", "tmm_testing_set_wait_hooks",
+EXPORTED = GEMM_ENTRY_POINTS + ("gemm_f32_tc3", "gemm_f32_tc3_workspace_size",
+                                 "tmm_check_device", "tmm_testing_set_wait_hooks",
                                  "tmm_last_error_string", "tmm_version")
 
 _lock = threading.Lock()
@@ -68,6 +69,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = [i64, i64, i64, ptr, i64, ptr, i64, ptr, i64, ptr]
             fn.restype = ctypes.c_int
+        lib.gemm_f32_tc3.argtypes = [i64, i64, i64, ptr, i64, ptr, i64, ptr, i64, ptr,
+                                     ctypes.c_size_t, ptr]
+        lib.gemm_f32_tc3.restype = ctypes.c_int
+        lib.gemm_f32_tc3_workspace_size.argtypes = [i64, i64, i64]
+        lib.gemm_f32_tc3_workspace_size.restype = ctypes.c_size_t
         lib.tmm_check_device.argtypes = [ptr]
         lib.tmm_check_device.restype = ctypes.c_int
         lib.tmm_testing_set_wait_hooks.argtypes = [ctypes.c_int, i64]

@@ -162,19 +162,66 @@ int tmm_check_device(tmm_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return fail(TMM_ERR_CUDA, "tmm_check_device: cudaStreamSynchronize: %s", cudaGetErrorString(e));
-  unsigned int status = 0;
-  e = tmm::simt_device_status(&status, true);
+  unsigned int simt = 0, tc3 = 0;
+  e = tmm::simt_device_status(&simt, true);
+  if (e == cudaSuccess) e = tmm::tc3_device_status(&tc3, true);
   if (e != cudaSuccess)
     return fail(TMM_ERR_CUDA, "tmm_check_device: status read: %s", cudaGetErrorString(e));
-  if (status & 1u)
+  if (simt | tc3)
     return fail(TMM_ERR_DEVICE_TIMEOUT,
-                "tmm_check_device: a bounded wait inside gemm_f32 ran out of time; the "
-                "affected results are not valid");
+                "tmm_check_device: a bounded wait inside %s ran out of time; the affected "
+                "results are not valid",
+                simt ? "gemm_f32" : "gemm_f32_tc3");
   return TMM_OK;
 }
 
 int tmm_testing_set_wait_hooks(int drop_signal_block, int64_t wait_limit_ns) {
   tmm::simt_set_test_hooks(drop_signal_block, wait_limit_ns);
+  tmm::tc3_set_wait_limit(wait_limit_ns);
+  return TMM_OK;
+}
+
+size_t gemm_f32_tc3_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return 0;
+  return tmm::tc3_workspace_bytes(M, N, K);
+}
+
+int gemm_f32_tc3(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                 int64_t ldb, float *C, int64_t ldc, void *workspace, size_t workspace_bytes,
+                 tmm_stream_t stream) {
+  const char *who = "gemm_f32_tc3";
+  bool noop = false;
+  int rc = check_args(who, M, N, K, A, lda, B, ldb, C, ldc, &noop);
+  if (rc != TMM_OK || noop) return rc;
+  tmm::DeviceInfo dev;
+  if ((rc = current_device(&dev)) != TMM_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    cudaError_t e = cudaMemset2DAsync(C, size_t(ldc) * sizeof(float), 0,
+                                      size_t(N) * sizeof(float), size_t(M), s);
+    if (e != cudaSuccess)
+      return fail(TMM_ERR_CUDA, "%s: cudaMemset2DAsync: %s", who, cudaGetErrorString(e));
+    return TMM_OK;
+  }
+  const size_t need = tmm::tc3_workspace_bytes(M, N, K);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(TMM_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", who, need,
+                workspace == nullptr ? size_t(0) : workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(TMM_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  {
+    uintptr_t c_lo, c_hi, a_lo, a_hi, b_lo, b_hi;
+    byte_span(C, M, ldc, N, &c_lo, &c_hi);
+    byte_span(A, M, lda, K, &a_lo, &a_hi);
+    byte_span(B, K, ldb, N, &b_lo, &b_hi);
+    const uintptr_t w_lo = reinterpret_cast<uintptr_t>(workspace), w_hi = w_lo + need;
+    if (overlaps(w_lo, w_hi, c_lo, c_hi) || overlaps(w_lo, w_hi, a_lo, a_hi) ||
+        overlaps(w_lo, w_hi, b_lo, b_hi))
+      return fail(TMM_ERR_ALIAS, "%s: the workspace overlaps A, B or C", who);
+  }
+  const tmm::GemmProblem p = {M, N, K, A, lda, B, ldb, C, ldc};
+  cudaError_t e = tmm::launch_tc3(p, dev, workspace, s);
+  if (e != cudaSuccess) return fail(TMM_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
   return TMM_OK;
 }
 

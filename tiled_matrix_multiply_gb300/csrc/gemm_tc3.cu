@@ -1,0 +1,527 @@
+// gemm_tc3.cu -- FP32 product on the tcgen05 tensor cores with split-TF32 operands.
+//
+// The product C = A x B is the same as gemm_f32's; only the arithmetic units
+// differ.  Each FP32 operand x is split into two TF32 values, hi (x with its
+// low 13 mantissa bits cleared) and lo (x - hi, exact in FP32, rounded to the
+// nearest TF32).  Then
+//     a b = a_hi b_hi + a_hi b_lo + a_lo b_hi + a_lo b_lo,
+// and the last term (about 2^-22 |a b|) is dropped: three TF32 tensor-core
+// products, accumulated in FP32, give a result within FP32 accuracy.  Small
+// integers (|x| < 2^11) are exact TF32 values (lo = 0), so integer-valued
+// inputs stay exact.
+//
+// Structure (two launches per call):
+//   1. split pre-pass -- A into A_hi, A_lo (M x Kp, K-major) and B, transposed,
+//      into B_hi, B_lo (N x Kp, K-major), in the caller's workspace; Kp is K
+//      rounded up to 32 with zeros, so every K-slice is whole;
+//   2. product kernel -- one 128 x 256 tile of C per block, three roles:
+//      * copy (one thread): TMA (tensor-map bulk copies, 64-byte swizzle)
+//        loads K-slices of 16 of the four operands into a 4-stage ring;
+//      * tensor core (one thread): tcgen05.mma.kind::tf32 (M=128, N=256, K=8),
+//        three per K-step, into one of two tensor-memory accumulators
+//        (128 lanes x 256 FP32 columns each), switching buffers every
+//        kTcChunk values of K;
+//      * accumulate (eight warps): as each chunk completes, read it with
+//        tcgen05.ld and add it into FP32 registers (round to nearest), then
+//        release the buffer; after the last chunk, store C.
+//      The tensor core's own FP32 accumulation does not round to nearest
+//      (measured: error growing linearly in K); bounding each tensor-memory
+//      sum to kTcChunk values of K and adding the chunks on the CUDA cores
+//      keeps the product within FP32 accuracy at any K.
+// This follows the block-tile / staged-slab schedule of "CMU DLSys Lecture 12"
+// section 5 and the double buffering of "Tiling Strategies" section 3; the
+// register tile is replaced by a tensor-memory accumulator.
+//
+// Every mbarrier wait is bounded (globaltimer); on timeout the block records
+// bit 1 in its device status word, stops issuing work, waits (bounded) for its
+// copies in flight, frees its tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "tmm_internal.h"
+
+namespace tmm {
+
+__device__ unsigned int g_tc3_status;   // bit 1: a bounded wait ran out of time
+
+namespace {
+
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 256;
+constexpr int kTcBK = 16;                          // floats per K-slice: one 64-byte swizzle row
+constexpr int kTcStages = 4;
+constexpr int kTcChunk = 128;                      // K values per tensor-memory sum
+constexpr int kTcAccWarps = 8;                     // accumulate / epilogue warps
+constexpr int kTcThreads = 32 * (2 + kTcAccWarps); // copy warp, tensor-core warp, 8 more
+constexpr int kKPad = 32;                          // workspace K is a multiple of this
+constexpr uint32_t kATileBytes = kTcBM * kTcBK * 4;   // 8 KiB
+constexpr uint32_t kBTileBytes = kTcBN * kTcBK * 4;   // 16 KiB
+constexpr uint32_t kStageBytes = 2 * kATileBytes + 2 * kBTileBytes;
+constexpr uint32_t kTmemCols = 2 * kTcBN;         // two FP32 accumulators of kTcBN columns
+constexpr uint32_t kBarrierBytes = 8 * (2 * kTcStages + 4) + 8;
+constexpr uint32_t kTcSmemBytes = 1024 + kTcStages * kStageBytes + kBarrierBytes;
+
+static_assert(kTcBK * 4 == 64, "one K-slice row is one 64-byte swizzle row");
+static_assert(kTcChunk % kTcBK == 0 && kKPad % kTcBK == 0, "chunks are whole slices");
+static_assert(kStageBytes % 1024 == 0 && kATileBytes % 1024 == 0 && kBTileBytes % 1024 == 0,
+              "tiles stay 1024-byte aligned");
+
+// Instruction descriptor of tcgen05.mma.kind::tf32: D = F32 (bits 4-5 = 1),
+// A = B = TF32 (bits 7-9, 10-12 = 2), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdescTf32 = (1u << 4) | (2u << 7) | (2u << 10) |
+                                (uint32_t(kTcBN >> 3) << 17) | (uint32_t(kTcBM >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major operand tile with 64-byte
+// swizzle: start address >> 4 (bits 0-13), leading byte offset (unused for
+// swizzled K-major tiles; 16 B) >> 4 (bits 16-29), stride byte offset = 8 rows
+// x 64 B = 512 B >> 4 (bits 32-45), descriptor version 1 (bits 46-47),
+// layout 4 = 64-byte swizzle (bits 61-63).
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t smem_addr) {
+  return uint64_t((smem_addr >> 4) & 0x3FFFu) | (uint64_t(1) << 16) |
+         (uint64_t(512 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(4) << 61);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Wait for phase `parity` of the barrier to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (int64_t(timer_ns() - t0) > limit_ns) return false;
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %3, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %4, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(accumulate), "r"(kIdescTf32)
+      : "memory");
+}
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+// 32 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_load_32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// hi: x truncated to TF32; lo: the exact remainder rounded to the nearest TF32.
+__device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
+  hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+  const float r = x - hi;
+  lo = __uint_as_float((__float_as_uint(r) + 0x1000u) & 0xFFFFE000u);
+}
+
+// ---- split pre-pass -----------------------------------------------------------
+
+// A (M x K, lda) -> hi, lo (M x Kp), zeros for k >= K.
+__global__ void tc3_split_a_kernel(int M, int K, int Kp, const float *__restrict__ A, int64_t lda,
+                                   float *__restrict__ hi, float *__restrict__ lo) {
+  const int64_t total = int64_t(M) * Kp;
+  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t m = e / Kp;
+    const int k = int(e - m * Kp);
+    const float x = k < K ? A[m * lda + k] : 0.0f;
+    float h, l;
+    split_tf32(x, h, l);
+    hi[e] = h;
+    lo[e] = l;
+  }
+}
+
+// B (K x N, ldb) -> hi, lo transposed (N x Kp), zeros for k >= K; 32 x 32 tiles.
+__global__ void tc3_split_bt_kernel(int K, int N, int Kp, const float *__restrict__ B, int64_t ldb,
+                                    float *__restrict__ hi, float *__restrict__ lo) {
+  __shared__ float tile[32][33];
+  const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
+#pragma unroll
+  for (int j = 0; j < 32; j += 8) {
+    const int k = k0 + ty + j, n = n0 + tx;
+    tile[ty + j][tx] = (k < K && n < N) ? B[int64_t(k) * ldb + n] : 0.0f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 32; j += 8) {
+    const int n = n0 + ty + j, k = k0 + tx;
+    if (n < N && k < Kp) {
+      float h, l;
+      split_tf32(tile[tx][ty + j], h, l);
+      hi[int64_t(n) * Kp + k] = h;
+      lo[int64_t(n) * Kp + k] = l;
+    }
+  }
+}
+
+// ---- product kernel ---------------------------------------------------------------
+
+struct Tc3Params {
+  int M, N, Kp;
+  float *C;
+  int64_t ldc;
+  int tiles_n;
+  int vec_store;         // C 16-byte aligned and ldc % 4 == 0
+  int64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
+                const __grid_constant__ CUtensorMap map_alo,
+                const __grid_constant__ CUtensorMap map_bhi,
+                const __grid_constant__ CUtensorMap map_blo, const Tc3Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;            // 1024-aligned stage ring
+  const uint32_t bar_full = base + kTcStages * kStageBytes;
+  const uint32_t bar_empty = bar_full + 8 * kTcStages;
+  const uint32_t bar_tfull = bar_empty + 8 * kTcStages;    // accumulator b complete
+  const uint32_t bar_tempty = bar_tfull + 16;              // accumulator b drained
+  const uint32_t tmem_slot = bar_tempty + 16;
+  volatile uint32_t *tmem_slot_ptr =
+      reinterpret_cast<volatile uint32_t *>(smem_raw + (tmem_slot - raw));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = (blockIdx.x / p.tiles_n) * kTcBM;
+  const int n0 = (blockIdx.x % p.tiles_n) * kTcBN;
+  const int num_k = p.Kp / kTcBK;
+  constexpr int kSlicesPerChunk = kTcChunk / kTcBK;
+  const int num_chunks = (num_k + kSlicesPerChunk - 1) / kSlicesPerChunk;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, kTcAccWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     tmem_slot),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_d = *tmem_slot_ptr;
+
+  bool timed_out = false;
+  if (threadIdx.x == 0) {
+    // Copy role: TMA loads of slice i into stage i % S once the stage is free.
+    int issued = 0;
+    for (int i = 0; i < num_k; ++i) {
+      const int s = i % kTcStages;
+      if (i >= kTcStages &&
+          !mbar_wait(bar_empty + 8 * s, uint32_t((i / kTcStages) - 1) & 1u, p.wait_limit_ns)) {
+        timed_out = true;
+        break;
+      }
+      const uint32_t full = bar_full + 8 * s;
+      const uint32_t st = base + s * kStageBytes;
+      const int kx = i * kTcBK;
+      mbar_arrive_expect_tx(full, kStageBytes);
+      tma_load_2d(st, &map_ahi, kx, m0, full);
+      tma_load_2d(st + kATileBytes, &map_alo, kx, m0, full);
+      tma_load_2d(st + 2 * kATileBytes, &map_bhi, kx, n0, full);
+      tma_load_2d(st + 2 * kATileBytes + kBTileBytes, &map_blo, kx, n0, full);
+      issued = i + 1;
+    }
+    if (timed_out) {
+      // Let the copies already in flight land before the block goes away.
+      for (int i = issued > kTcStages ? issued - kTcStages : 0; i < issued; ++i)
+        mbar_wait(bar_full + 8 * (i % kTcStages), uint32_t(i / kTcStages) & 1u, p.wait_limit_ns);
+    }
+  } else if (threadIdx.x == 32) {
+    // Tensor-core role: three TF32 products per K-step of 8, small terms first,
+    // into accumulator (chunk % 2).
+    for (int i = 0; i < num_k && !timed_out; ++i) {
+      const int s = i % kTcStages;
+      const int chunk = i / kSlicesPerChunk;
+      const int buf = chunk & 1;
+      const bool chunk_start = (i % kSlicesPerChunk) == 0;
+      if (chunk_start && chunk >= 2 &&
+          !mbar_wait(bar_tempty + 8 * buf, uint32_t((chunk >> 1) - 1) & 1u, p.wait_limit_ns)) {
+        timed_out = true;
+        break;
+      }
+      if (!mbar_wait(bar_full + 8 * s, uint32_t(i / kTcStages) & 1u, p.wait_limit_ns)) {
+        timed_out = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t st = base + s * kStageBytes;
+      const uint32_t d = tmem_d + uint32_t(buf * kTcBN);
+#pragma unroll
+      for (int kk = 0; kk < kTcBK / 8; ++kk) {
+        const uint32_t koff = 32u * kk;   // 8 TF32 values along K
+        const uint64_t a_hi = sw64_desc(st + koff);
+        const uint64_t a_lo = sw64_desc(st + kATileBytes + koff);
+        const uint64_t b_hi = sw64_desc(st + 2 * kATileBytes + koff);
+        const uint64_t b_lo = sw64_desc(st + 2 * kATileBytes + kBTileBytes + koff);
+        mma_tf32(d, a_lo, b_hi, (chunk_start && kk == 0) ? 0u : 1u);
+        mma_tf32(d, a_hi, b_lo, 1u);
+        mma_tf32(d, a_hi, b_hi, 1u);
+      }
+      mma_commit(bar_empty + 8 * s);   // stage s is free once these products have read it
+      if ((i % kSlicesPerChunk) == kSlicesPerChunk - 1 || i == num_k - 1)
+        mma_commit(bar_tfull + 8 * buf);   // accumulator buf holds a finished chunk
+    }
+    // Wait (bounded) until every product issued above has completed, so the
+    // tensor memory is not released under them.
+    mma_commit(bar_empty + 8 * (num_k % kTcStages));
+  } else if (warp >= 2) {
+    // Accumulate role: warp w reads TMEM lanes 32 (w % 4).. (its rows), columns
+    // half * 128.. of each finished chunk, and adds them in FP32 registers.
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    float acc[kTcBN / 2];
+#pragma unroll
+    for (int j = 0; j < kTcBN / 2; ++j) acc[j] = 0.0f;
+    for (int chunk = 0; chunk < num_chunks; ++chunk) {
+      const int buf = chunk & 1;
+      // The whole warp takes one decision: tcgen05.ld below is warp-collective.
+      const bool ready = mbar_wait(bar_tfull + 8 * buf, uint32_t(chunk >> 1) & 1u, p.wait_limit_ns);
+      if (!__all_sync(0xffffffffu, ready)) {
+        timed_out = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_d + (uint32_t(32 * quarter) << 16) + uint32_t(buf * kTcBN + half * (kTcBN / 2));
+#pragma unroll
+      for (int c = 0; c < kTcBN / 2; c += 32) {
+        float v[32];
+        __syncwarp();
+        tmem_load_32(taddr + uint32_t(c), v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[c + j] += v[j];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
+    }
+    // Epilogue: this thread's row, 128 consecutive columns.
+    const int row = m0 + 32 * quarter + lane;
+    const int col0 = n0 + half * (kTcBN / 2);
+    if (!timed_out && row < p.M) {
+      float *c_row = p.C + int64_t(row) * p.ldc;
+#pragma unroll
+      for (int c = 0; c < kTcBN / 2; c += 4) {
+        const int col = col0 + c;
+        if (p.vec_store && col + 4 <= p.N) {
+          *reinterpret_cast<float4 *>(c_row + col) =
+              make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (col + j < p.N) c_row[col + j] = acc[c + j];
+        }
+      }
+    }
+  }
+  __syncwarp();
+  if (threadIdx.x == 32) {
+    // The final commit above arrives once all products are done: wait for it.
+    const int i = num_k;
+    if (!mbar_wait(bar_empty + 8 * (i % kTcStages), uint32_t(i / kTcStages) & 1u,
+                   p.wait_limit_ns))
+      timed_out = true;
+  }
+  if (timed_out) atomicOr(&g_tc3_status, 2u);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d),
+                 "r"(kTmemCols)
+                 : "memory");
+}
+
+// ---- host side ------------------------------------------------------------------
+
+int64_t pad_k(int64_t K) { return (K + kKPad - 1) / kKPad * kKPad; }
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_status = cudaSuccess;
+
+cudaError_t get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    g_encode_status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                       cudaEnableDefault, &q);
+    if (g_encode_status == cudaSuccess && (q != cudaDriverEntryPointSuccess || fn == nullptr))
+      g_encode_status = cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode_status;
+}
+
+// K-major operand of `rows` x Kp floats; box of kTcBK x box_rows, 64-byte swizzle.
+cudaError_t encode_operand(CUtensorMap *map, const float *base, int64_t rows, int64_t Kp,
+                           uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cuuint64_t(Kp), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(Kp) * 4};
+  const cuuint32_t box[2] = {cuuint32_t(kTcBK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+std::atomic<uint64_t> g_tc3_configured{0};
+std::atomic<int64_t> g_tc3_wait_limit_ns{int64_t(10) * 1000 * 1000 * 1000};
+
+}  // namespace
+
+size_t tc3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int64_t Kp = pad_k(K);
+  return 2 * round256(size_t(M) * Kp * 4) + 2 * round256(size_t(N) * Kp * 4);
+}
+
+cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *workspace,
+                       cudaStream_t stream) {
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  const int64_t Kp = pad_k(p.K);
+  char *ws = static_cast<char *>(workspace);
+  float *a_hi = reinterpret_cast<float *>(ws);
+  float *a_lo = reinterpret_cast<float *>(ws + round256(size_t(p.M) * Kp * 4));
+  float *b_hi = reinterpret_cast<float *>(ws + 2 * round256(size_t(p.M) * Kp * 4));
+  float *b_lo = reinterpret_cast<float *>(ws + 2 * round256(size_t(p.M) * Kp * 4) +
+                                          round256(size_t(p.N) * Kp * 4));
+
+  // 1. split pre-pass.
+  {
+    const int64_t total = p.M * Kp;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, int64_t(dev.sm_count) * 32);
+    tc3_split_a_kernel<<<unsigned(blocks), 256, 0, stream>>>(int(p.M), int(p.K), int(Kp), p.A,
+                                                             p.lda, a_hi, a_lo);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const dim3 grid(unsigned((p.N + 31) / 32), unsigned(Kp / 32));
+    tc3_split_bt_kernel<<<grid, dim3(32, 8), 0, stream>>>(int(p.K), int(p.N), int(Kp), p.B, p.ldb,
+                                                          b_hi, b_lo);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+
+  // 2. product kernel.
+  CUtensorMap maps[4];
+  if ((e = encode_operand(&maps[0], a_hi, p.M, Kp, kTcBM)) != cudaSuccess ||
+      (e = encode_operand(&maps[1], a_lo, p.M, Kp, kTcBM)) != cudaSuccess ||
+      (e = encode_operand(&maps[2], b_hi, p.N, Kp, kTcBN)) != cudaSuccess ||
+      (e = encode_operand(&maps[3], b_lo, p.N, Kp, kTcBN)) != cudaSuccess)
+    return e;
+  const uint64_t bit = uint64_t(1) << (dev.id & 63);
+  if (!(g_tc3_configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(gemm_tc3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kTcSmemBytes));
+    if (e != cudaSuccess) return e;
+    g_tc3_configured.fetch_or(bit, std::memory_order_release);
+  }
+  Tc3Params prm = {};
+  prm.M = int(p.M);
+  prm.N = int(p.N);
+  prm.Kp = int(Kp);
+  prm.C = p.C;
+  prm.ldc = p.ldc;
+  prm.tiles_n = int((p.N + kTcBN - 1) / kTcBN);
+  prm.vec_store = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0) ? 1 : 0;
+  prm.wait_limit_ns = g_tc3_wait_limit_ns.load(std::memory_order_relaxed);
+  const int64_t tiles = int64_t(prm.tiles_n) * ((p.M + kTcBM - 1) / kTcBM);
+  if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  gemm_tc3_kernel<<<unsigned(tiles), kTcThreads, kTcSmemBytes, stream>>>(maps[0], maps[1], maps[2],
+                                                                         maps[3], prm);
+  return cudaGetLastError();
+}
+
+cudaError_t tc3_device_status(unsigned int *status, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, g_tc3_status, sizeof(unsigned int));
+  if (e != cudaSuccess || !clear) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_tc3_status, &zero, sizeof(unsigned int));
+}
+
+void tc3_set_wait_limit(int64_t wait_limit_ns) {
+  g_tc3_wait_limit_ns.store(wait_limit_ns > 0 ? wait_limit_ns : int64_t(10) * 1000 * 1000 * 1000,
+                            std::memory_order_relaxed);
+}
+
+}  // namespace tmm

@@ -31,6 +31,14 @@ struct DeviceInfo {
 cudaError_t launch_naive(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream);
 cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream);
 
+// Split-TF32 tensor-core path: workspace bytes for an M x N x K product, and
+// the launch (split pre-pass + product kernel); `workspace` is 256-byte aligned.
+size_t tc3_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *workspace,
+                       cudaStream_t stream);
+cudaError_t tc3_device_status(unsigned int *status, bool clear);
+void tc3_set_wait_limit(int64_t wait_limit_ns);
+
 // Device status word of the tiled kernel (bit 0: a bounded wait ran out of
 // time); read from the current device, optionally cleared.
 cudaError_t simt_device_status(unsigned int *status, bool clear);
