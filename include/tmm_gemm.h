@@ -143,6 +143,36 @@ int gemm_f32_tc3(int64_t M, int64_t N, int64_t K,
 size_t gemm_f32_tc3_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
+ * gemm_f32_tc3_noalloc -- gemm_f32_tc3 for callers that cannot allocate device
+ * memory where they call it: code under a memory manager that owns the whole
+ * device budget and forbids raw cudaMalloc, code on a latency-critical path
+ * that cannot afford cudaMalloc's implicit synchronisation, or code where the
+ * CUDA allocation API may not be called.  The pages have no counterpart; this
+ * is a library convenience.  Same product, contract and status codes as
+ * gemm_f32_tc3 (inputs and output are still the caller's device pointers),
+ * but the split operands go to a fixed scratch array inside the library
+ * instead of a caller-supplied workspace, and nothing is allocated:
+ *   - the scratch is TMM_TC3_NOALLOC_SCRATCH_BYTES (64 MiB) of device memory
+ *     set aside when the library's module is loaded; every GPU that loads it
+ *     holds it until the process exits;
+ *   - products needing more than that (gemm_f32_tc3_workspace_size(M, N, K)
+ *     > TMM_TC3_NOALLOC_SCRATCH_BYTES, for example beyond about 2048^3) are
+ *     rejected with TMM_ERR_INVALID_ARG and a message naming the sizes;
+ *   - the first call on each device looks up the scratch's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture;
+ *   - every call on a device uses the same scratch and leaves its contents
+ *     behind; calls that overlap on the GPU (for example on two streams) race
+ *     on it and must be serialised by the caller.
+ */
+#define TMM_TC3_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K,
+                         const float *A, int64_t lda,
+                         const float *B, int64_t ldb,
+                         float *C, int64_t ldc,
+                         tmm_stream_t stream);
+
+/*
  * tmm_check_device -- synchronise `stream`, then read and clear the current
  * device's status word.  Returns TMM_OK, or TMM_ERR_DEVICE_TIMEOUT when a
  * bounded wait inside gemm_f32 (between the two blocks sharing a split tile)

@@ -19,7 +19,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libtmm_gemm.so")
 
-SOURCES = ["gemm_abi.cpp", "gemm_naive.cu", "gemm_simt.cu", "gemm_tc3.cu"]
+SOURCES = ["gemm_abi.cpp", "gemm_naive.cu", "gemm_simt.cu", "gemm_tc3.cu",
+           "gemm_tc3_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC] + ARCH

@@ -225,6 +225,40 @@ int gemm_f32_tc3(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, c
   return TMM_OK;
 }
 
+int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                         const float *B, int64_t ldb, float *C, int64_t ldc,
+                         tmm_stream_t stream) {
+  const char *who = "gemm_f32_tc3_noalloc";
+  bool noop = false;
+  int rc = check_args(who, M, N, K, A, lda, B, ldb, C, ldc, &noop);
+  if (rc != TMM_OK || noop) return rc;
+  tmm::DeviceInfo dev;
+  if ((rc = current_device(&dev)) != TMM_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    cudaError_t e = cudaMemset2DAsync(C, size_t(ldc) * sizeof(float), 0,
+                                      size_t(N) * sizeof(float), size_t(M), s);
+    if (e != cudaSuccess)
+      return fail(TMM_ERR_CUDA, "%s: cudaMemset2DAsync: %s", who, cudaGetErrorString(e));
+    return TMM_OK;
+  }
+  const size_t need = tmm::tc3_workspace_bytes(M, N, K);
+  const size_t limit = tmm::tc3_noalloc_scratch_bytes();
+  if (need > limit)
+    return fail(TMM_ERR_INVALID_ARG,
+                "%s: this product needs %zu bytes of scratch but the fixed scratch holds %zu; "
+                "use gemm_f32_tc3 with a caller-supplied workspace",
+                who, need, limit);
+  void *scratch = nullptr;
+  cudaError_t e = tmm::tc3_noalloc_scratch(dev.id, &scratch);
+  if (e != cudaSuccess)
+    return fail(TMM_ERR_CUDA, "%s: scratch address lookup: %s", who, cudaGetErrorString(e));
+  const tmm::GemmProblem p = {M, N, K, A, lda, B, ldb, C, ldc};
+  e = tmm::launch_tc3(p, dev, scratch, s);
+  if (e != cudaSuccess) return fail(TMM_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
+  return TMM_OK;
+}
+
 const char *tmm_last_error_string(void) { return g_last_error; }
 
 int tmm_version(void) { return 100; }

@@ -37,6 +37,10 @@ size_t tc3_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *workspace,
                        cudaStream_t stream);
 cudaError_t tc3_device_status(unsigned int *status, bool clear);
+// Fixed scratch of gemm_f32_tc3_noalloc: its size, and the current device's
+// address of it (looked up once per device; `device` must be current).
+size_t tc3_noalloc_scratch_bytes();
+cudaError_t tc3_noalloc_scratch(int device, void **ptr);
 void tc3_set_wait_limit(int64_t wait_limit_ns);
 
 // Device status word of the tiled kernel (bit 0: a bounded wait ran out of
