@@ -165,7 +165,7 @@ def ffma_peak_tflops(sm_count: int, peaks: dict) -> tuple[float, str]:
         f"{sm_count} SMs x 128 FFMA/clk x 2 FLOP x {mhz:.0f} MHz ({src})"
 
 
-KERNEL_SOURCES = {"gemm_simt": ["gemm_simt.cu", "tmm_internal.h"]}
+KERNEL_SOURCES = {"gemm_simt": ["gemm_simt.cu"], "gemm_tc3": ["gemm_tc3.cu"]}
 
 
 def recorded_traffic(kernel: str, workload: str):

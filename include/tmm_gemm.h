@@ -186,8 +186,9 @@ int tmm_check_device(tmm_stream_t stream);
 
 /*
  * tmm_testing_set_wait_hooks -- testing only; no counterpart in the pages.
- * drop_signal_block >= 0 makes that block of later stream-K launches skip
- * raising its flag, so the block waiting on it runs into the time limit;
+ * drop_signal_block >= 0 makes that block of later stream-K launches (of
+ * gemm_f32 and gemm_f32_tc3) skip raising its flags, so the block waiting on
+ * it runs into the time limit;
  * wait_limit_ns > 0 sets the limit of every bounded wait of both kernels
  * (default, and for values <= 0, 10 s).
  * Process-wide; pass (-1, 0) to restore the defaults.  Always TMM_OK.

@@ -178,3 +178,25 @@ def test_python_binding_side_stream():
         C = tmm.gemm_f32_tc3(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda())
         tmm.check_device(s)
     parity.assert_close(C.cpu().numpy(), oracle.gemm(A, B), 200, "binding")
+
+
+def test_stream_k_wait_timeout_is_reported_and_recovers():
+    # 2560 x 2560 gives 20 x 10 = 200 tiles of 128 x 256: more than one per SM
+    # and a partial last wave, so the persistent grid splits tiles along K.
+    lib = _abi.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    M, N, K = 2560, 2560, 512
+    rng = np.random.default_rng(58)
+    A = rng.integers(-4, 5, (M, K)).astype(np.float32)
+    B = rng.integers(-4, 5, (K, N)).astype(np.float32)
+    assert lib.tmm_check_device(stream) == _abi.TMM_OK
+    try:
+        assert lib.tmm_testing_set_wait_hooks(1, 2_000_000) == _abi.TMM_OK
+        _run(A, B, check_canaries=False, check_status=False)
+        rc = lib.tmm_check_device(stream)
+        assert rc == _abi.TMM_ERR_DEVICE_TIMEOUT, rc
+        assert "gemm_f32_tc3" in _abi.last_error()
+    finally:
+        lib.tmm_testing_set_wait_hooks(-1, 0)
+    assert lib.tmm_check_device(stream) == _abi.TMM_OK
+    parity.assert_bit_exact(_run(A, B, check_canaries=False), oracle.gemm(A, B), "after timeout")

@@ -177,7 +177,7 @@ int tmm_check_device(tmm_stream_t stream) {
 
 int tmm_testing_set_wait_hooks(int drop_signal_block, int64_t wait_limit_ns) {
   tmm::simt_set_test_hooks(drop_signal_block, wait_limit_ns);
-  tmm::tc3_set_wait_limit(wait_limit_ns);
+  tmm::tc3_set_test_hooks(drop_signal_block, wait_limit_ns);
   return TMM_OK;
 }
 

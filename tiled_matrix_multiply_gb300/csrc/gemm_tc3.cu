@@ -28,6 +28,14 @@
 //      (measured: error growing linearly in K); bounding each tensor-memory
 //      sum to kTcChunk values of K and adding the chunks on the CUDA cores
 //      keeps the product within FP32 accuracy at any K.
+// Scheduling: one block per tile, tiles in row-major order, so the blocks of
+// a wave move through K together and share the A and B panels in L2.  When
+// the tile count leaves the last wave at most half full, each of its tiles is
+// split into two halves of the K range, run side by side by two blocks: the
+// block holding the upper half stores its partial sums into C and raises a
+// flag (one per accumulate warp), the block holding the lower half waits for
+// it (bounded), adds, and stores the total -- in that fixed order, so results
+// are deterministic.  The last wave then takes half the time.
 // This follows the block-tile / staged-slab schedule of "CMU DLSys Lecture 12"
 // section 5 and the double buffering of "Tiling Strategies" section 3; the
 // register tile is replaced by a tensor-memory accumulator.
@@ -48,6 +56,12 @@
 namespace tmm {
 
 __device__ unsigned int g_tc3_status;   // bit 1: a bounded wait ran out of time
+// Split-tile flags, one per (tail block, accumulate warp): kTc3FlagRegions
+// rings; a call uses region epoch % kTc3FlagRegions and raises flags to its epoch.
+constexpr int kTc3FlagRegions = 16;
+constexpr int kTc3MaxBlocks = 1024;   // tail blocks of one call
+constexpr int kTc3FlagsPerBlock = 8;   // = the accumulate warps
+__device__ unsigned int g_tc3_flags[kTc3FlagRegions * kTc3MaxBlocks * kTc3FlagsPerBlock];
 
 namespace {
 
@@ -63,7 +77,7 @@ constexpr uint32_t kATileBytes = kTcBM * kTcBK * 4;   // 8 KiB
 constexpr uint32_t kBTileBytes = kTcBN * kTcBK * 4;   // 16 KiB
 constexpr uint32_t kStageBytes = 2 * kATileBytes + 2 * kBTileBytes;
 constexpr uint32_t kTmemCols = 2 * kTcBN;         // two FP32 accumulators of kTcBN columns
-constexpr uint32_t kBarrierBytes = 8 * (2 * kTcStages + 4) + 8;
+constexpr uint32_t kBarrierBytes = 8 * (2 * kTcStages + 5) + 8;
 constexpr uint32_t kTcSmemBytes = 1024 + kTcStages * kStageBytes + kBarrierBytes;
 
 static_assert(kTcBK * 4 == 64, "one K-slice row is one 64-byte swizzle row");
@@ -151,22 +165,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                    bar)
                : "memory");
 }
-// 32 consecutive FP32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_load_32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
+// 8 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_load_8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // hi: x truncated to TF32; lo: the exact remainder rounded to the nearest TF32.
@@ -178,19 +186,28 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
 
 // ---- split pre-pass -----------------------------------------------------------
 
-// A (M x K, lda) -> hi, lo (M x Kp), zeros for k >= K.
+// A (M x K, lda) -> hi, lo (M x Kp), zeros for k >= K.  Thread handles 4
+// consecutive k of one row; rows advance with the grid's y extent.
 __global__ void tc3_split_a_kernel(int M, int K, int Kp, const float *__restrict__ A, int64_t lda,
-                                   float *__restrict__ hi, float *__restrict__ lo) {
-  const int64_t total = int64_t(M) * Kp;
-  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
-       e += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t m = e / Kp;
-    const int k = int(e - m * Kp);
-    const float x = k < K ? A[m * lda + k] : 0.0f;
-    float h, l;
-    split_tf32(x, h, l);
-    hi[e] = h;
-    lo[e] = l;
+                                   int vec_load, float *__restrict__ hi, float *__restrict__ lo) {
+  const int k = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (k >= Kp) return;
+  for (int m = blockIdx.y; m < M; m += gridDim.y) {
+    const float *a = A + int64_t(m) * lda;
+    float x[4];
+    if (vec_load && k + 4 <= K) {
+      const float4 v = *reinterpret_cast<const float4 *>(a + k);
+      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[j] = k + j < K ? a[k + j] : 0.0f;
+    }
+    float h[4], l[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) split_tf32(x[j], h[j], l[j]);
+    const int64_t o = int64_t(m) * Kp + k;
+    *reinterpret_cast<float4 *>(hi + o) = make_float4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<float4 *>(lo + o) = make_float4(l[0], l[1], l[2], l[3]);
   }
 }
 
@@ -224,15 +241,62 @@ struct Tc3Params {
   int M, N, Kp;
   float *C;
   int64_t ldc;
-  int tiles_n;
+  int tiles_m, tiles_n;
+  int slices;            // K-slices per tile
+  int dp_tiles;          // blocks [0, dp_tiles) each process tile blockIdx.x whole
+  int split;             // blocks from dp_tiles on: tail tile halves [0, split), [split, S)
+  unsigned int epoch;    // this call's flag value (never 0)
   int vec_store;         // C 16-byte aligned and ldc % 4 == 0
   int64_t wait_limit_ns;
+  int drop_signal_block; // testing hook: this block never raises its flags (-1: none)
+};
+
+__device__ __forceinline__ void tc3_tile_coords(int tile, int tiles_n, int &tm, int &tn) {
+  tm = tile / tiles_n;
+  tn = tile - tm * tiles_n;
+}
+
+// This block's single work item (tile, K-slice range); `unit` >= 0 numbers
+// the blocks that share a split tile (even: lower half, owner; odd: upper half).
+struct Tc3Work {
+  bool done;
+  __device__ __forceinline__ void init(const Tc3Params &) { done = false; }
+  __device__ __forceinline__ bool next(const Tc3Params &p, int &tile, int &kb, int &ke,
+                                       int &unit) {
+    if (done) return false;
+    done = true;
+    const int b = blockIdx.x;
+    if (b < p.dp_tiles) {
+      tile = b;
+      kb = 0;
+      ke = p.slices;
+      unit = -1;
+      return true;
+    }
+    unit = b - p.dp_tiles;
+    tile = p.dp_tiles + unit / 2;
+    kb = (unit & 1) ? p.split : 0;
+    ke = (unit & 1) ? p.slices : p.split;
+    return true;
+  }
 };
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned int *p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+static_assert(kTc3FlagsPerBlock == kTcAccWarps, "one flag per accumulate warp");
+
+// 320 threads: with 3 warps on some SM sub-partitions (16K registers each),
+// at most 168 registers per thread.
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
                 const __grid_constant__ CUtensorMap map_alo,
@@ -243,18 +307,17 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
   const uint32_t base = (raw + 1023u) & ~1023u;            // 1024-aligned stage ring
   const uint32_t bar_full = base + kTcStages * kStageBytes;
   const uint32_t bar_empty = bar_full + 8 * kTcStages;
-  const uint32_t bar_tfull = bar_empty + 8 * kTcStages;    // accumulator b complete
+  const uint32_t bar_tfull = bar_empty + 8 * kTcStages;    // accumulator b holds a finished chunk
   const uint32_t bar_tempty = bar_tfull + 16;              // accumulator b drained
-  const uint32_t tmem_slot = bar_tempty + 16;
+  const uint32_t bar_drain = bar_tempty + 16;              // every product issued has completed
+  const uint32_t tmem_slot = bar_drain + 8;
   volatile uint32_t *tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t *>(smem_raw + (tmem_slot - raw));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = (blockIdx.x / p.tiles_n) * kTcBM;
-  const int n0 = (blockIdx.x % p.tiles_n) * kTcBN;
-  const int num_k = p.Kp / kTcBK;
   constexpr int kSlicesPerChunk = kTcChunk / kTcBK;
-  const int num_chunks = (num_k + kSlicesPerChunk - 1) / kSlicesPerChunk;
+  unsigned int *flags =
+      g_tc3_flags + (p.epoch % kTc3FlagRegions) * (kTc3MaxBlocks * kTc3FlagsPerBlock);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
@@ -265,6 +328,7 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
       mbar_init(bar_tfull + 8 * b, 1);
       mbar_init(bar_tempty + 8 * b, kTcAccWarps);
     }
+    mbar_init(bar_drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -280,127 +344,174 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
   const uint32_t tmem_d = *tmem_slot_ptr;
 
   bool timed_out = false;
+  Tc3Work work;
+  work.init(p);
+  int tile, kb, ke, unit;
   if (threadIdx.x == 0) {
-    // Copy role: TMA loads of slice i into stage i % S once the stage is free.
-    int issued = 0;
-    for (int i = 0; i < num_k; ++i) {
-      const int s = i % kTcStages;
-      if (i >= kTcStages &&
-          !mbar_wait(bar_empty + 8 * s, uint32_t((i / kTcStages) - 1) & 1u, p.wait_limit_ns)) {
-        timed_out = true;
-        break;
+    // Copy role: TMA loads of each work item's slices into the ring.
+    int r = 0;   // ring position (slices issued so far)
+    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
+      int tm, tn;
+      tc3_tile_coords(tile, p.tiles_n, tm, tn);
+      const int m0 = tm * kTcBM, n0 = tn * kTcBN;
+      for (int i = kb; i < ke; ++i, ++r) {
+        const int s = r % kTcStages;
+        if (r >= kTcStages &&
+            !mbar_wait(bar_empty + 8 * s, uint32_t((r / kTcStages) - 1) & 1u, p.wait_limit_ns)) {
+          timed_out = true;
+          break;
+        }
+        const uint32_t full = bar_full + 8 * s;
+        const uint32_t st = base + s * kStageBytes;
+        const int kx = i * kTcBK;
+        mbar_arrive_expect_tx(full, kStageBytes);
+        tma_load_2d(st, &map_ahi, kx, m0, full);
+        tma_load_2d(st + kATileBytes, &map_alo, kx, m0, full);
+        tma_load_2d(st + 2 * kATileBytes, &map_bhi, kx, n0, full);
+        tma_load_2d(st + 2 * kATileBytes + kBTileBytes, &map_blo, kx, n0, full);
       }
-      const uint32_t full = bar_full + 8 * s;
-      const uint32_t st = base + s * kStageBytes;
-      const int kx = i * kTcBK;
-      mbar_arrive_expect_tx(full, kStageBytes);
-      tma_load_2d(st, &map_ahi, kx, m0, full);
-      tma_load_2d(st + kATileBytes, &map_alo, kx, m0, full);
-      tma_load_2d(st + 2 * kATileBytes, &map_bhi, kx, n0, full);
-      tma_load_2d(st + 2 * kATileBytes + kBTileBytes, &map_blo, kx, n0, full);
-      issued = i + 1;
     }
     if (timed_out) {
       // Let the copies already in flight land before the block goes away.
-      for (int i = issued > kTcStages ? issued - kTcStages : 0; i < issued; ++i)
+      for (int i = r > kTcStages ? r - kTcStages : 0; i < r; ++i)
         mbar_wait(bar_full + 8 * (i % kTcStages), uint32_t(i / kTcStages) & 1u, p.wait_limit_ns);
     }
   } else if (threadIdx.x == 32) {
     // Tensor-core role: three TF32 products per K-step of 8, small terms first,
-    // into accumulator (chunk % 2).
-    for (int i = 0; i < num_k && !timed_out; ++i) {
-      const int s = i % kTcStages;
-      const int chunk = i / kSlicesPerChunk;
-      const int buf = chunk & 1;
-      const bool chunk_start = (i % kSlicesPerChunk) == 0;
-      if (chunk_start && chunk >= 2 &&
-          !mbar_wait(bar_tempty + 8 * buf, uint32_t((chunk >> 1) - 1) & 1u, p.wait_limit_ns)) {
-        timed_out = true;
-        break;
-      }
-      if (!mbar_wait(bar_full + 8 * s, uint32_t(i / kTcStages) & 1u, p.wait_limit_ns)) {
-        timed_out = true;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t st = base + s * kStageBytes;
-      const uint32_t d = tmem_d + uint32_t(buf * kTcBN);
+    // each chunk of kSlicesPerChunk slices into accumulator (chunk count % 2).
+    int r = 0;   // ring position
+    int q = 0;   // chunks started so far
+    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
+      for (int i = kb; i < ke && !timed_out; ++i, ++r) {
+        const int s = r % kTcStages;
+        const bool chunk_start = ((i - kb) % kSlicesPerChunk) == 0;
+        if (chunk_start) {
+          if (q >= 2 && !mbar_wait(bar_tempty + 8 * (q & 1), uint32_t((q >> 1) - 1) & 1u,
+                                   p.wait_limit_ns)) {
+            timed_out = true;
+            break;
+          }
+          ++q;
+        }
+        const int buf = (q - 1) & 1;
+        if (!mbar_wait(bar_full + 8 * s, uint32_t(r / kTcStages) & 1u, p.wait_limit_ns)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = base + s * kStageBytes;
+        const uint32_t d = tmem_d + uint32_t(buf * kTcBN);
 #pragma unroll
-      for (int kk = 0; kk < kTcBK / 8; ++kk) {
-        const uint32_t koff = 32u * kk;   // 8 TF32 values along K
-        const uint64_t a_hi = sw64_desc(st + koff);
-        const uint64_t a_lo = sw64_desc(st + kATileBytes + koff);
-        const uint64_t b_hi = sw64_desc(st + 2 * kATileBytes + koff);
-        const uint64_t b_lo = sw64_desc(st + 2 * kATileBytes + kBTileBytes + koff);
-        mma_tf32(d, a_lo, b_hi, (chunk_start && kk == 0) ? 0u : 1u);
-        mma_tf32(d, a_hi, b_lo, 1u);
-        mma_tf32(d, a_hi, b_hi, 1u);
+        for (int kk = 0; kk < kTcBK / 8; ++kk) {
+          const uint32_t koff = 32u * kk;   // 8 TF32 values along K
+          const uint64_t a_hi = sw64_desc(st + koff);
+          const uint64_t a_lo = sw64_desc(st + kATileBytes + koff);
+          const uint64_t b_hi = sw64_desc(st + 2 * kATileBytes + koff);
+          const uint64_t b_lo = sw64_desc(st + 2 * kATileBytes + kBTileBytes + koff);
+          mma_tf32(d, a_lo, b_hi, (chunk_start && kk == 0) ? 0u : 1u);
+          mma_tf32(d, a_hi, b_lo, 1u);
+          mma_tf32(d, a_hi, b_hi, 1u);
+        }
+        mma_commit(bar_empty + 8 * s);   // stage s is free once these products have read it
+        if ((i - kb) % kSlicesPerChunk == kSlicesPerChunk - 1 || i == ke - 1)
+          mma_commit(bar_tfull + 8 * buf);   // accumulator buf holds a finished chunk
       }
-      mma_commit(bar_empty + 8 * s);   // stage s is free once these products have read it
-      if ((i % kSlicesPerChunk) == kSlicesPerChunk - 1 || i == num_k - 1)
-        mma_commit(bar_tfull + 8 * buf);   // accumulator buf holds a finished chunk
     }
-    // Wait (bounded) until every product issued above has completed, so the
-    // tensor memory is not released under them.
-    mma_commit(bar_empty + 8 * (num_k % kTcStages));
+    mma_commit(bar_drain);
+    if (!mbar_wait(bar_drain, 0u, p.wait_limit_ns)) timed_out = true;
   } else if (warp >= 2) {
     // Accumulate role: warp w reads TMEM lanes 32 (w % 4).. (its rows), columns
     // half * 128.. of each finished chunk, and adds them in FP32 registers.
+    // Warp w of a split tile's owner adds what warp w of the partner block
+    // stored (the same rows and columns), so the two meet through one flag per
+    // warp, without any block-level barrier.
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
-    float acc[kTcBN / 2];
+    const int acc_warp = warp - 2;
+    int q = 0;   // chunks consumed so far
+    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
+      float acc[kTcBN / 2];
 #pragma unroll
-    for (int j = 0; j < kTcBN / 2; ++j) acc[j] = 0.0f;
-    for (int chunk = 0; chunk < num_chunks; ++chunk) {
-      const int buf = chunk & 1;
-      // The whole warp takes one decision: tcgen05.ld below is warp-collective.
-      const bool ready = mbar_wait(bar_tfull + 8 * buf, uint32_t(chunk >> 1) & 1u, p.wait_limit_ns);
-      if (!__all_sync(0xffffffffu, ready)) {
-        timed_out = true;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t taddr =
-          tmem_d + (uint32_t(32 * quarter) << 16) + uint32_t(buf * kTcBN + half * (kTcBN / 2));
+      for (int j = 0; j < kTcBN / 2; ++j) acc[j] = 0.0f;
+      const int chunks = (ke - kb + kSlicesPerChunk - 1) / kSlicesPerChunk;
+      for (int c = 0; c < chunks; ++c, ++q) {
+        const int buf = q & 1;
+        // The whole warp takes one decision: tcgen05.ld below is warp-collective.
+        const bool ready =
+            mbar_wait(bar_tfull + 8 * buf, uint32_t(q >> 1) & 1u, p.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, ready)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_d + (uint32_t(32 * quarter) << 16) +
+                               uint32_t(buf * kTcBN + half * (kTcBN / 2));
 #pragma unroll
-      for (int c = 0; c < kTcBN / 2; c += 32) {
-        float v[32];
+        for (int cc = 0; cc < kTcBN / 2; cc += 8) {
+          float v[8];
+          __syncwarp();
+          tmem_load_8(taddr + uint32_t(cc), v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[cc + j] += v[j];
+        }
+        tc_fence_before();
         __syncwarp();
-        tmem_load_32(taddr + uint32_t(c), v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[c + j] += v[j];
+        if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
-    }
-    // Epilogue: this thread's row, 128 consecutive columns.
-    const int row = m0 + 32 * quarter + lane;
-    const int col0 = n0 + half * (kTcBN / 2);
-    if (!timed_out && row < p.M) {
-      float *c_row = p.C + int64_t(row) * p.ldc;
+      if (timed_out) break;
+      int tm, tn;
+      tc3_tile_coords(tile, p.tiles_n, tm, tn);
+      const int row = tm * kTcBM + 32 * quarter + lane;
+      const int col0 = tn * kTcBN + half * (kTcBN / 2);
+      const bool owner_of_split = kb == 0 && ke < p.slices;   // slices [ke, S): unit + 1
+      if (owner_of_split) {
+        if (lane == 0) {
+          const unsigned int *f = &flags[(unit + 1) * kTc3FlagsPerBlock + acc_warp];
+          const uint64_t t0 = timer_ns();
+          while (ld_acquire_u32(f) != p.epoch) {
+            if (int64_t(timer_ns() - t0) > p.wait_limit_ns) {
+              atomicOr(&g_tc3_status, 2u);
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+        __syncwarp();
+      }
+      if (row < p.M) {
+        float *c_row = p.C + int64_t(row) * p.ldc;
 #pragma unroll
-      for (int c = 0; c < kTcBN / 2; c += 4) {
-        const int col = col0 + c;
-        if (p.vec_store && col + 4 <= p.N) {
-          *reinterpret_cast<float4 *>(c_row + col) =
-              make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-        } else {
+        for (int c = 0; c < kTcBN / 2; c += 4) {
+          const int col = col0 + c;
+          if (p.vec_store && col + 4 <= p.N) {
+            float4 v = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+            if (owner_of_split) {
+              const float4 w = __ldcg(reinterpret_cast<const float4 *>(c_row + col));
+              v.x = w.x + v.x; v.y = w.y + v.y; v.z = w.z + v.z; v.w = w.w + v.w;
+            }
+            *reinterpret_cast<float4 *>(c_row + col) = v;
+          } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (col + j < p.N) c_row[col + j] = acc[c + j];
+            for (int j = 0; j < 4; ++j)
+              if (col + j < p.N) {
+                float v = acc[c + j];
+                if (owner_of_split) v = __ldcg(c_row + col + j) + v;
+                c_row[col + j] = v;
+              }
+          }
+        }
+      }
+      if (kb > 0) {
+        // Slices [kb, S) of a split tile: this warp's partial sums are in C.
+        __syncwarp();
+        if (lane == 0 && unit != p.drop_signal_block) {
+          __threadfence();
+          st_release_u32(&flags[unit * kTc3FlagsPerBlock + acc_warp], p.epoch);
         }
       }
     }
   }
   __syncwarp();
-  if (threadIdx.x == 32) {
-    // The final commit above arrives once all products are done: wait for it.
-    const int i = num_k;
-    if (!mbar_wait(bar_empty + 8 * (i % kTcStages), uint32_t(i / kTcStages) & 1u,
-                   p.wait_limit_ns))
-      timed_out = true;
-  }
   if (timed_out) atomicOr(&g_tc3_status, 2u);
 
   tc_fence_before();
@@ -448,7 +559,10 @@ cudaError_t encode_operand(CUtensorMap *map, const float *base, int64_t rows, in
 }
 
 std::atomic<uint64_t> g_tc3_configured{0};
+std::atomic<int> g_tc3_blocks_per_sm[64];
 std::atomic<int64_t> g_tc3_wait_limit_ns{int64_t(10) * 1000 * 1000 * 1000};
+std::atomic<unsigned int> g_tc3_epoch{0};
+std::atomic<int> g_tc3_drop_signal_block{-1};
 
 }  // namespace
 
@@ -471,10 +585,10 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
 
   // 1. split pre-pass.
   {
-    const int64_t total = p.M * Kp;
-    const int64_t blocks = std::min<int64_t>((total + 255) / 256, int64_t(dev.sm_count) * 32);
-    tc3_split_a_kernel<<<unsigned(blocks), 256, 0, stream>>>(int(p.M), int(p.K), int(Kp), p.A,
-                                                             p.lda, a_hi, a_lo);
+    const bool vec_a = (reinterpret_cast<uintptr_t>(p.A) & 15u) == 0 && p.lda % 4 == 0;
+    const dim3 grid_a(unsigned((Kp / 4 + 255) / 256), unsigned(std::min<int64_t>(p.M, 65535)));
+    tc3_split_a_kernel<<<grid_a, 256, 0, stream>>>(int(p.M), int(p.K), int(Kp), p.A, p.lda,
+                                                   vec_a ? 1 : 0, a_hi, a_lo);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const dim3 grid(unsigned((p.N + 31) / 32), unsigned(Kp / 32));
     tc3_split_bt_kernel<<<grid, dim3(32, 8), 0, stream>>>(int(p.K), int(p.N), int(Kp), p.B, p.ldb,
@@ -494,21 +608,51 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
     e = cudaFuncSetAttribute(gemm_tc3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kTcSmemBytes));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_tc3_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int nb = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, gemm_tc3_kernel, kTcThreads,
+                                                      kTcSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (nb < 1) return cudaErrorLaunchOutOfResources;
+    g_tc3_blocks_per_sm[dev.id & 63].store(nb, std::memory_order_relaxed);
     g_tc3_configured.fetch_or(bit, std::memory_order_release);
   }
+  // One block per tile; a last wave at most half full is split along K.
+  const int64_t tiles_m = (p.M + kTcBM - 1) / kTcBM;
+  const int64_t tiles_n = (p.N + kTcBN - 1) / kTcBN;
+  const int64_t tiles = tiles_m * tiles_n;
+  const int slices = int(Kp / kTcBK);
+  constexpr int kSlicesPerChunk = kTcChunk / kTcBK;
+  const int64_t slots =
+      int64_t(g_tc3_blocks_per_sm[dev.id & 63].load(std::memory_order_relaxed)) * dev.sm_count;
+  const int64_t rem = slots > 0 ? tiles % slots : 0;
+  const bool split_tail = tiles > slots && rem > 0 && 2 * rem <= slots &&
+                          2 * rem <= kTc3MaxBlocks && slices >= 2 * kSlicesPerChunk;
+  if (tiles + (split_tail ? rem : 0) > 0x7fffffff) return cudaErrorInvalidConfiguration;
   Tc3Params prm = {};
   prm.M = int(p.M);
   prm.N = int(p.N);
   prm.Kp = int(Kp);
   prm.C = p.C;
   prm.ldc = p.ldc;
-  prm.tiles_n = int((p.N + kTcBN - 1) / kTcBN);
+  prm.tiles_m = int(tiles_m);
+  prm.tiles_n = int(tiles_n);
+  prm.slices = slices;
   prm.vec_store = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0) ? 1 : 0;
   prm.wait_limit_ns = g_tc3_wait_limit_ns.load(std::memory_order_relaxed);
-  const int64_t tiles = int64_t(prm.tiles_n) * ((p.M + kTcBM - 1) / kTcBM);
-  if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  gemm_tc3_kernel<<<unsigned(tiles), kTcThreads, kTcSmemBytes, stream>>>(maps[0], maps[1], maps[2],
-                                                                         maps[3], prm);
+  prm.drop_signal_block = g_tc3_drop_signal_block.load(std::memory_order_relaxed);
+  // The halves meet at a chunk boundary near the middle of K.
+  prm.split = std::max(kSlicesPerChunk, (slices / 2) / kSlicesPerChunk * kSlicesPerChunk);
+  prm.dp_tiles = int(split_tail ? tiles - rem : tiles);
+  const int64_t grid = split_tail ? (tiles - rem) + 2 * rem : tiles;
+  unsigned int ep = g_tc3_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (ep == 0) ep = g_tc3_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  prm.epoch = ep;
+
+  gemm_tc3_kernel<<<unsigned(grid), kTcThreads, kTcSmemBytes, stream>>>(maps[0], maps[1],
+                                                                       maps[2], maps[3], prm);
   return cudaGetLastError();
 }
 
@@ -519,7 +663,8 @@ cudaError_t tc3_device_status(unsigned int *status, bool clear) {
   return cudaMemcpyToSymbol(g_tc3_status, &zero, sizeof(unsigned int));
 }
 
-void tc3_set_wait_limit(int64_t wait_limit_ns) {
+void tc3_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns) {
+  g_tc3_drop_signal_block.store(drop_signal_block, std::memory_order_relaxed);
   g_tc3_wait_limit_ns.store(wait_limit_ns > 0 ? wait_limit_ns : int64_t(10) * 1000 * 1000 * 1000,
                             std::memory_order_relaxed);
 }

@@ -41,7 +41,7 @@ cudaError_t tc3_device_status(unsigned int *status, bool clear);
 // address of it (looked up once per device; `device` must be current).
 size_t tc3_noalloc_scratch_bytes();
 cudaError_t tc3_noalloc_scratch(int device, void **ptr);
-void tc3_set_wait_limit(int64_t wait_limit_ns);
+void tc3_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns);
 
 // Device status word of the tiled kernel (bit 0: a bounded wait ran out of
 // time); read from the current device, optionally cleared.
