@@ -427,7 +427,8 @@ def tc3_leg(args, w, A, B, C, flush, stream, peaks) -> dict:
             "steps": steps, "gpu_launches": launches["n"] - 3 * args.warmup,
             "workspace_bytes": need,
             "roofline": {"bound": "tensor", "achieved": tensor_tflops, "peak": peak, "unit": UNIT,
-                         "frac": tensor_tflops / peak, "traffic": None,
+                         "frac": tensor_tflops / peak,
+                         "traffic": recorded_traffic("gemm_tc3", w.name),
                          "peak_source": ("MEASURED_PEAKS.json bf16_tflops x 1.1/2.25 (nominal "
                                          "TF32/BF16 dense ratio)" if bf16 else
                                          "fallback 1.9 PFLOP/s bf16 x 1.1/2.25"),
