@@ -366,6 +366,8 @@ def run_ours(args, world, rank, local):
     extra = {}
     if not args.no_tc3 and rank == 0:
         extra["tc3"] = tc3_leg(args, w, A, B, C, flush, stream, peaks)
+    if not args.no_layouts and rank == 0:
+        extra["layouts"] = layouts_leg(args, w, A, B, C, flush, stream)
     if not args.no_contrast and rank == 0:
         extra["contrast"] = contrast_paths(args, w, A, B, C, flush, stream, props, peaks)
 
@@ -436,6 +438,40 @@ def tc3_leg(args, w, A, B, C, flush, stream, peaks) -> dict:
                                         "(split pre-pass included in the step time)"}}
 
 
+def layouts_leg(args, w, A, B, C, flush, stream) -> dict:
+    """The same product with A and/or B stored transposed (gemm_f32_ex, gemm_f32_tc3_ex):
+    op(A) = A^T reads A stored K x M, the layout of "CMU DLSys Lecture 12" section 4."""
+    import torch
+    from tiled_matrix_multiply_gb300 import _abi
+    lib = _abi.load()
+    At = A.t().contiguous()     # stored K x M
+    Bt = B.t().contiguous()     # stored N x K
+    need = int(lib.gemm_f32_tc3_workspace_size(w.M, w.N, w.K))
+    ws = torch.empty(need + 256, dtype=torch.uint8, device=A.device)
+    wptr = (ws.data_ptr() + 255) // 256 * 256
+    out = {}
+    steps = max(3, min(args.steps, 50))
+    for name, ta, tb in (("tn", 1, 0), ("nt", 0, 1), ("tt", 1, 1)):
+        a, lda = (At, w.M) if ta else (A, w.K)
+        b, ldb = (Bt, w.K) if tb else (B, w.N)
+
+        def simt():
+            rc = lib.gemm_f32_ex(ta, tb, w.M, w.N, w.K, a.data_ptr(), lda, b.data_ptr(), ldb,
+                                 C.data_ptr(), w.N, stream.cuda_stream)
+            assert rc == _abi.TMM_OK, _abi.last_error()
+
+        def tc3():
+            rc = lib.gemm_f32_tc3_ex(ta, tb, w.M, w.N, w.K, a.data_ptr(), lda, b.data_ptr(), ldb,
+                                     C.data_ptr(), w.N, wptr, need, stream.cuda_stream)
+            assert rc == _abi.TMM_OK, _abi.last_error()
+        rec = {}
+        for label, fn in (("gemm_f32_ex", simt), ("gemm_f32_tc3_ex", tc3)):
+            ms = statistics.mean(time_device(fn, flush, steps, args.warmup, stream, None))
+            rec[label] = {"value": w.flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms}
+        out[name] = rec
+    return {"steps": steps, "transa_transb": {"tn": [1, 0], "nt": [0, 1], "tt": [1, 1]}, **out}
+
+
 def contrast_paths(args, w, A, B, C, flush, stream, props, peaks) -> dict:
     """The naive kernel on the same workload (a few steps): the untiled contrast."""
     import torch
@@ -463,6 +499,8 @@ def main(argv=None):
     ap.add_argument("--no-contrast", action="store_true", help="skip the naive-kernel contrast")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-tc3", action="store_true", help="skip the tensor-core (3xTF32) leg")
+    ap.add_argument("--no-layouts", action="store_true",
+                    help="skip the transposed-layout (gemm_f32_ex, gemm_f32_tc3_ex) leg")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps, always
     world, rank, local = dist_env()

@@ -99,6 +99,25 @@ int gemm_f32(int64_t M, int64_t N, int64_t K,
              tmm_stream_t stream);
 
 /*
+ * gemm_f32_ex -- gemm_f32 with either operand read transposed:
+ *     C = op(A) x op(B),  op(A) = A   (transa = 0, A stored M x K, lda >= max(1, K))
+ *                                 A^T (transa = 1, A stored K x M, lda >= max(1, M))
+ *                         op(B) = B   (transb = 0, B stored K x N, ldb >= max(1, N))
+ *                                 B^T (transb = 1, B stored N x K, ldb >= max(1, K)).
+ * transa = 1, transb = 0 is the layout of "CMU DLSys Lecture 12" section 4,
+ * C_ij = sum_k A_ki B_kj.  Only the copy of the slabs into shared memory
+ * changes with the layout (the shared-memory slabs are k-major in every
+ * case); the register tiles, scheduling and contract are gemm_f32's.
+ * TMM_ERR_INVALID_ARG also for transa or transb not 0 or 1.
+ */
+int gemm_f32_ex(int transa, int transb,
+                int64_t M, int64_t N, int64_t K,
+                const float *A, int64_t lda,
+                const float *B, int64_t ldb,
+                float *C, int64_t ldc,
+                tmm_stream_t stream);
+
+/*
  * gemm_f32_naive -- one output per thread, each walking a row of A and a
  * column of B straight from global memory ("Tiling Strategies" section 2,
  * "The Problem"; "CMU DLSys Lecture 12" section 1 for the bounds-checked
@@ -136,6 +155,17 @@ int gemm_f32_tc3(int64_t M, int64_t N, int64_t K,
                  float *C, int64_t ldc,
                  void *workspace, size_t workspace_bytes,
                  tmm_stream_t stream);
+
+/* gemm_f32_tc3 with either operand read transposed (transa, transb as for
+ * gemm_f32_ex); the split pre-pass reads the operands in their stored layout.
+ * Same workspace size as gemm_f32_tc3. */
+int gemm_f32_tc3_ex(int transa, int transb,
+                    int64_t M, int64_t N, int64_t K,
+                    const float *A, int64_t lda,
+                    const float *B, int64_t ldb,
+                    float *C, int64_t ldc,
+                    void *workspace, size_t workspace_bytes,
+                    tmm_stream_t stream);
 
 /* Workspace bytes gemm_f32_tc3 needs for an M x N x K product (0 for an empty
  * product or sizes out of range):  4 Kp (2M + 2N) rounded to 256-byte

@@ -93,3 +93,16 @@ def test_python_binding_rejects_host_tensors():
         tmm.gemm_f32(A, A)
     with pytest.raises(TypeError):
         tmm.gemm_f32(A.double(), A.double())
+
+
+@pytest.mark.parametrize("entry", ["gemm_f32_ex", "gemm_f32_tc3_ex"])
+@pytest.mark.parametrize("trans,args", [
+    ((2, 0), (4, 4, 4, FAKE, 4, FAKE + (1 << 20), 4, FAKE + (2 << 20), 4)),   # bad transa
+    ((0, -1), (4, 4, 4, FAKE, 4, FAKE + (1 << 20), 4, FAKE + (2 << 20), 4)),  # bad transb
+    ((1, 0), (8, 4, 6, FAKE, 6, FAKE + (1 << 20), 4, FAKE + (2 << 20), 4)),   # A^T: lda < M
+    ((0, 1), (8, 4, 6, FAKE, 6, FAKE + (1 << 20), 4, FAKE + (2 << 20), 4)),   # B^T: ldb < K
+])
+def test_ex_entry_points_reject_bad_layouts(lib, entry, trans, args):
+    extra = (0, 0) if entry == "gemm_f32_tc3_ex" else ()
+    rc = getattr(lib, entry)(*trans, *args, *extra, None)
+    assert rc == _abi.TMM_ERR_INVALID_ARG

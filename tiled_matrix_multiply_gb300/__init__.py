@@ -22,7 +22,13 @@ __all__ = ["gemm_f32", "gemm_f32_naive", "gemm_f32_tc3", "tc3_workspace_bytes",
            "check_device", "raw_call", "TmmError"]
 
 
-def _matrix(x, name):
+def _matrix(x, name, allow_transposed=False):
+    """(rows, cols, ld, trans) of a float32 CUDA matrix.
+
+    trans = 0: row-major (unit column stride, ld = row stride); trans = 1: a
+    transposed view of a row-major matrix (unit row stride, ld = column stride),
+    accepted only where the entry point can read the operand transposed.
+    """
     import torch
     if not isinstance(x, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -33,19 +39,23 @@ def _matrix(x, name):
     if not x.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     rows, cols = x.shape
-    if cols > 1 and x.stride(1) != 1:
-        raise ValueError(f"{name} must be row-major (unit column stride)")
-    ld = x.stride(0) if rows > 1 else max(cols, 1)
-    if x.numel() and ld < cols:
-        raise ValueError(f"{name} has a row stride shorter than its rows")
-    return rows, cols, max(ld, cols, 1)
+    if cols <= 1 or x.stride(1) == 1:
+        ld = x.stride(0) if rows > 1 else max(cols, 1)
+        if x.numel() and ld < cols:
+            raise ValueError(f"{name} has a row stride shorter than its rows")
+        return rows, cols, max(ld, cols, 1), 0
+    if allow_transposed and (rows <= 1 or x.stride(0) == 1) and x.stride(1) >= rows:
+        return rows, cols, max(x.stride(1), rows, 1), 1
+    raise ValueError(f"{name} must be row-major (unit column stride)"
+                     + (" or a transposed row-major view" if allow_transposed else ""))
 
 
 def _product(entry: str, A, B, C=None, stream=None):
     import torch
     from . import _abi
-    M, K, lda = _matrix(A, "A")
-    K2, N, ldb = _matrix(B, "B")
+    transposable = entry == "gemm_f32"
+    M, K, lda, ta = _matrix(A, "A", transposable)
+    K2, N, ldb, tb = _matrix(B, "B", transposable)
     if K != K2:
         raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
     if A.device != B.device:
@@ -54,16 +64,26 @@ def _product(entry: str, A, B, C=None, stream=None):
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     elif C.shape != (M, N) or C.device != A.device:
         raise ValueError(f"C must be ({M}, {N}) on {A.device}")
-    _, _, ldc = _matrix(C, "C")
+    _, _, ldc, _ = _matrix(C, "C")
     with torch.cuda.device(A.device):
         s = stream if stream is not None else torch.cuda.current_stream(A.device)
-        _abi.check(entry, M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
-                   s.cuda_stream)
+        if ta or tb:
+            rc = _abi.load().gemm_f32_ex(ta, tb, M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
+                                         C.data_ptr(), ldc, s.cuda_stream)
+            if rc != _abi.TMM_OK:
+                raise _abi.TmmError("gemm_f32_ex", rc, _abi.last_error())
+        else:
+            _abi.check(entry, M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
+                       s.cuda_stream)
     return C
 
 
 def gemm_f32(A, B, C=None, stream=None):
-    """C = A x B on the tiled FFMA path (C allocated when not given)."""
+    """C = A x B on the tiled FFMA path (C allocated when not given).
+
+    A and B may also be transposed views of row-major matrices (``X.t()``):
+    they are read transposed in place, without a copy.
+    """
     return _product("gemm_f32", A, B, C, stream)
 
 
@@ -81,14 +101,15 @@ def tc3_workspace_bytes(M: int, N: int, K: int) -> int:
 def gemm_f32_tc3(A, B, C=None, workspace=None, stream=None):
     """C = A x B on the tensor cores (3 x TF32 split products, FP32 accumulation).
 
+    A and B may be transposed views of row-major matrices, as for gemm_f32.
     ``workspace``: a CUDA tensor of at least ``tc3_workspace_bytes(M, N, K)``
     bytes whose storage starts 256-byte aligned (torch allocations do); one is
     allocated when not given.
     """
     import torch
     from . import _abi
-    M, K, lda = _matrix(A, "A")
-    K2, N, ldb = _matrix(B, "B")
+    M, K, lda, ta = _matrix(A, "A", True)
+    K2, N, ldb, tb = _matrix(B, "B", True)
     if K != K2:
         raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
     if A.device != B.device:
@@ -97,16 +118,16 @@ def gemm_f32_tc3(A, B, C=None, workspace=None, stream=None):
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     elif C.shape != (M, N) or C.device != A.device:
         raise ValueError(f"C must be ({M}, {N}) on {A.device}")
-    _, _, ldc = _matrix(C, "C")
+    _, _, ldc, _ = _matrix(C, "C")
     need = tc3_workspace_bytes(M, N, K)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(A.device):
         s = stream if stream is not None else torch.cuda.current_stream(A.device)
-        rc = _abi.load().gemm_f32_tc3(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
-                                      C.data_ptr(), ldc, workspace.data_ptr(), ws_bytes,
-                                      s.cuda_stream)
+        rc = _abi.load().gemm_f32_tc3_ex(ta, tb, M, N, K, A.data_ptr(), lda, B.data_ptr(),
+                                         ldb, C.data_ptr(), ldc, workspace.data_ptr(), ws_bytes,
+                                         s.cuda_stream)
         if rc != _abi.TMM_OK:
             raise _abi.TmmError("gemm_f32_tc3", rc, _abi.last_error())
     return C

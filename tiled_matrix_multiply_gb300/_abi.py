@@ -32,8 +32,8 @@ STATUS_NAMES = {
 # (M, N, K, A, lda, B, ldb, C, ldc, stream) -> int.
 GEMM_ENTRY_POINTS = ("gemm_f32", "gemm_f32_naive")
 # Every symbol include/tmm_gemm.h declares.
-EXPORTED = GEMM_ENTRY_POINTS + ("gemm_f32_tc3", "gemm_f32_tc3_workspace_size",
-                                 "gemm_f32_tc3_noalloc",
+EXPORTED = GEMM_ENTRY_POINTS + ("gemm_f32_ex", "gemm_f32_tc3", "gemm_f32_tc3_ex",
+                                 "gemm_f32_tc3_workspace_size", "gemm_f32_tc3_noalloc",
                                  "tmm_check_device", "tmm_testing_set_wait_hooks",
                                  "tmm_last_error_string", "tmm_version")
 
@@ -73,6 +73,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gemm_f32_tc3.argtypes = [i64, i64, i64, ptr, i64, ptr, i64, ptr, i64, ptr,
                                      ctypes.c_size_t, ptr]
         lib.gemm_f32_tc3.restype = ctypes.c_int
+        ci = ctypes.c_int
+        lib.gemm_f32_ex.argtypes = [ci, ci, i64, i64, i64, ptr, i64, ptr, i64, ptr, i64, ptr]
+        lib.gemm_f32_ex.restype = ctypes.c_int
+        lib.gemm_f32_tc3_ex.argtypes = [ci, ci, i64, i64, i64, ptr, i64, ptr, i64, ptr, i64,
+                                        ptr, ctypes.c_size_t, ptr]
+        lib.gemm_f32_tc3_ex.restype = ctypes.c_int
         lib.gemm_f32_tc3_noalloc.argtypes = [i64, i64, i64, ptr, i64, ptr, i64, ptr, i64, ptr]
         lib.gemm_f32_tc3_noalloc.restype = ctypes.c_int
         lib.gemm_f32_tc3_workspace_size.argtypes = [i64, i64, i64]

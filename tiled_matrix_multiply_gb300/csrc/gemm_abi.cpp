@@ -82,20 +82,30 @@ bool overlaps(uintptr_t a_lo, uintptr_t a_hi, uintptr_t b_lo, uintptr_t b_hi) {
 }
 
 // Checks shared by every entry point; on success *nothing_to_do tells whether
-// the call is a no-op (M == 0 or N == 0).
-int check_args(const char *who, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
-               const float *B, int64_t ldb, const float *C, int64_t ldc, bool *nothing_to_do) {
+// the call is a no-op (M == 0 or N == 0).  transa/transb select how A and B
+// are stored: A as M x K (0) or K x M (1), B as K x N (0) or N x K (1).
+int check_args(const char *who, int64_t M, int64_t N, int64_t K, int transa, int transb,
+               const float *A, int64_t lda, const float *B, int64_t ldb, const float *C,
+               int64_t ldc, bool *nothing_to_do) {
   *nothing_to_do = false;
+  if ((transa != 0 && transa != 1) || (transb != 0 && transb != 1))
+    return fail(TMM_ERR_INVALID_ARG, "%s: transa and transb must be 0 or 1", who);
   if (M < 0 || N < 0 || K < 0)
     return fail(TMM_ERR_INVALID_ARG, "%s: negative size (M=%lld N=%lld K=%lld)", who,
                 (long long)M, (long long)N, (long long)K);
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
     return fail(TMM_ERR_INVALID_ARG, "%s: sizes above 2^31-1 are not supported", who);
-  const int64_t min_lda = K > 1 ? K : 1, min_ldn = N > 1 ? N : 1;
-  if (lda < min_lda || ldb < min_ldn || ldc < min_ldn)
+  const int64_t a_rows = transa ? K : M, a_cols = transa ? M : K;
+  const int64_t b_rows = transb ? N : K, b_cols = transb ? K : N;
+  const int64_t min_lda = a_cols > 1 ? a_cols : 1, min_ldb = b_cols > 1 ? b_cols : 1;
+  const int64_t min_ldc = N > 1 ? N : 1;
+  if (lda < min_lda || ldb < min_ldb || ldc < min_ldc)
     return fail(TMM_ERR_INVALID_ARG,
-                "%s: leading dimension too small (lda=%lld ldb=%lld ldc=%lld for K=%lld N=%lld)",
-                who, (long long)lda, (long long)ldb, (long long)ldc, (long long)K, (long long)N);
+                "%s: leading dimension too small (lda=%lld ldb=%lld ldc=%lld for stored A %lldx%lld, "
+                "B %lldx%lld, C %lldx%lld)",
+                who, (long long)lda, (long long)ldb, (long long)ldc, (long long)a_rows,
+                (long long)a_cols, (long long)b_rows, (long long)b_cols, (long long)M,
+                (long long)N);
   if (M == 0 || N == 0) {
     *nothing_to_do = true;
     return TMM_OK;
@@ -103,7 +113,7 @@ int check_args(const char *who, int64_t M, int64_t N, int64_t K, const float *A,
   if (C == nullptr) return fail(TMM_ERR_INVALID_ARG, "%s: C is NULL", who);
   if (K > 0 && (A == nullptr || B == nullptr))
     return fail(TMM_ERR_INVALID_ARG, "%s: A or B is NULL", who);
-  if (!span_ok(M, lda, K) || !span_ok(K, ldb, N) || !span_ok(M, ldc, N))
+  if (!span_ok(a_rows, lda, a_cols) || !span_ok(b_rows, ldb, b_cols) || !span_ok(M, ldc, N))
     return fail(TMM_ERR_INVALID_ARG, "%s: matrix extent overflows 64-bit byte offsets", who);
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
        reinterpret_cast<uintptr_t>(C)) & 3u)
@@ -111,8 +121,8 @@ int check_args(const char *who, int64_t M, int64_t N, int64_t K, const float *A,
   if (K > 0) {
     uintptr_t c_lo, c_hi, a_lo, a_hi, b_lo, b_hi;
     byte_span(C, M, ldc, N, &c_lo, &c_hi);
-    byte_span(A, M, lda, K, &a_lo, &a_hi);
-    byte_span(B, K, ldb, N, &b_lo, &b_hi);
+    byte_span(A, a_rows, lda, a_cols, &a_lo, &a_hi);
+    byte_span(B, b_rows, ldb, b_cols, &b_lo, &b_hi);
     if (overlaps(c_lo, c_hi, a_lo, a_hi) || overlaps(c_lo, c_hi, b_lo, b_hi))
       return fail(TMM_ERR_ALIAS, "%s: the byte range of C overlaps A or B", who);
   }
@@ -121,10 +131,11 @@ int check_args(const char *who, int64_t M, int64_t N, int64_t K, const float *A,
 
 using Launcher = cudaError_t (*)(const tmm::GemmProblem &, const tmm::DeviceInfo &, cudaStream_t);
 
-int run(const char *who, Launcher launch, int64_t M, int64_t N, int64_t K, const float *A,
-        int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc, tmm_stream_t stream) {
+int run(const char *who, Launcher launch, int transa, int transb, int64_t M, int64_t N,
+        int64_t K, const float *A, int64_t lda, const float *B, int64_t ldb, float *C,
+        int64_t ldc, tmm_stream_t stream) {
   bool noop = false;
-  int rc = check_args(who, M, N, K, A, lda, B, ldb, C, ldc, &noop);
+  int rc = check_args(who, M, N, K, transa, transb, A, lda, B, ldb, C, ldc, &noop);
   if (rc != TMM_OK || noop) return rc;
   tmm::DeviceInfo dev;
   if ((rc = current_device(&dev)) != TMM_OK) return rc;
@@ -138,7 +149,9 @@ int run(const char *who, Launcher launch, int64_t M, int64_t N, int64_t K, const
       return fail(TMM_ERR_CUDA, "%s: cudaMemset2DAsync: %s", who, cudaGetErrorString(e));
     return TMM_OK;
   }
-  const tmm::GemmProblem p = {M, N, K, A, lda, B, ldb, C, ldc};
+  tmm::GemmProblem p = {M, N, K, A, lda, B, ldb, C, ldc};
+  p.transa = transa;
+  p.transb = transb;
   e = launch(p, dev, s);
   if (e != cudaSuccess) return fail(TMM_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
   return TMM_OK;
@@ -150,12 +163,20 @@ extern "C" {
 
 int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
              int64_t ldb, float *C, int64_t ldc, tmm_stream_t stream) {
-  return run("gemm_f32", tmm::launch_simt, M, N, K, A, lda, B, ldb, C, ldc, stream);
+  return run("gemm_f32", tmm::launch_simt, 0, 0, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+int gemm_f32_ex(int transa, int transb, int64_t M, int64_t N, int64_t K, const float *A,
+                int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
+                tmm_stream_t stream) {
+  return run("gemm_f32_ex", tmm::launch_simt, transa, transb, M, N, K, A, lda, B, ldb, C, ldc,
+             stream);
 }
 
 int gemm_f32_naive(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
                    int64_t ldb, float *C, int64_t ldc, tmm_stream_t stream) {
-  return run("gemm_f32_naive", tmm::launch_naive, M, N, K, A, lda, B, ldb, C, ldc, stream);
+  return run("gemm_f32_naive", tmm::launch_naive, 0, 0, M, N, K, A, lda, B, ldb, C, ldc,
+             stream);
 }
 
 int tmm_check_device(tmm_stream_t stream) {
@@ -186,12 +207,12 @@ size_t gemm_f32_tc3_workspace_size(int64_t M, int64_t N, int64_t K) {
   return tmm::tc3_workspace_bytes(M, N, K);
 }
 
-int gemm_f32_tc3(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
-                 int64_t ldb, float *C, int64_t ldc, void *workspace, size_t workspace_bytes,
-                 tmm_stream_t stream) {
+int gemm_f32_tc3_ex(int transa, int transb, int64_t M, int64_t N, int64_t K, const float *A,
+                    int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
+                    void *workspace, size_t workspace_bytes, tmm_stream_t stream) {
   const char *who = "gemm_f32_tc3";
   bool noop = false;
-  int rc = check_args(who, M, N, K, A, lda, B, ldb, C, ldc, &noop);
+  int rc = check_args(who, M, N, K, transa, transb, A, lda, B, ldb, C, ldc, &noop);
   if (rc != TMM_OK || noop) return rc;
   tmm::DeviceInfo dev;
   if ((rc = current_device(&dev)) != TMM_OK) return rc;
@@ -212,17 +233,26 @@ int gemm_f32_tc3(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, c
   {
     uintptr_t c_lo, c_hi, a_lo, a_hi, b_lo, b_hi;
     byte_span(C, M, ldc, N, &c_lo, &c_hi);
-    byte_span(A, M, lda, K, &a_lo, &a_hi);
-    byte_span(B, K, ldb, N, &b_lo, &b_hi);
+    byte_span(A, transa ? K : M, lda, transa ? M : K, &a_lo, &a_hi);
+    byte_span(B, transb ? N : K, ldb, transb ? K : N, &b_lo, &b_hi);
     const uintptr_t w_lo = reinterpret_cast<uintptr_t>(workspace), w_hi = w_lo + need;
     if (overlaps(w_lo, w_hi, c_lo, c_hi) || overlaps(w_lo, w_hi, a_lo, a_hi) ||
         overlaps(w_lo, w_hi, b_lo, b_hi))
       return fail(TMM_ERR_ALIAS, "%s: the workspace overlaps A, B or C", who);
   }
-  const tmm::GemmProblem p = {M, N, K, A, lda, B, ldb, C, ldc};
+  tmm::GemmProblem p = {M, N, K, A, lda, B, ldb, C, ldc};
+  p.transa = transa;
+  p.transb = transb;
   cudaError_t e = tmm::launch_tc3(p, dev, workspace, s);
   if (e != cudaSuccess) return fail(TMM_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
   return TMM_OK;
+}
+
+int gemm_f32_tc3(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                 int64_t ldb, float *C, int64_t ldc, void *workspace, size_t workspace_bytes,
+                 tmm_stream_t stream) {
+  return gemm_f32_tc3_ex(0, 0, M, N, K, A, lda, B, ldb, C, ldc, workspace, workspace_bytes,
+                         stream);
 }
 
 int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
@@ -230,7 +260,7 @@ int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_
                          tmm_stream_t stream) {
   const char *who = "gemm_f32_tc3_noalloc";
   bool noop = false;
-  int rc = check_args(who, M, N, K, A, lda, B, ldb, C, ldc, &noop);
+  int rc = check_args(who, M, N, K, 0, 0, A, lda, B, ldb, C, ldc, &noop);
   if (rc != TMM_OK || noop) return rc;
   tmm::DeviceInfo dev;
   if ((rc = current_device(&dev)) != TMM_OK) return rc;

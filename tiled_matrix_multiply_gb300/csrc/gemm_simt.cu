@@ -71,6 +71,15 @@ namespace {
 
 constexpr int kGroupM = 16;
 
+// How an operand slab reaches its k-major shared-memory layout:
+//   kCopyTransposing  -- the stored rows run along m (A) or n (B) with k contiguous,
+//                        so each element is placed by a 4-byte copy (4 rows x 8 k per
+//                        warp instruction, into 32 distinct banks);
+//   kCopyVec          -- the stored rows run along k, contiguous in m or n, 16-byte
+//                        aligned: whole 16-byte vectors;
+//   kCopyScalar       -- as kCopyVec without the alignment: 4-byte copies.
+constexpr int kCopyTransposing = 0, kCopyVec = 1, kCopyScalar = 2;
+
 template <int TM_, int TN_, int kWarpsM_, int kWarpsN_, int BK_, int kStages_, int kMinBlocks_>
 struct SimtConfig {
   static constexpr int TM = TM_, TN = TN_;
@@ -84,10 +93,21 @@ struct SimtConfig {
   static constexpr int kThreads = 32 * kWarpsM * kWarpsN;
   static constexpr int kWarps = kWarpsM * kWarpsN;
   static constexpr int kMinBlocks = kMinBlocks_;
+  // Row pitches of the k-major slabs; both are 4 mod 32 floats when filled by
+  // transposing copies, which spreads a warp's 4 rows x 8 k over 32 banks.
   static constexpr int kAsLd = BM + 4;
-  static constexpr int kBsLd = BN;
-  static constexpr int kStageFloats = BK * kAsLd + BK * kBsLd;
-  static constexpr int kSmemBytes = kStages * kStageFloats * 4;
+  template <int kBCopy>
+  __host__ __device__ static constexpr int bs_ld() {
+    return kBCopy == kCopyTransposing ? BN + 4 : BN;
+  }
+  template <int kBCopy>
+  __host__ __device__ static constexpr int stage_floats() {
+    return BK * kAsLd + BK * bs_ld<kBCopy>();
+  }
+  template <int kBCopy>
+  __host__ __device__ static constexpr int smem_bytes() {
+    return kStages * stage_floats<kBCopy>() * 4;
+  }
   // A copies: groups of 4 rows x 8 k per warp instruction.
   static constexpr int kARowGroups = BM / 4;
   static constexpr int kARowGroupsPerWarp = kARowGroups / kWarps;
@@ -101,6 +121,10 @@ struct SimtConfig {
   static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tiles are made of 4 x 4 quadrants");
   static_assert(BK % 8 == 0 && BK % kKUnroll == 0, "slice depth");
   static_assert(kARowGroups % kWarps == 0, "A copy groups divide among warps");
+  static_assert((BN / 4) % kWarps == 0, "transposing B copy groups divide among warps");
+  static_assert(kThreads % (BM / 4) == 0 && (BK * BM) % (4 * kThreads) == 0 &&
+                (BK * BM) % kThreads == 0 && BM % 32 == 0, "direct A copies");
+  static_assert(kAsLd % 32 == 4 && (BN + 4) % 32 == 4, "pitches for transposing copies");
   static_assert(kThreads % kBVecPerRow == 0, "B vector copies cover whole rows");
   static_assert((BK * BN) % (4 * kThreads) == 0 && (BK * BN) % kThreads == 0, "B copies");
   static_assert(BN % 32 == 0, "scalar B copies: a warp copies 32 consecutive columns");
@@ -184,6 +208,7 @@ struct SimtParams {
   float *C;
   int64_t ldc;
   int tiles_m, tiles_n;
+  int vec_store;         // C 16-byte aligned and ldc, N multiples of 4
   int slices;            // K-slices per tile
   int dp_tiles;          // tiles [0, dp_tiles) are processed whole, striding by gridDim.x
   int64_t sk_iters;      // (tiles - dp_tiles) * slices, divided evenly among the blocks
@@ -192,8 +217,10 @@ struct SimtParams {
   int drop_signal_block; // testing hook: this block never raises its flag (-1: none)
 };
 
-// One block's work on tile `tile`, K-slices [s_begin, s_end).
-template <class Cf, bool kVecB, bool kVecStore>
+// One block's work on tile `tile`, K-slices [s_begin, s_end).  kACopy, kBCopy:
+// how the A and B slabs are copied (kCopyTransposing for A stored M x K and B
+// stored N x K; kCopyVec / kCopyScalar for A stored K x M and B stored K x N).
+template <class Cf, int kACopy, int kBCopy>
 struct SimtBlock {
   // Accumulators in pairs along N: acc[i][jp] holds columns 2 jp (lo), 2 jp + 1 (hi).
   uint64_t acc[Cf::TM][Cf::TN / 2];
@@ -216,58 +243,118 @@ struct SimtBlock {
 
   __device__ __forceinline__ void mainloop(const SimtParams &p, float *smem, int m0, int n0,
                                            int s_begin, int s_end) {
-    constexpr int BK = Cf::BK, kAsLd = Cf::kAsLd, kBsLd = Cf::kBsLd;
-    constexpr int kStageFloats = Cf::kStageFloats, kStages = Cf::kStages;
+    constexpr int BK = Cf::BK, kAsLd = Cf::kAsLd, kBsLd = Cf::template bs_ld<kBCopy>();
+    constexpr int kStageFloats = Cf::template stage_floats<kBCopy>(), kStages = Cf::kStages;
 
-    // A copies: warp instruction (r, h) copies rows 4 (warp + kWarps r) + lane/8,
-    // k 8 h + lane % 8.
-    const int a_row = (lane >> 3) + 4 * warp;
-    const int a_k = lane & 7;
-    uint32_t a_rows_ok = 0;
+    // Transposing copies (A stored M x K, B stored N x K): warp instruction
+    // (r, h) copies rows 4 (warp + kWarps r) + lane/8 of the tile, k 8 h + lane % 8.
+    const int t_row = (lane >> 3) + 4 * warp;
+    const int t_k = lane & 7;
+    // Direct copies (A stored K x M, B stored K x N): vector v is k row
+    // tid / (E/4) + v (threads / (E/4)) of the slab, columns 4 (tid % (E/4));
+    // scalar it is k row warp + kWarps (it / (E/32)), column lane + 32 (it % (E/32)),
+    // E = BM or BN.
+    const float *a_src;
+    int64_t a_step;            // between copy groups (transposing) or slab rows (direct)
+    uint32_t a_rows_ok = 0;    // transposing: bit r: row t_row + 4 kWarps r inside M
+    int a_k = 0, a_m = 0;      // direct: this thread's k row and column in the slab
+    uint32_t a_dst0;
+    if (kACopy == kCopyTransposing) {
 #pragma unroll
-    for (int r = 0; r < Cf::kARowGroupsPerWarp; ++r)
-      a_rows_ok |= uint32_t(m0 + a_row + 4 * Cf::kWarps * r < p.M) << r;
-    const float *a_src = p.A + int64_t(min(m0 + a_row, p.M - 1)) * p.lda + a_k;
-    const int64_t a_row_step = int64_t(4 * Cf::kWarps) * p.lda;
-    const uint32_t a_dst0 = smem_addr(smem) + 4u * (a_k * kAsLd + a_row);
-
-    // B copies: vector v is k row tid / (BN/4) + v * (threads / (BN/4)), columns 4 (tid % (BN/4));
-    // scalar it is k row warp + kWarps (it / (BN/32)), column lane + 32 (it % (BN/32)).
-    constexpr int kBRowsPerPass = Cf::kThreads / Cf::kBVecPerRow;
-    const int b_k = kVecB ? tid / Cf::kBVecPerRow : warp;
-    const int b_n = kVecB ? (tid % Cf::kBVecPerRow) * 4 : lane;
-    const float *b_src = p.B + int64_t(b_k) * p.ldb + min(n0 + b_n, p.N - 1);
-    const uint32_t b_dst0 = smem_addr(smem) + 4u * (BK * kAsLd + b_k * kBsLd + b_n);
+      for (int r = 0; r < Cf::kARowGroupsPerWarp; ++r)
+        a_rows_ok |= uint32_t(m0 + t_row + 4 * Cf::kWarps * r < p.M) << r;
+      a_src = p.A + int64_t(min(m0 + t_row, p.M - 1)) * p.lda + t_k;
+      a_step = int64_t(4 * Cf::kWarps) * p.lda;
+      a_dst0 = smem_addr(smem) + 4u * (t_k * kAsLd + t_row);
+    } else {
+      a_k = kACopy == kCopyVec ? tid / (Cf::BM / 4) : warp;
+      a_m = kACopy == kCopyVec ? (tid % (Cf::BM / 4)) * 4 : lane;
+      a_src = p.A + int64_t(a_k) * p.lda + min(m0 + a_m, p.M - 1);
+      a_step = p.lda;
+      a_dst0 = smem_addr(smem) + 4u * (a_k * kAsLd + a_m);
+    }
+    const float *b_src;
+    int64_t b_step;
+    uint32_t b_rows_ok = 0;
+    int b_k = 0, b_n = 0;
+    uint32_t b_dst0;
+    if (kBCopy == kCopyTransposing) {
+#pragma unroll
+      for (int r = 0; r < Cf::BN / 4 / Cf::kWarps; ++r)
+        b_rows_ok |= uint32_t(n0 + t_row + 4 * Cf::kWarps * r < p.N) << r;
+      b_src = p.B + int64_t(min(n0 + t_row, p.N - 1)) * p.ldb + t_k;
+      b_step = int64_t(4 * Cf::kWarps) * p.ldb;
+      b_dst0 = smem_addr(smem) + 4u * (BK * kAsLd + t_k * kBsLd + t_row);
+    } else {
+      b_k = kBCopy == kCopyVec ? tid / Cf::kBVecPerRow : warp;
+      b_n = kBCopy == kCopyVec ? (tid % Cf::kBVecPerRow) * 4 : lane;
+      b_src = p.B + int64_t(b_k) * p.ldb + min(n0 + b_n, p.N - 1);
+      b_step = p.ldb;
+      b_dst0 = smem_addr(smem) + 4u * (BK * kAsLd + b_k * kBsLd + b_n);
+    }
 
     auto issue_slice = [&](int s, int stage) {
       const int k0 = s * BK;
       const uint32_t st_off = 4u * stage * kStageFloats;
-      const float *a = a_src + k0;
+      if (kACopy == kCopyTransposing) {
+        const float *a = a_src + k0;
 #pragma unroll
-      for (int it = 0; it < Cf::kACopies; ++it) {
-        const int r = it % Cf::kARowGroupsPerWarp, h = it / Cf::kARowGroupsPerWarp;
-        const bool ok = ((a_rows_ok >> r) & 1u) && (k0 + a_k + 8 * h < p.K);
-        cp_async_4(a_dst0 + st_off + 4u * (8 * h * kAsLd + 4 * Cf::kWarps * r),
-                   a + r * a_row_step + 8 * h, ok, p.A);
+        for (int it = 0; it < Cf::kACopies; ++it) {
+          const int r = it % Cf::kARowGroupsPerWarp, h = it / Cf::kARowGroupsPerWarp;
+          const bool ok = ((a_rows_ok >> r) & 1u) && (k0 + t_k + 8 * h < p.K);
+          cp_async_4(a_dst0 + st_off + 4u * (8 * h * kAsLd + 4 * Cf::kWarps * r),
+                     a + r * a_step + 8 * h, ok, p.A);
+        }
+      } else if (kACopy == kCopyVec) {
+        constexpr int kRowsPerPass = Cf::kThreads / (Cf::BM / 4);
+        const float *a = a_src + int64_t(k0) * a_step;
+        const bool col_ok = m0 + a_m < p.M;
+#pragma unroll
+        for (int v = 0; v < BK * Cf::BM / 4 / Cf::kThreads; ++v) {
+          const int kr = a_k + kRowsPerPass * v;
+          cp_async_16(a_dst0 + st_off + 4u * (kRowsPerPass * v * kAsLd),
+                      a + int64_t(kRowsPerPass * v) * a_step, col_ok && (k0 + kr < p.K), p.A);
+        }
+      } else {
+        constexpr int kColPasses = Cf::BM / 32;
+        const float *a = a_src + int64_t(k0) * a_step;
+#pragma unroll
+        for (int it = 0; it < BK * Cf::BM / Cf::kThreads; ++it) {
+          const int kr = Cf::kWarps * (it / kColPasses), c = it % kColPasses;
+          const bool ok = (m0 + a_m + 32 * c < p.M) && (k0 + a_k + kr < p.K);
+          cp_async_4(a_dst0 + st_off + 4u * (kr * kAsLd + 32 * c),
+                     a + int64_t(kr) * a_step + 32 * c, ok, p.A);
+        }
       }
-      const float *b = b_src + int64_t(k0) * p.ldb;
-      if (kVecB) {
+      if (kBCopy == kCopyTransposing) {
+        const float *b = b_src + k0;
+#pragma unroll
+        for (int it = 0; it < Cf::BN / 4 / Cf::kWarps * (BK / 8); ++it) {
+          const int r = it % (Cf::BN / 4 / Cf::kWarps), h = it / (Cf::BN / 4 / Cf::kWarps);
+          const bool ok = ((b_rows_ok >> r) & 1u) && (k0 + t_k + 8 * h < p.K);
+          cp_async_4(b_dst0 + st_off + 4u * (8 * h * kBsLd + 4 * Cf::kWarps * r),
+                     b + r * b_step + 8 * h, ok, p.B);
+        }
+      } else if (kBCopy == kCopyVec) {
+        constexpr int kBRowsPerPass = Cf::kThreads / Cf::kBVecPerRow;
+        const float *b = b_src + int64_t(k0) * b_step;
         const bool col_ok = n0 + b_n < p.N;
 #pragma unroll
         for (int v = 0; v < Cf::kBVecCopies; ++v) {
           const int kr = b_k + kBRowsPerPass * v;
           const bool ok = col_ok && (k0 + kr < p.K);
           cp_async_16(b_dst0 + st_off + 4u * (kBRowsPerPass * v * kBsLd),
-                      b + int64_t(kBRowsPerPass * v) * p.ldb, ok, p.B);
+                      b + int64_t(kBRowsPerPass * v) * b_step, ok, p.B);
         }
       } else {
         constexpr int kColPasses = Cf::BN / 32;
+        const float *b = b_src + int64_t(k0) * b_step;
 #pragma unroll
         for (int it = 0; it < Cf::kBScalarCopies; ++it) {
           const int kr = Cf::kWarps * (it / kColPasses), c = it % kColPasses;
           const bool ok = (n0 + b_n + 32 * c < p.N) && (k0 + b_k + kr < p.K);
           cp_async_4(b_dst0 + st_off + 4u * (kr * kBsLd + 32 * c),
-                     b + int64_t(kr) * p.ldb + 32 * c, ok, p.B);
+                     b + int64_t(kr) * b_step + 32 * c, ok, p.B);
         }
       }
     };
@@ -356,7 +443,7 @@ struct SimtBlock {
 #pragma unroll
         for (int c = 0; c < Cf::TN / 4; ++c) {
           const int dc = 4 * Cf::LN * c;
-          if (kVecStore) {
+          if (p.vec_store) {
             if (col0 + dc < p.N) {
               float4 v = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
               if (kAdd) {
@@ -380,11 +467,11 @@ struct SimtBlock {
   }
 };
 
-template <class Cf, bool kVecB, bool kVecStore>
+template <class Cf, int kACopy, int kBCopy>
 __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 gemm_simt_kernel(const SimtParams p) {
   extern __shared__ __align__(16) float smem[];
-  SimtBlock<Cf, kVecB, kVecStore> blk;
+  SimtBlock<Cf, kACopy, kBCopy> blk;
   blk.init_lanes();
 
   // Whole tiles.
@@ -451,20 +538,21 @@ std::atomic<unsigned int> g_epoch{0};
 std::atomic<int64_t> g_wait_limit_ns{int64_t(10) * 1000 * 1000 * 1000};
 std::atomic<int> g_drop_signal_block{-1};
 
-template <class Cf, bool kVecB, bool kVecStore>
+template <class Cf, int kACopy, int kBCopy>
 cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
   static LaunchState state;
-  auto kernel = gemm_simt_kernel<Cf, kVecB, kVecStore>;
+  auto kernel = gemm_simt_kernel<Cf, kACopy, kBCopy>;
+  constexpr int kSmemBytes = Cf::template smem_bytes<kBCopy>();
   const uint64_t bit = uint64_t(1) << (dev.id & 63);
   if (!(state.configured.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cf::kSmemBytes);
+                                         kSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int nb = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, Cf::kThreads, Cf::kSmemBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, Cf::kThreads, kSmemBytes);
     if (e != cudaSuccess) return e;
     state.blocks_per_sm[dev.id & 63].store(nb, std::memory_order_relaxed);
     state.configured.fetch_or(bit, std::memory_order_release);
@@ -481,6 +569,8 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStre
   prm.M = int(p.M); prm.N = int(p.N); prm.K = int(p.K);
   prm.A = p.A; prm.lda = p.lda; prm.B = p.B; prm.ldb = p.ldb; prm.C = p.C; prm.ldc = p.ldc;
   prm.tiles_m = int(tiles_m); prm.tiles_n = int(tiles_n);
+  prm.vec_store = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0 &&
+                   p.N % 4 == 0) ? 1 : 0;
   prm.slices = slices;
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   prm.drop_signal_block = g_drop_signal_block.load(std::memory_order_relaxed);
@@ -494,7 +584,7 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStre
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(Cf::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cf::kSmemBytes;
+  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   if (stream_k) {
     const int64_t sk_tiles = rem + slots;
@@ -523,13 +613,23 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
   using Cf = DefaultConfig;
+  // A stored K x M (transa) or B stored K x N (no transb) are copied directly,
+  // in 16-byte vectors when aligned; the other two layouts by transposing copies.
+  const bool vec_a = aligned16(p.A) && p.lda % 4 == 0 && p.M % 4 == 0;
   const bool vec_b = aligned16(p.B) && p.ldb % 4 == 0 && p.N % 4 == 0;
-  const bool vec_store = aligned16(p.C) && p.ldc % 4 == 0 && p.N % 4 == 0;
-  if (vec_b)
-    return vec_store ? launch_variant<Cf, true, true>(p, dev, stream)
-                     : launch_variant<Cf, true, false>(p, dev, stream);
-  return vec_store ? launch_variant<Cf, false, true>(p, dev, stream)
-                   : launch_variant<Cf, false, false>(p, dev, stream);
+  if (!p.transa) {
+    if (p.transb) return launch_variant<Cf, kCopyTransposing, kCopyTransposing>(p, dev, stream);
+    return vec_b ? launch_variant<Cf, kCopyTransposing, kCopyVec>(p, dev, stream)
+                 : launch_variant<Cf, kCopyTransposing, kCopyScalar>(p, dev, stream);
+  }
+  if (p.transb)
+    return vec_a ? launch_variant<Cf, kCopyVec, kCopyTransposing>(p, dev, stream)
+                 : launch_variant<Cf, kCopyScalar, kCopyTransposing>(p, dev, stream);
+  if (vec_a)
+    return vec_b ? launch_variant<Cf, kCopyVec, kCopyVec>(p, dev, stream)
+                 : launch_variant<Cf, kCopyVec, kCopyScalar>(p, dev, stream);
+  return vec_b ? launch_variant<Cf, kCopyScalar, kCopyVec>(p, dev, stream)
+               : launch_variant<Cf, kCopyScalar, kCopyScalar>(p, dev, stream);
 }
 
 cudaError_t simt_device_status(unsigned int *status, bool clear) {

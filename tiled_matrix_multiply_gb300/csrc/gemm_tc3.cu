@@ -186,8 +186,8 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
 
 // ---- split pre-pass -----------------------------------------------------------
 
-// A (M x K, lda) -> hi, lo (M x Kp), zeros for k >= K.  Thread handles 4
-// consecutive k of one row; rows advance with the grid's y extent.
+// Rows of K values (M x K, ld) -> hi, lo (M x Kp), zeros for k >= K.  Thread
+// handles 4 consecutive k of one row; rows advance with the grid's y extent.
 __global__ void tc3_split_a_kernel(int M, int K, int Kp, const float *__restrict__ A, int64_t lda,
                                    int vec_load, float *__restrict__ hi, float *__restrict__ lo) {
   const int k = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
@@ -211,7 +211,8 @@ __global__ void tc3_split_a_kernel(int M, int K, int Kp, const float *__restrict
   }
 }
 
-// B (K x N, ldb) -> hi, lo transposed (N x Kp), zeros for k >= K; 32 x 32 tiles.
+// K rows of N values (K x N, ldb) -> hi, lo transposed (N x Kp), zeros for
+// k >= K; 32 x 32 tiles through shared memory.
 __global__ void tc3_split_bt_kernel(int K, int N, int Kp, const float *__restrict__ B, int64_t ldb,
                                     float *__restrict__ hi, float *__restrict__ lo) {
   __shared__ float tile[32][33];
@@ -583,17 +584,30 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
   float *b_lo = reinterpret_cast<float *>(ws + 2 * round256(size_t(p.M) * Kp * 4) +
                                           round256(size_t(p.N) * Kp * 4));
 
-  // 1. split pre-pass.
+  // 1. split pre-pass: op(A) -> M x Kp and op(B)^T -> N x Kp, K-major.  An
+  // operand stored with K contiguous (A as M x K, B as N x K) is split row by
+  // row; one stored with K as its rows (A as K x M, B as K x N) is transposed.
   {
-    const bool vec_a = (reinterpret_cast<uintptr_t>(p.A) & 15u) == 0 && p.lda % 4 == 0;
-    const dim3 grid_a(unsigned((Kp / 4 + 255) / 256), unsigned(std::min<int64_t>(p.M, 65535)));
-    tc3_split_a_kernel<<<grid_a, 256, 0, stream>>>(int(p.M), int(p.K), int(Kp), p.A, p.lda,
-                                                   vec_a ? 1 : 0, a_hi, a_lo);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const dim3 grid(unsigned((p.N + 31) / 32), unsigned(Kp / 32));
-    tc3_split_bt_kernel<<<grid, dim3(32, 8), 0, stream>>>(int(p.K), int(p.N), int(Kp), p.B, p.ldb,
-                                                          b_hi, b_lo);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto split_rows = [&](const float *src, int64_t ld, int64_t rows, float *hi, float *lo) {
+      const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && ld % 4 == 0;
+      const dim3 grid(unsigned((Kp / 4 + 255) / 256), unsigned(std::min<int64_t>(rows, 65535)));
+      tc3_split_a_kernel<<<grid, 256, 0, stream>>>(int(rows), int(p.K), int(Kp), src, ld,
+                                                   vec ? 1 : 0, hi, lo);
+      return cudaGetLastError();
+    };
+    auto split_transposed = [&](const float *src, int64_t ld, int64_t cols, float *hi,
+                                float *lo) {
+      const dim3 grid(unsigned((cols + 31) / 32), unsigned(Kp / 32));
+      tc3_split_bt_kernel<<<grid, dim3(32, 8), 0, stream>>>(int(p.K), int(cols), int(Kp), src,
+                                                            ld, hi, lo);
+      return cudaGetLastError();
+    };
+    e = p.transa ? split_transposed(p.A, p.lda, p.M, a_hi, a_lo)
+                 : split_rows(p.A, p.lda, p.M, a_hi, a_lo);
+    if (e != cudaSuccess) return e;
+    e = p.transb ? split_rows(p.B, p.ldb, p.N, b_hi, b_lo)
+                 : split_transposed(p.B, p.ldb, p.N, b_hi, b_lo);
+    if (e != cudaSuccess) return e;
   }
 
   // 2. product kernel.

@@ -7,7 +7,9 @@
 
 namespace tmm {
 
-// One validated product C = A x B (row-major, element strides lda/ldb/ldc).
+// One validated product C = op(A) x op(B) (row-major, element strides
+// lda/ldb/ldc).  op(A) is M x K: A itself (stored M x K) or, with transa, the
+// transpose of A stored K x M; op(B) is K x N likewise (B stored N x K with transb).
 struct GemmProblem {
   int64_t M, N, K;
   const float *A;
@@ -16,6 +18,7 @@ struct GemmProblem {
   int64_t ldb;
   float *C;
   int64_t ldc;
+  int transa = 0, transb = 0;
 };
 
 // Properties of the current device the launchers size their grids by.
