@@ -528,6 +528,11 @@ gemm_simt_kernel(const SimtParams p) {
 // ---- host side ------------------------------------------------------------------
 
 using DefaultConfig = SimtConfig<8, 16, 1, 4, 16, 4, 2>;
+// Transposing copies cost one 4-byte copy per element, so a layout that reads
+// B stored N x K keeps the tile narrow in N: 256 x 64 tiles when A is copied
+// directly (A stored K x M), 128 x 128 when both operands are transposed.
+using WideMConfig = SimtConfig<8, 16, 4, 1, 16, 4, 2>;
+using SquareConfig = SimtConfig<8, 16, 2, 2, 16, 4, 2>;
 
 struct LaunchState {
   std::atomic<uint64_t> configured{0};   // bit per device: smem opt-in done
@@ -618,13 +623,14 @@ cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_
   const bool vec_a = aligned16(p.A) && p.lda % 4 == 0 && p.M % 4 == 0;
   const bool vec_b = aligned16(p.B) && p.ldb % 4 == 0 && p.N % 4 == 0;
   if (!p.transa) {
-    if (p.transb) return launch_variant<Cf, kCopyTransposing, kCopyTransposing>(p, dev, stream);
+    if (p.transb)
+      return launch_variant<SquareConfig, kCopyTransposing, kCopyTransposing>(p, dev, stream);
     return vec_b ? launch_variant<Cf, kCopyTransposing, kCopyVec>(p, dev, stream)
                  : launch_variant<Cf, kCopyTransposing, kCopyScalar>(p, dev, stream);
   }
   if (p.transb)
-    return vec_a ? launch_variant<Cf, kCopyVec, kCopyTransposing>(p, dev, stream)
-                 : launch_variant<Cf, kCopyScalar, kCopyTransposing>(p, dev, stream);
+    return vec_a ? launch_variant<WideMConfig, kCopyVec, kCopyTransposing>(p, dev, stream)
+                 : launch_variant<WideMConfig, kCopyScalar, kCopyTransposing>(p, dev, stream);
   if (vec_a)
     return vec_b ? launch_variant<Cf, kCopyVec, kCopyVec>(p, dev, stream)
                  : launch_variant<Cf, kCopyVec, kCopyScalar>(p, dev, stream);
