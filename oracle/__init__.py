@@ -12,7 +12,10 @@ summed in ascending k.  ``gemm`` returns that double matrix; ``gemm_f32``
 rounds it once to float (round to nearest even), the value an exact FP32
 result must equal bit for bit.
 
-Every function here is pinned by ``tests/test_oracle.py`` against closed forms
+``window_sum`` follows "CMU DLSys Lecture 12" section 3 (``window_oracle.c``)
+and is pinned by ``tests/test_window_oracle.py``.
+
+Every gemm function here is pinned by ``tests/test_oracle.py`` against closed forms
 (identity, permutation, all-ones, integer rank-1 products), the worked
 outer-product example of "CMU DLSys Lecture 12: GPU Acceleration" section 4
 (``tests/golden``), exact rational brute force on tiny shapes and an
@@ -29,31 +32,33 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "gemm_oracle.c")
+SOURCES = [SOURCE, os.path.join(_HERE, "window_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
-_LIB_PATH = os.path.join(_BUILD_DIR, "libgemm_oracle.so")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libtmm_oracle.so")
 
 _lock = threading.Lock()
 _default = None
 
 
-def compile_source(src: str, out: str) -> str:
-    """gcc a C source of the oracle's form into a shared library at ``out``."""
+def compile_source(src, out: str) -> str:
+    """gcc C sources of the oracle's form (one path or a list) into a shared library."""
+    srcs = [src] if isinstance(src, str) else list(src)
     tmp = out + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-           "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, src]
+           "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, *srcs]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
 
 
 def build(force: bool = False) -> str:
-    """Compile gemm_oracle.c (gcc, OpenMP) unless an up-to-date build exists."""
+    """Compile the oracle's C sources (gcc, OpenMP) unless an up-to-date build exists."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     fresh = (os.path.exists(_LIB_PATH)
-             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(SOURCE))
+             and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(f) for f in SOURCES))
     if fresh and not force:
         return _LIB_PATH
-    return compile_source(SOURCE, _LIB_PATH)
+    return compile_source(SOURCES, _LIB_PATH)
 
 
 def _row_major_view(x: np.ndarray, name: str):
@@ -88,6 +93,11 @@ class OracleLib:
         lib.oracle_gemm_entries_f64.restype = ctypes.c_int
         lib.oracle_default_threads.argtypes = []
         lib.oracle_default_threads.restype = ctypes.c_int
+        if hasattr(lib, "oracle_window_sum_f64"):
+            lib.oracle_window_sum_f64.argtypes = [i64, ctypes.c_int, ptr, ptr]
+            lib.oracle_window_sum_f64.restype = ctypes.c_int
+            lib.oracle_window_sum_f32_ascending.argtypes = [i64, ctypes.c_int, ptr, ptr]
+            lib.oracle_window_sum_f32_ascending.restype = ctypes.c_int
         self._lib = lib
         self.path = path
 
@@ -128,6 +138,25 @@ class OracleLib:
         return out
 
 
+    def window_sum(self, x: np.ndarray, W: int, fp32_ascending: bool = False) -> np.ndarray:
+        """y_i = sum_{d<W} x_{i+d} for the n = len(x) - W + 1 valid windows."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        if x.ndim != 1:
+            raise ValueError("x must be 1-D")
+        n = x.shape[0] - W + 1
+        if n < 0:
+            raise ValueError("x shorter than one window")
+        if fp32_ascending:
+            y = np.empty(n, dtype=np.float32)
+            rc = self._lib.oracle_window_sum_f32_ascending(n, W, x.ctypes.data, y.ctypes.data)
+        else:
+            y = np.empty(n, dtype=np.float64)
+            rc = self._lib.oracle_window_sum_f64(n, W, x.ctypes.data, y.ctypes.data)
+        if rc != 0:
+            raise ValueError("window sum rejected its arguments")
+        return y
+
+
 def _oracle() -> OracleLib:
     global _default
     with _lock:
@@ -155,3 +184,13 @@ def gemm_entries(A: np.ndarray, B: np.ndarray, ii, jj,
                  threads: int | None = None) -> np.ndarray:
     """C[ii[t], jj[t]] for each t, each a separate FP64 dot product in ascending k."""
     return _oracle().gemm_entries(A, B, ii, jj, threads)
+
+
+def window_sum(x: np.ndarray, W: int = 5) -> np.ndarray:
+    """Sliding-window sums y_i = sum_{d<W} x_{i+d} in FP64 (the definition)."""
+    return _oracle().window_sum(x, W)
+
+
+def window_sum_f32_ascending(x: np.ndarray, W: int = 5) -> np.ndarray:
+    """The same sums accumulated in float from 0 in ascending d, as the page's fragment does."""
+    return _oracle().window_sum(x, W, fp32_ascending=True)
