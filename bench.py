@@ -368,6 +368,8 @@ def run_ours(args, world, rank, local):
         extra["tc3"] = tc3_leg(args, w, A, B, C, flush, stream, peaks)
     if not args.no_layouts and rank == 0:
         extra["layouts"] = layouts_leg(args, w, A, B, C, flush, stream)
+    if not args.no_window and rank == 0:
+        extra["window5"] = window_leg(args, flush, stream, peaks)
     if not args.no_contrast and rank == 0:
         extra["contrast"] = contrast_paths(args, w, A, B, C, flush, stream, props, peaks)
 
@@ -472,6 +474,38 @@ def layouts_leg(args, w, A, B, C, flush, stream) -> dict:
     return {"steps": steps, "transa_transb": {"tn": [1, 0], "nt": [0, 1], "tt": [1, 1]}, **out}
 
 
+WINDOW_N = 1 << 28
+
+
+def window_leg(args, flush, stream, peaks) -> dict:
+    """window_sum_f32 ("CMU DLSys Lecture 12" section 3, W = 5) on 2^28 outputs:
+    HBM-bound, 4 (n + W - 1) bytes read and 4 n written per call."""
+    import torch
+    from tiled_matrix_multiply_gb300 import _abi
+    lib = _abi.load()
+    W = 5
+    n = WINDOW_N
+    g = torch.Generator(device="cuda").manual_seed(5)
+    x = torch.rand(n + W - 1, device="cuda", generator=g)
+    y = torch.empty(n, device="cuda")
+
+    def step():
+        rc = lib.window_sum_f32(n, W, x.data_ptr(), y.data_ptr(), stream.cuda_stream)
+        assert rc == _abi.TMM_OK, _abi.last_error()
+    steps = max(3, min(args.steps, 100))
+    ms = statistics.mean(time_device(step, flush, steps, args.warmup, stream, None))
+    nbytes = 4 * (n + W - 1) + 4 * n
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peak = peaks.get("hbm_gbs") or 6800.0
+    return {"workload": f"window sum W={W}, n=2^28 outputs, uniform[0,1) floats",
+            "ms_per_step": ms, "value": gbs, "unit": "GB/s", "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "traffic": None,
+                         "peak_source": ("MEASURED_PEAKS.json hbm_gbs" if peaks.get("hbm_gbs")
+                                         else "fallback 6.8 TB/s"),
+                         "algorithmic": f"4 (n + W - 1) + 4 n = {nbytes} bytes per call"}}
+
+
 def contrast_paths(args, w, A, B, C, flush, stream, props, peaks) -> dict:
     """The naive kernel on the same workload (a few steps): the untiled contrast."""
     import torch
@@ -499,6 +533,7 @@ def main(argv=None):
     ap.add_argument("--no-contrast", action="store_true", help="skip the naive-kernel contrast")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-tc3", action="store_true", help="skip the tensor-core (3xTF32) leg")
+    ap.add_argument("--no-window", action="store_true", help="skip the window-sum leg")
     ap.add_argument("--no-layouts", action="store_true",
                     help="skip the transposed-layout (gemm_f32_ex, gemm_f32_tc3_ex) leg")
     args = ap.parse_args(argv)

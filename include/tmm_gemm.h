@@ -225,6 +225,20 @@ int tmm_check_device(tmm_stream_t stream);
  */
 int tmm_testing_set_wait_hooks(int drop_signal_block, int64_t wait_limit_ns);
 
+/*
+ * window_sum_f32 -- valid sliding-window sums, "CMU DLSys Lecture 12: GPU
+ * Acceleration" section 3:
+ *     y[i] = sum_{d=0}^{W-1} x[i + d],   0 <= i < n,
+ * the page's window5 for W = 5.  x: DEVICE pointer to n + W - 1 floats; y:
+ * DEVICE pointer to n floats; both caller-owned, 4-byte aligned, and they
+ * must not overlap (TMM_ERR_ALIAS).  1 <= W <= 129, 0 <= n <= 2^40 (n == 0
+ * is a no-op).  Each block stages its tile of inputs plus the W - 1 halo in
+ * shared memory once (the page's cooperative loading); each sum starts from
+ * 0 and adds the window in ascending d in FP32, the page's order.
+ * Asynchronous on `stream`; no allocation.
+ */
+int window_sum_f32(int64_t n, int W, const float *x, float *y, tmm_stream_t stream);
+
 /* One-line description of the calling thread's last failed call ("" if none).
  * The string is owned by the library and valid until the thread's next call. */
 const char *tmm_last_error_string(void);

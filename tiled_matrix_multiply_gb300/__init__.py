@@ -19,7 +19,7 @@ from ._abi import (TMM_ERR_ALIAS, TMM_ERR_CUDA, TMM_ERR_INVALID_ARG,  # noqa: F4
                    TMM_ERR_UNSUPPORTED_DEVICE, TMM_OK, TmmError)
 
 __all__ = ["gemm_f32", "gemm_f32_naive", "gemm_f32_tc3", "tc3_workspace_bytes",
-           "check_device", "raw_call", "TmmError"]
+           "window_sum_f32", "check_device", "raw_call", "TmmError"]
 
 
 def _matrix(x, name, allow_transposed=False):
@@ -131,6 +131,29 @@ def gemm_f32_tc3(A, B, C=None, workspace=None, stream=None):
         if rc != _abi.TMM_OK:
             raise _abi.TmmError("gemm_f32_tc3", rc, _abi.last_error())
     return C
+
+
+def window_sum_f32(x, W=5, y=None, stream=None):
+    """y[i] = sum_{d<W} x[i + d] for the len(x) - W + 1 valid windows (float32 CUDA tensors)."""
+    import torch
+    from . import _abi
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.float32 or not x.is_cuda:
+        raise TypeError("x must be a float32 CUDA tensor")
+    if x.dim() != 1 or (x.numel() > 1 and x.stride(0) != 1):
+        raise ValueError("x must be a contiguous 1-D tensor")
+    n = x.numel() - W + 1
+    if n < 0:
+        raise ValueError("x is shorter than one window")
+    if y is None:
+        y = torch.empty(n, dtype=torch.float32, device=x.device)
+    elif y.shape != (n,) or (n > 1 and y.stride(0) != 1):
+        raise ValueError(f"y must be a contiguous tensor of {n} floats")
+    with torch.cuda.device(x.device):
+        s = stream if stream is not None else torch.cuda.current_stream(x.device)
+        rc = _abi.load().window_sum_f32(n, W, x.data_ptr(), y.data_ptr(), s.cuda_stream)
+        if rc != _abi.TMM_OK:
+            raise _abi.TmmError("window_sum_f32", rc, _abi.last_error())
+    return y
 
 
 def check_device(stream=None) -> None:

@@ -289,6 +289,29 @@ int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_
   return TMM_OK;
 }
 
+int window_sum_f32(int64_t n, int W, const float *x, float *y, tmm_stream_t stream) {
+  const char *who = "window_sum_f32";
+  if (n < 0 || W < 1 || W > tmm::kMaxWindow)
+    return fail(TMM_ERR_INVALID_ARG, "%s: need n >= 0 and 1 <= W <= %d (n=%lld W=%d)", who,
+                tmm::kMaxWindow, (long long)n, W);
+  if (n == 0) return TMM_OK;
+  if (n > (int64_t(1) << 40))
+    return fail(TMM_ERR_INVALID_ARG, "%s: n above 2^40 is not supported", who);
+  if (x == nullptr || y == nullptr) return fail(TMM_ERR_INVALID_ARG, "%s: x or y is NULL", who);
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 3u)
+    return fail(TMM_ERR_INVALID_ARG, "%s: pointers must be 4-byte aligned", who);
+  const uintptr_t x_lo = reinterpret_cast<uintptr_t>(x), x_hi = x_lo + uintptr_t(n + W - 1) * 4;
+  const uintptr_t y_lo = reinterpret_cast<uintptr_t>(y), y_hi = y_lo + uintptr_t(n) * 4;
+  if (overlaps(x_lo, x_hi, y_lo, y_hi))
+    return fail(TMM_ERR_ALIAS, "%s: the output overlaps the input", who);
+  tmm::DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc != TMM_OK) return rc;
+  cudaError_t e = tmm::launch_window_sum(n, W, x, y, dev, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(TMM_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
+  return TMM_OK;
+}
+
 const char *tmm_last_error_string(void) { return g_last_error; }
 
 int tmm_version(void) { return 100; }

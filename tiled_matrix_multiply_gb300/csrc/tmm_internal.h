@@ -2,6 +2,7 @@
 // Not part of the public ABI (that is include/tmm_gemm.h).
 #pragma once
 
+#include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -45,6 +46,11 @@ cudaError_t tc3_device_status(unsigned int *status, bool clear);
 size_t tc3_noalloc_scratch_bytes();
 cudaError_t tc3_noalloc_scratch(int device, void **ptr);
 void tc3_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns);
+
+// Sliding-window sums (y_i = sum_{d<W} x_{i+d}, i < n); 1 <= W <= kMaxWindow.
+constexpr int kMaxWindow = 129;
+cudaError_t launch_window_sum(int64_t n, int W, const float *x, float *y,
+                              const DeviceInfo &dev, cudaStream_t stream);
 
 // Device status word of the tiled kernel (bit 0: a bounded wait ran out of
 // time); read from the current device, optionally cleared.
