@@ -13,7 +13,9 @@ rounds it once to float (round to nearest even), the value an exact FP32
 result must equal bit for bit.
 
 ``window_sum`` follows "CMU DLSys Lecture 12" section 3 (``window_oracle.c``)
-and is pinned by ``tests/test_window_oracle.py``.
+and is pinned by ``tests/test_window_oracle.py``; ``array_sum`` and
+``softmax_rows`` follow "Tiling Strategies" section 5 (``reduce_oracle.c``)
+and are pinned by ``tests/test_reduce_oracle.py``.
 
 Every gemm function here is pinned by ``tests/test_oracle.py`` against closed forms
 (identity, permutation, all-ones, integer rank-1 products), the worked
@@ -32,7 +34,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "gemm_oracle.c")
-SOURCES = [SOURCE, os.path.join(_HERE, "window_oracle.c")]
+SOURCES = [SOURCE, os.path.join(_HERE, "window_oracle.c"),
+           os.path.join(_HERE, "reduce_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libtmm_oracle.so")
 
@@ -45,7 +48,7 @@ def compile_source(src, out: str) -> str:
     srcs = [src] if isinstance(src, str) else list(src)
     tmp = out + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-           "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, *srcs]
+           "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, *srcs, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -98,6 +101,11 @@ class OracleLib:
             lib.oracle_window_sum_f64.restype = ctypes.c_int
             lib.oracle_window_sum_f32_ascending.argtypes = [i64, ctypes.c_int, ptr, ptr]
             lib.oracle_window_sum_f32_ascending.restype = ctypes.c_int
+        if hasattr(lib, "oracle_sum_f64"):
+            lib.oracle_sum_f64.argtypes = [i64, ptr, ptr]
+            lib.oracle_sum_f64.restype = ctypes.c_int
+            lib.oracle_softmax_rows_f64.argtypes = [i64, i64, ptr, i64, ptr, i64]
+            lib.oracle_softmax_rows_f64.restype = ctypes.c_int
         self._lib = lib
         self.path = path
 
@@ -157,6 +165,26 @@ class OracleLib:
         return y
 
 
+    def array_sum(self, x: np.ndarray) -> float:
+        """sum_i x_i of a float32 vector, FP64 in ascending i."""
+        x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+        out = ctypes.c_double(0.0)
+        rc = self._lib.oracle_sum_f64(x.shape[0], x.ctypes.data, ctypes.byref(out))
+        if rc != 0:
+            raise ValueError("oracle_sum_f64 rejected its arguments")
+        return out.value
+
+    def softmax_rows(self, x: np.ndarray) -> np.ndarray:
+        """Row softmax of a float32 (rows, cols) matrix (row stride allowed), as float64."""
+        rows, cols, ldx = _row_major_view(x, "x")
+        y = np.empty((rows, cols), dtype=np.float64)
+        rc = self._lib.oracle_softmax_rows_f64(rows, cols, x.ctypes.data, ldx,
+                                               y.ctypes.data, max(cols, 1))
+        if rc != 0:
+            raise ValueError("oracle_softmax_rows_f64 rejected its arguments")
+        return y
+
+
 def _oracle() -> OracleLib:
     global _default
     with _lock:
@@ -194,3 +222,13 @@ def window_sum(x: np.ndarray, W: int = 5) -> np.ndarray:
 def window_sum_f32_ascending(x: np.ndarray, W: int = 5) -> np.ndarray:
     """The same sums accumulated in float from 0 in ascending d, as the page's fragment does."""
     return _oracle().window_sum(x, W, fp32_ascending=True)
+
+
+def array_sum(x: np.ndarray) -> float:
+    """sum_i x_i over a float32 array, every term in double, ascending i."""
+    return _oracle().array_sum(x)
+
+
+def softmax_rows(x: np.ndarray) -> np.ndarray:
+    """Row-wise softmax of a float32 matrix in FP64: max pass, then normalise pass."""
+    return _oracle().softmax_rows(x)
