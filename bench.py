@@ -370,6 +370,8 @@ def run_ours(args, world, rank, local):
         extra["layouts"] = layouts_leg(args, w, A, B, C, flush, stream)
     if not args.no_window and rank == 0:
         extra["window5"] = window_leg(args, flush, stream, peaks)
+    if not args.no_reduce and rank == 0:
+        extra.update(reduction_legs(args, flush, stream, peaks))
     if not args.no_contrast and rank == 0:
         extra["contrast"] = contrast_paths(args, w, A, B, C, flush, stream, props, peaks)
 
@@ -506,6 +508,64 @@ def window_leg(args, flush, stream, peaks) -> dict:
                          "algorithmic": f"4 (n + W - 1) + 4 n = {nbytes} bytes per call"}}
 
 
+SUM_N = 1 << 28
+SOFTMAX_SHAPE = (65536, 4096)
+
+
+def _hbm_roofline(gbs, peaks, nbytes, what):
+    peak = peaks.get("hbm_gbs") or 6800.0
+    return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+            "traffic": None,
+            "peak_source": ("MEASURED_PEAKS.json hbm_gbs" if peaks.get("hbm_gbs")
+                            else "fallback 6.8 TB/s"),
+            "algorithmic": f"{what} = {nbytes} bytes per call"}
+
+
+def reduction_legs(args, flush, stream, peaks) -> dict:
+    """sum_f32 over 2^28 floats and softmax_rows_f32 over 65536 rows of 4096 logits
+    ("Tiling Strategies" section 5): HBM-bound, each input read once."""
+    import torch
+    from tiled_matrix_multiply_gb300 import _abi
+    lib = _abi.load()
+    steps = max(3, min(args.steps, 100))
+    g = torch.Generator(device="cuda").manual_seed(6)
+    out = {}
+
+    x = torch.randn(SUM_N, device="cuda", generator=g)
+    res = torch.empty(1, device="cuda")
+    need = int(lib.sum_f32_workspace_size(SUM_N))
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+
+    def sum_step():
+        rc = lib.sum_f32(SUM_N, x.data_ptr(), res.data_ptr(), ws.data_ptr(), need,
+                         stream.cuda_stream)
+        assert rc == _abi.TMM_OK, _abi.last_error()
+    ms = statistics.mean(time_device(sum_step, flush, steps, args.warmup, stream, None))
+    nbytes = 4 * SUM_N
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out["sum"] = {"workload": "array sum, n = 2^28 standard-normal floats", "ms_per_step": ms,
+                  "value": gbs, "unit": "GB/s", "steps": steps, "launches_per_step": 2,
+                  "roofline": _hbm_roofline(gbs, peaks, nbytes, "4 n")}
+    del x
+
+    rows, cols = SOFTMAX_SHAPE
+    xs = torch.randn(rows, cols, device="cuda", generator=g) * 4
+    ys = torch.empty_like(xs)
+
+    def softmax_step():
+        rc = lib.softmax_rows_f32(rows, cols, xs.data_ptr(), cols, ys.data_ptr(), cols,
+                                  stream.cuda_stream)
+        assert rc == _abi.TMM_OK, _abi.last_error()
+    ms = statistics.mean(time_device(softmax_step, flush, steps, args.warmup, stream, None))
+    nbytes = 8 * rows * cols
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out["softmax"] = {"workload": f"row softmax, {rows} rows x {cols} cols, N(0, 16) logits",
+                      "ms_per_step": ms, "value": gbs, "unit": "GB/s", "steps": steps,
+                      "rows_per_s": rows / (ms / 1e3),
+                      "roofline": _hbm_roofline(gbs, peaks, nbytes, "4 rows cols read + 4 rows cols written")}
+    return out
+
+
 def contrast_paths(args, w, A, B, C, flush, stream, props, peaks) -> dict:
     """The naive kernel on the same workload (a few steps): the untiled contrast."""
     import torch
@@ -534,6 +594,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-tc3", action="store_true", help="skip the tensor-core (3xTF32) leg")
     ap.add_argument("--no-window", action="store_true", help="skip the window-sum leg")
+    ap.add_argument("--no-reduce", action="store_true", help="skip the sum and softmax legs")
     ap.add_argument("--no-layouts", action="store_true",
                     help="skip the transposed-layout (gemm_f32_ex, gemm_f32_tc3_ex) leg")
     args = ap.parse_args(argv)

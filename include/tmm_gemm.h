@@ -239,6 +239,47 @@ int tmm_testing_set_wait_hooks(int drop_signal_block, int64_t wait_limit_ns);
  */
 int window_sum_f32(int64_t n, int W, const float *x, float *y, tmm_stream_t stream);
 
+/*
+ * sum_f32 -- the tiled reduction of "Tiling Strategies" section 5 ("Tiling
+ * Beyond GEMM": the input cut into chunks whose partial sums are accumulated
+ * in shared memory):
+ *     *out = sum_{i=0}^{n-1} x[i].
+ * x: DEVICE pointer to n floats, 4-byte aligned; out: DEVICE pointer to one
+ * float; workspace: DEVICE buffer of at least sum_f32_workspace_size(n) bytes,
+ * 16-byte aligned, which holds one partial sum per block and must not overlap
+ * x (TMM_ERR_ALIAS).  All caller-owned; n == 0 writes 0.  0 <= n <= 2^40.
+ * Accumulates in FP32 in a fixed order (no atomics), so repeated calls give
+ * the same bits; every term passes through at most ceil(n / 2^20) + 28
+ * additions, so |*out - sum| <= (ceil(n / 2^20) + 28) 2^-24 sum |x[i]| (to
+ * first order).  Two kernel launches on `stream`; no allocation.
+ */
+int sum_f32(int64_t n, const float *x, float *out, void *workspace, size_t workspace_bytes,
+            tmm_stream_t stream);
+
+/* Bytes of workspace sum_f32 needs for n elements (at most 4 KiB). */
+size_t sum_f32_workspace_size(int64_t n);
+
+/*
+ * softmax_rows_f32 -- the two-pass softmax of "Tiling Strategies" section 5
+ * (input chunks for the maximum and the sum, "max, then normalize" on the
+ * same data), row by row:
+ *     y[r*ldy + j] = exp(x[r*ldx + j] - m_r) / sum_k exp(x[r*ldx + k] - m_r),
+ *     m_r = max_k x[r*ldx + k],   0 <= r < rows, 0 <= j, k < cols.
+ * x, y: DEVICE pointers, row-major with row strides ldx, ldy >= max(1, cols)
+ * floats, 4-byte aligned (16-byte alignment and strides that are multiples of
+ * 4 select vector loads).  y may be x with ldy == ldx (in place); any other
+ * overlap is TMM_ERR_ALIAS.  0 <= cols < 2^31; rows == 0 or cols == 0 is a
+ * no-op.  Each row is read from HBM once: rows of up to 1024 columns are held
+ * in a warp's registers, up to 49152 columns staged in shared memory; longer
+ * rows are read three times (max, sum, normalise), the later reads mostly from
+ * L2.  FP32 throughout: exp by CUDA's expf, the sum in a fixed order, the
+ * normalisation as a product with fl(1 / s).  A row whose maximum is +inf, or
+ * all of whose entries are -inf, gives NaN (as the formula does); NaN inputs
+ * are not supported.  Asynchronous on `stream`; no allocation.
+ */
+int softmax_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y,
+                     int64_t ldy, tmm_stream_t stream);
+
 /* One-line description of the calling thread's last failed call ("" if none).
  * The string is owned by the library and valid until the thread's next call. */
 const char *tmm_last_error_string(void);

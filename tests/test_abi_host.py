@@ -106,3 +106,50 @@ def test_ex_entry_points_reject_bad_layouts(lib, entry, trans, args):
     extra = (0, 0) if entry == "gemm_f32_tc3_ex" else ()
     rc = getattr(lib, entry)(*trans, *args, *extra, None)
     assert rc == _abi.TMM_ERR_INVALID_ARG
+
+
+def test_sum_workspace_size(lib):
+    assert lib.sum_f32_workspace_size(0) == lib.sum_f32_workspace_size(1 << 30) == 4096
+
+
+@pytest.mark.parametrize("args,status", [
+    ((-1, FAKE, FAKE + (1 << 30), FAKE + (1 << 31), 4096), _abi.TMM_ERR_INVALID_ARG),  # n < 0
+    (((1 << 40) + 1, FAKE, FAKE + (1 << 30), FAKE + (1 << 31), 4096),
+     _abi.TMM_ERR_INVALID_ARG),                                                    # n > 2^40
+    ((8, FAKE, 0, FAKE + (1 << 31), 4096), _abi.TMM_ERR_INVALID_ARG),              # out NULL
+    ((8, 0, FAKE + (1 << 30), FAKE + (1 << 31), 4096), _abi.TMM_ERR_INVALID_ARG),  # x NULL
+    ((8, FAKE, FAKE + (1 << 30), 0, 4096), _abi.TMM_ERR_INVALID_ARG),              # no workspace
+    ((8, FAKE, FAKE + (1 << 30), FAKE + (1 << 31), 4095), _abi.TMM_ERR_INVALID_ARG),  # too small
+    ((8, FAKE, FAKE + (1 << 30), FAKE + (1 << 31) + 4, 4096),
+     _abi.TMM_ERR_INVALID_ARG),                                                    # ws misaligned
+    ((8, FAKE + 2, FAKE + (1 << 30), FAKE + (1 << 31), 4096),
+     _abi.TMM_ERR_INVALID_ARG),                                                    # x misaligned
+    ((4096, FAKE, FAKE + (1 << 30), FAKE + 64, 4096), _abi.TMM_ERR_ALIAS),         # ws inside x
+])
+def test_sum_rejects_bad_arguments_without_a_launch(lib, args, status):
+    assert lib.sum_f32(*args, None) == status
+    assert lib.tmm_last_error_string().decode()
+
+
+@pytest.mark.parametrize("args,status", [
+    ((-1, 4, FAKE, 4, FAKE + (1 << 30), 4), _abi.TMM_ERR_INVALID_ARG),           # rows < 0
+    ((4, -4, FAKE, 4, FAKE + (1 << 30), 4), _abi.TMM_ERR_INVALID_ARG),           # cols < 0
+    ((1, 1 << 31, FAKE, 1 << 31, FAKE + (1 << 40), 1 << 31),
+     _abi.TMM_ERR_INVALID_ARG),                                                  # cols >= 2^31
+    ((4, 8, FAKE, 7, FAKE + (1 << 30), 8), _abi.TMM_ERR_INVALID_ARG),            # ldx < cols
+    ((4, 8, FAKE, 8, FAKE + (1 << 30), 7), _abi.TMM_ERR_INVALID_ARG),            # ldy < cols
+    ((4, 8, 0, 8, FAKE + (1 << 30), 8), _abi.TMM_ERR_INVALID_ARG),               # x NULL
+    ((4, 8, FAKE, 8, 0, 8), _abi.TMM_ERR_INVALID_ARG),                           # y NULL
+    ((4, 8, FAKE + 1, 8, FAKE + (1 << 30), 8), _abi.TMM_ERR_INVALID_ARG),        # misaligned
+    ((1 << 40, 8, FAKE, 1 << 60, FAKE + (1 << 30), 8), _abi.TMM_ERR_INVALID_ARG),  # overflow
+    ((4, 8, FAKE, 8, FAKE + 4, 8), _abi.TMM_ERR_ALIAS),                          # shifted by one
+    ((4, 8, FAKE, 8, FAKE, 16), _abi.TMM_ERR_ALIAS),                             # same base, ld differs
+])
+def test_softmax_rejects_bad_arguments_without_a_launch(lib, args, status):
+    assert lib.softmax_rows_f32(*args, None) == status
+    assert lib.tmm_last_error_string().decode()
+
+
+def test_softmax_empty_shapes_need_no_device(lib):
+    assert lib.softmax_rows_f32(0, 8, FAKE, 8, FAKE + 64, 8, None) == _abi.TMM_OK
+    assert lib.softmax_rows_f32(8, 0, FAKE, 1, FAKE, 1, None) == _abi.TMM_OK

@@ -10,8 +10,10 @@ memory and streams only.
 ``gemm_f32`` is the tiled FFMA path; ``gemm_f32_naive`` is the
 one-output-per-thread contrast kernel; ``gemm_f32_tc3`` runs the product on the
 tensor cores with split-TF32 operands (it needs a workspace, allocated here
-through torch unless one is passed).  All are asynchronous on the current
-torch stream of the operands' device.
+through torch unless one is passed).  ``window_sum_f32``, ``sum_f32`` and
+``softmax_rows_f32`` are the other tiled workloads of the same pages (sliding
+window sums, the array reduction, the two-pass row softmax).  All are
+asynchronous on the current torch stream of the operands' device.
 """
 from __future__ import annotations
 
@@ -19,7 +21,8 @@ from ._abi import (TMM_ERR_ALIAS, TMM_ERR_CUDA, TMM_ERR_INVALID_ARG,  # noqa: F4
                    TMM_ERR_UNSUPPORTED_DEVICE, TMM_OK, TmmError)
 
 __all__ = ["gemm_f32", "gemm_f32_naive", "gemm_f32_tc3", "tc3_workspace_bytes",
-           "window_sum_f32", "check_device", "raw_call", "TmmError"]
+           "window_sum_f32", "sum_f32", "softmax_rows_f32", "check_device", "raw_call",
+           "TmmError"]
 
 
 def _matrix(x, name, allow_transposed=False):
@@ -153,6 +156,47 @@ def window_sum_f32(x, W=5, y=None, stream=None):
         rc = _abi.load().window_sum_f32(n, W, x.data_ptr(), y.data_ptr(), s.cuda_stream)
         if rc != _abi.TMM_OK:
             raise _abi.TmmError("window_sum_f32", rc, _abi.last_error())
+    return y
+
+
+def sum_f32(x, out=None, stream=None):
+    """sum of every element of a contiguous float32 CUDA tensor, as a 0-d tensor (FP32)."""
+    import torch
+    from . import _abi
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.float32 or not x.is_cuda:
+        raise TypeError("x must be a float32 CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    if out is None:
+        out = torch.empty((), dtype=torch.float32, device=x.device)
+    lib = _abi.load()
+    need = int(lib.sum_f32_workspace_size(x.numel()))
+    ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        s = stream if stream is not None else torch.cuda.current_stream(x.device)
+        rc = lib.sum_f32(x.numel(), x.data_ptr(), out.data_ptr(), ws.data_ptr(), need,
+                         s.cuda_stream)
+        if rc != _abi.TMM_OK:
+            raise _abi.TmmError("sum_f32", rc, _abi.last_error())
+    return out
+
+
+def softmax_rows_f32(x, y=None, stream=None):
+    """Softmax of every row of a float32 CUDA matrix (rows, cols); y may be x (in place)."""
+    import torch
+    from . import _abi
+    rows, cols, ldx, trans = _matrix(x, "x")
+    if y is None:
+        y = torch.empty((rows, cols), dtype=torch.float32, device=x.device)
+    ry, cy, ldy, _ = _matrix(y, "y")
+    if (ry, cy) != (rows, cols):
+        raise ValueError(f"y must be {rows} x {cols}")
+    with torch.cuda.device(x.device):
+        s = stream if stream is not None else torch.cuda.current_stream(x.device)
+        rc = _abi.load().softmax_rows_f32(rows, cols, x.data_ptr(), ldx, y.data_ptr(), ldy,
+                                          s.cuda_stream)
+        if rc != _abi.TMM_OK:
+            raise _abi.TmmError("softmax_rows_f32", rc, _abi.last_error())
     return y
 
 

@@ -34,7 +34,8 @@ GEMM_ENTRY_POINTS = ("gemm_f32", "gemm_f32_naive")
 # Every symbol include/tmm_gemm.h declares.
 EXPORTED = GEMM_ENTRY_POINTS + ("gemm_f32_ex", "gemm_f32_tc3", "gemm_f32_tc3_ex",
                                  "gemm_f32_tc3_workspace_size", "gemm_f32_tc3_noalloc",
-                                 "window_sum_f32",
+                                 "window_sum_f32", "sum_f32", "sum_f32_workspace_size",
+                                 "softmax_rows_f32",
                                  "tmm_check_device", "tmm_testing_set_wait_hooks",
                                  "tmm_last_error_string", "tmm_version")
 
@@ -86,6 +87,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gemm_f32_tc3_workspace_size.restype = ctypes.c_size_t
         lib.window_sum_f32.argtypes = [i64, ctypes.c_int, ptr, ptr, ptr]
         lib.window_sum_f32.restype = ctypes.c_int
+        lib.sum_f32.argtypes = [i64, ptr, ptr, ptr, ctypes.c_size_t, ptr]
+        lib.sum_f32.restype = ctypes.c_int
+        lib.sum_f32_workspace_size.argtypes = [i64]
+        lib.sum_f32_workspace_size.restype = ctypes.c_size_t
+        lib.softmax_rows_f32.argtypes = [i64, i64, ptr, i64, ptr, i64, ptr]
+        lib.softmax_rows_f32.restype = ctypes.c_int
         lib.tmm_check_device.argtypes = [ptr]
         lib.tmm_check_device.restype = ctypes.c_int
         lib.tmm_testing_set_wait_hooks.argtypes = [ctypes.c_int, i64]

@@ -312,6 +312,78 @@ int window_sum_f32(int64_t n, int W, const float *x, float *y, tmm_stream_t stre
   return TMM_OK;
 }
 
+size_t sum_f32_workspace_size(int64_t n) {
+  (void)n;
+  return size_t(tmm::kSumMaxPartials) * sizeof(float);
+}
+
+int sum_f32(int64_t n, const float *x, float *out, void *workspace, size_t workspace_bytes,
+            tmm_stream_t stream) {
+  const char *who = "sum_f32";
+  if (n < 0 || n > (int64_t(1) << 40))
+    return fail(TMM_ERR_INVALID_ARG, "%s: need 0 <= n <= 2^40 (n=%lld)", who, (long long)n);
+  if (out == nullptr) return fail(TMM_ERR_INVALID_ARG, "%s: out is NULL", who);
+  if (reinterpret_cast<uintptr_t>(out) & 3u)
+    return fail(TMM_ERR_INVALID_ARG, "%s: out must be 4-byte aligned", who);
+  const size_t need = sum_f32_workspace_size(n);
+  if (n > 0) {
+    if (x == nullptr) return fail(TMM_ERR_INVALID_ARG, "%s: x is NULL", who);
+    if (reinterpret_cast<uintptr_t>(x) & 3u)
+      return fail(TMM_ERR_INVALID_ARG, "%s: x must be 4-byte aligned", who);
+    if (workspace == nullptr || workspace_bytes < need)
+      return fail(TMM_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", who, need,
+                  workspace == nullptr ? size_t(0) : workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u)
+      return fail(TMM_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", who);
+    const uintptr_t x_lo = reinterpret_cast<uintptr_t>(x), x_hi = x_lo + uintptr_t(n) * 4;
+    const uintptr_t w_lo = reinterpret_cast<uintptr_t>(workspace), w_hi = w_lo + need;
+    if (overlaps(x_lo, x_hi, w_lo, w_hi))
+      return fail(TMM_ERR_ALIAS, "%s: the workspace overlaps x", who);
+  }
+  tmm::DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc != TMM_OK) return rc;
+  cudaError_t e = tmm::launch_sum(n, x, out, static_cast<float *>(workspace), dev,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(TMM_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
+  return TMM_OK;
+}
+
+int softmax_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y,
+                     int64_t ldy, tmm_stream_t stream) {
+  const char *who = "softmax_rows_f32";
+  if (rows < 0 || cols < 0)
+    return fail(TMM_ERR_INVALID_ARG, "%s: negative size (rows=%lld cols=%lld)", who,
+                (long long)rows, (long long)cols);
+  if (cols > INT32_MAX)
+    return fail(TMM_ERR_INVALID_ARG, "%s: cols above 2^31-1 is not supported", who);
+  const int64_t min_ld = cols > 1 ? cols : 1;
+  if (ldx < min_ld || ldy < min_ld)
+    return fail(TMM_ERR_INVALID_ARG, "%s: row stride too small (ldx=%lld ldy=%lld, cols=%lld)",
+                who, (long long)ldx, (long long)ldy, (long long)cols);
+  if (rows == 0 || cols == 0) return TMM_OK;
+  if (x == nullptr || y == nullptr) return fail(TMM_ERR_INVALID_ARG, "%s: x or y is NULL", who);
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 3u)
+    return fail(TMM_ERR_INVALID_ARG, "%s: pointers must be 4-byte aligned", who);
+  if (!span_ok(rows, ldx, cols) || !span_ok(rows, ldy, cols))
+    return fail(TMM_ERR_INVALID_ARG, "%s: matrix extent overflows 64-bit byte offsets", who);
+  const bool in_place = x == y && ldx == ldy;
+  if (!in_place) {
+    uintptr_t x_lo, x_hi, y_lo, y_hi;
+    byte_span(x, rows, ldx, cols, &x_lo, &x_hi);
+    byte_span(y, rows, ldy, cols, &y_lo, &y_hi);
+    if (overlaps(x_lo, x_hi, y_lo, y_hi))
+      return fail(TMM_ERR_ALIAS, "%s: y overlaps x without being x itself", who);
+  }
+  tmm::DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc != TMM_OK) return rc;
+  cudaError_t e = tmm::launch_softmax_rows(rows, int(cols), x, ldx, y, ldy, dev,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(TMM_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
+  return TMM_OK;
+}
+
 const char *tmm_last_error_string(void) { return g_last_error; }
 
 int tmm_version(void) { return 100; }

@@ -58,4 +58,16 @@ cudaError_t simt_device_status(unsigned int *status, bool clear);
 // Testing hooks of the tiled kernel's stream-K waits (see tmm_gemm.h).
 void simt_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns);
 
+// Array sum: a first launch writes one partial per block (at most
+// kSumMaxPartials, in a caller-supplied workspace), a second adds them.
+constexpr int kSumMaxPartials = 1024;
+int64_t sum_grid_blocks(int64_t n, const DeviceInfo &dev);
+cudaError_t launch_sum(int64_t n, const float *x, float *out, float *partials,
+                       const DeviceInfo &dev, cudaStream_t stream);
+
+// Row softmax; rows of up to kMaxStagedRowBytes are staged in shared memory.
+constexpr int kMaxStagedRowBytes = 49152 * 4;
+cudaError_t launch_softmax_rows(int64_t rows, int cols, const float *x, int64_t ldx, float *y,
+                                int64_t ldy, const DeviceInfo &dev, cudaStream_t stream);
+
 }  // namespace tmm
