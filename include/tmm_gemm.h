@@ -269,11 +269,14 @@ size_t sum_f32_workspace_size(int64_t n);
  * floats, 4-byte aligned (16-byte alignment and strides that are multiples of
  * 4 select vector loads).  y may be x with ldy == ldx (in place); any other
  * overlap is TMM_ERR_ALIAS.  0 <= cols < 2^31; rows == 0 or cols == 0 is a
- * no-op.  Each row is read from HBM once: rows of up to 1024 columns are held
- * in a warp's registers, up to 49152 columns staged in shared memory; longer
- * rows are read three times (max, sum, normalise), the later reads mostly from
- * L2.  FP32 throughout: exp by CUDA's expf, the sum in a fixed order, the
- * normalisation as a product with fl(1 / s).  A row whose maximum is +inf, or
+ * no-op.  Each row is read from HBM once: rows of up to 2048 columns are held
+ * in registers, up to 16384 columns staged in one block's shared memory, up to
+ * 393216 columns split over a thread-block cluster whose blocks combine their
+ * partial maxima and sums through distributed shared memory; longer rows are
+ * read three times (max, sum, normalise), the later reads mostly from L2.
+ * FP32 throughout: exp by CUDA's expf, the sum in a fixed order, the
+ * normalisation as a product with fl(1 / s) (in a cluster, with
+ * fl(e^{m_c - m} / s) for the chunk maximum m_c).  A row whose maximum is +inf, or
  * all of whose entries are -inf, gives NaN (as the formula does); NaN inputs
  * are not supported.  Asynchronous on `stream`; no allocation.
  */

@@ -158,7 +158,8 @@ def logits(rows, cols, seed, scale=4.0):
 
 
 COLS = [1, 2, 31, 32, 33, 64, 100, 128, 255, 256, 511, 512, 1000, 1024, 1025, 2047, 2048, 2049,
-        4096, 8191, 8192, 8193, 16384, 16385, 32768, 49152, 49153, 65536, 100003]
+        4096, 8191, 8192, 8193, 16384, 16385, 24577, 32768, 49152, 49153, 65536, 100003,
+        131072, 131073, 262144, 786432, 800000]
 
 
 def rows_for(cols):
@@ -170,7 +171,7 @@ def test_softmax_contiguous(cols):
     check_softmax(logits(rows_for(cols), cols, 120 + cols % 1000))
 
 
-@pytest.mark.parametrize("cols", [33, 1000, 1025, 4096, 8193, 49152, 65536])
+@pytest.mark.parametrize("cols", [3, 17, 33, 1000, 1025, 4096, 8193, 49152, 65536, 262147])
 def test_softmax_strided_and_unaligned(cols):
     x = logits(min(37, rows_for(cols)), cols, 121)
     check_softmax(x, ldx=cols + 3, ldy=cols + 5)      # row starts off 16-byte boundaries

@@ -22,27 +22,38 @@
 //   to the result (P >= 2^18 whenever the grid is capped).
 //
 // Row softmax (softmax_rows_f32): y_{r,j} = e^{x_{r,j} - m_r} / sum_k e^{x_{r,k} - m_r}
-// with m_r the row maximum.  Which unit owns a row depends on its length:
-//   * cols <= 1024: one warp per row, the row in the warp's registers
-//     (lane l holds columns l, l + 32, ...); shuffles reduce max and sum.
-//   * cols <= 49152: one block per row (128-1024 threads by length).  Pass 1
-//     copies the row into shared memory (16-byte streaming loads when the rows
-//     are 16-byte aligned) while taking the maximum; pass 2 replaces each
-//     staged value by e^{x - m} and sums them; the stores scale by 1 / s.
-//     Each thread touches only its own staged columns, so consecutive rows
-//     need no barrier on the staging buffer, only on the reduction scratch.
+// with m_r the row maximum.  Each row is read from HBM once and written once;
+// what holds it on chip between the two passes depends on its length:
+//   * up to 2048 columns (rows on 16-byte boundaries, cols % 4 == 0; 1024
+//     otherwise): a group of 1-32 lanes per row, the row in registers (lane s
+//     holds columns or 16-byte vectors s, s + group, ...); group shuffles
+//     reduce max and sum.  Short rows share a warp (32 / group rows at once).
+//   * up to 16384 columns: one block per row.  The row is copied into shared
+//     memory with cp.async, two buffers deep, so the next row's copies are in
+//     flight while this one is reduced; pass 1 takes the maximum, pass 2
+//     replaces each staged value by e^{x - m} and sums them, and the stores
+//     scale by 1 / s.
+//   * up to 8 x 49152 columns: a cluster of 2-8 blocks per row, each staging
+//     one chunk, the partial maxima and sums combined through distributed
+//     shared memory (softmax_staged_kernel describes the exchange).
 //   * longer rows: one block of 1024 threads per row, three passes over
 //     global memory (max, sum, normalise); the second and third reads of a row
 //     come from L2 when the rows in flight fit there.
 // Arithmetic: t = fl(x - m), e = expf(t) (CUDA's, within 2 ulp), s summed in
-// FP32 (each thread in ascending column order, then a shuffle tree), y = e * fl(1/s).
-// y may be x itself (in place): every row is read completely before any of its
-// outputs is written, and only coherent loads are used.
+// FP32 in a fixed order (each thread in ascending column order, then a shuffle
+// tree, then the cluster's chunks in rank order), y = e * fl(1 / s) (in a
+// cluster, e^{x - m_c} * fl(e^{m_c - m} / s)).
+// y may be x itself (in place): every row (chunk) is read completely before
+// any of its outputs is written, and only coherent loads are used.
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 
+#include <cooperative_groups.h>
+
 #include "tmm_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace tmm {
 namespace {
@@ -119,93 +130,252 @@ sum_final_kernel(int G, const float *__restrict__ partials, float *__restrict__ 
 
 // ------------------------------------------------------------------ softmax
 
-constexpr int kWarpRowThreads = 256;      // 8 rows at a time per block
+__device__ __forceinline__ void cp_async_16(float *dst, const float *src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
 
-template <int kPer>   // columns per lane: cols <= 32 kPer
+__device__ __forceinline__ void cp_async_4(float *dst, const float *src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+constexpr int kWarpRowThreads = 256;      // 8 warps per block
+constexpr int kMaxCluster = 16;           // blocks sharing one row, at most
+
+template <int kW>   // max over each aligned group of kW lanes (a power of 2)
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+  for (int o = kW / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+template <int kW>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = kW / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Rows owned by groups of kW lanes (32 / kW rows per warp at a time), any
+// alignment: lane s of a group holds columns s, s + kW, ... (cols <= kW kPer).
+// The whole row stays in registers; group shuffles reduce max and sum.
+template <int kW, int kPer>
 __global__ void __launch_bounds__(kWarpRowThreads)
 softmax_warp_kernel(int64_t rows, int cols, const float *x, int64_t ldx, float *y, int64_t ldy) {
-  const int lane = threadIdx.x & 31;
+  constexpr int kRowsPerWarp = 32 / kW;
+  const int lane = threadIdx.x & 31, sub = lane % kW;
+  const int64_t groups = (rows + kRowsPerWarp - 1) / kRowsPerWarp;
   const int64_t warps = int64_t(gridDim.x) * (kWarpRowThreads / 32);
-  for (int64_t r = int64_t(blockIdx.x) * (kWarpRowThreads / 32) + (threadIdx.x >> 5); r < rows;
-       r += warps) {
-    const float *xr = x + r * ldx;
-    float *yr = y + r * ldy;
+  for (int64_t gi = int64_t(blockIdx.x) * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
+       gi < groups; gi += warps) {
+    const int64_t r = gi * kRowsPerWarp + lane / kW;
+    const bool live = r < rows;
+    const float *xr = x + (live ? r : 0) * ldx;
     float v[kPer];
     float m = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-      const int j = lane + 32 * i;
-      v[i] = j < cols ? __ldcs(xr + j) : -INFINITY;
+      const int j = sub + kW * i;
+      v[i] = (live && j < cols) ? __ldcs(xr + j) : -INFINITY;
       m = fmaxf(m, v[i]);
     }
-    m = warp_max(m);
+    m = group_max<kW>(m);
     float s = 0.0f;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-      const int j = lane + 32 * i;
-      v[i] = j < cols ? expf(v[i] - m) : 0.0f;
+      const int j = sub + kW * i;
+      v[i] = (live && j < cols) ? expf(v[i] - m) : 0.0f;
       s += v[i];
     }
-    s = warp_sum(s);
+    s = group_sum<kW>(s);
     const float inv = 1.0f / s;
+    if (live) {
+      float *yr = y + r * ldy;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int j = lane + 32 * i;
-      if (j < cols) __stcs(yr + j, v[i] * inv);
+      for (int i = 0; i < kPer; ++i) {
+        const int j = sub + kW * i;
+        if (j < cols) __stcs(yr + j, v[i] * inv);
+      }
     }
   }
 }
 
-// One block per row, the row staged in shared memory.  kVec: rows start on
-// 16-byte boundaries (x, y 16-byte aligned, ldx and ldy multiples of 4).
-template <int kThreads, bool kVec>
+// The same with 16-byte accesses: rows start on 16-byte boundaries and
+// cols % 4 == 0; lane s of a group holds vectors s, s + kW, ... (cols <= 4 kW kVec).
+template <int kW, int kVec>
+__global__ void __launch_bounds__(kWarpRowThreads)
+softmax_warp_vec_kernel(int64_t rows, int cols, const float *x, int64_t ldx, float *y,
+                        int64_t ldy) {
+  constexpr int kRowsPerWarp = 32 / kW;
+  const int lane = threadIdx.x & 31, sub = lane % kW;
+  const int nv = cols >> 2;
+  const int64_t groups = (rows + kRowsPerWarp - 1) / kRowsPerWarp;
+  const int64_t warps = int64_t(gridDim.x) * (kWarpRowThreads / 32);
+  for (int64_t gi = int64_t(blockIdx.x) * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
+       gi < groups; gi += warps) {
+    const int64_t r = gi * kRowsPerWarp + lane / kW;
+    const bool live = r < rows;
+    const float4 *xr = reinterpret_cast<const float4 *>(x + (live ? r : 0) * ldx);
+    const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float4 v[kVec];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      const int q = sub + kW * i;
+      v[i] = (live && q < nv) ? __ldcs(xr + q) : none;
+      m = fmaxf(fmaxf(m, fmaxf(v[i].x, v[i].y)), fmaxf(v[i].z, v[i].w));
+    }
+    m = group_max<kW>(m);
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      const bool ok = live && sub + kW * i < nv;
+      v[i].x = ok ? expf(v[i].x - m) : 0.0f; s += v[i].x;
+      v[i].y = ok ? expf(v[i].y - m) : 0.0f; s += v[i].y;
+      v[i].z = ok ? expf(v[i].z - m) : 0.0f; s += v[i].z;
+      v[i].w = ok ? expf(v[i].w - m) : 0.0f; s += v[i].w;
+    }
+    s = group_sum<kW>(s);
+    const float inv = 1.0f / s;
+    if (live) {
+      float4 *yr = reinterpret_cast<float4 *>(y + r * ldy);
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) {
+        const int q = sub + kW * i;
+        if (q < nv)
+          __stcs(yr + q, make_float4(v[i].x * inv, v[i].y * inv, v[i].z * inv, v[i].w * inv));
+      }
+    }
+  }
+}
+
+// Rows staged in shared memory, one row per block, or per cluster of C blocks
+// (kCluster) for rows longer than one block should hold.
+//
+// kVec: rows start on 16-byte boundaries (x, y 16-byte aligned, ldx and ldy
+// multiples of 4; chunk is a multiple of 4).  kDouble: two staging buffers;
+// the next row's asynchronous copies are in flight while the current row is
+// reduced and stored (the page's double buffering, across rows).  Thread t
+// copies, reads and writes only the columns it owns (vectors t, t + T, ...,
+// then the scalars 4 nv + t, ...), so a buffer needs no barrier between its
+// uses; only the reduction scratch does.
+//
+// A cluster splits each row into C chunks: block c stages columns
+// [c chunk, (c + 1) chunk), takes its maximum m_c and s_c = sum e^{x - m_c}
+// over them, and thread k pushes (m_c, s_c) into slot c of block k's shared
+// memory (distributed shared memory).  After one cluster barrier every block
+// reads the C slots in rank order, so all of them form the same
+//     m = max_c m_c,   s = sum_c s_c e^{m_c - m},
+// which equals sum_j e^{x_j - m} (e^{x - m} = e^{x - m_c} e^{m_c - m}), and
+// scales its staged e^{x - m_c} by e^{m_c - m} / s.  A chunk that is all
+// -inf has s_c = 0 and adds nothing.  The slots alternate between two sets
+// by row parity: a block writes a set again only after passing the barrier of
+// the following row, which every block reaches after reading that set.
+template <int kThreads, bool kVec, bool kDouble, bool kCluster>
 __global__ void __launch_bounds__(kThreads)
-softmax_staged_kernel(int64_t rows, int cols, const float *x, int64_t ldx, float *y,
+softmax_staged_kernel(int64_t rows, int cols, int chunk, const float *x, int64_t ldx, float *y,
                       int64_t ldy) {
-  extern __shared__ __align__(16) float row[];
+  extern __shared__ __align__(16) float stage[];
   __shared__ float scratch[32];
+  __shared__ float2 slots[2][kMaxCluster];
   const int t = threadIdx.x;
-  const int nv = kVec ? cols >> 2 : 0;     // 16-byte vectors of the row
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const float *xr = x + r * ldx;
-    float *yr = y + r * ldy;
-    // Pass 1: stage the row, taking the maximum on the way.
+  int C = 1, c = 0;
+  int64_t unit = blockIdx.x, units = gridDim.x;
+  if (kCluster) {
+    cg::cluster_group cl = cg::this_cluster();
+    C = int(cl.num_blocks());
+    c = int(cl.block_rank());
+    unit = blockIdx.x / C;
+    units = gridDim.x / C;
+  }
+  const int c0 = c * chunk;
+  const int len = max(0, min(cols - c0, chunk));   // columns of this block
+  const int nv = kVec ? len >> 2 : 0;               // 16-byte vectors of them
+  const int chunk_pad = (chunk + 3) & ~3;
+  auto copy_row = [&](float *buf, int64_t r) {
+    const float *xr = x + r * ldx + c0;
+    for (int q = t; q < nv; q += kThreads) cp_async_16(buf + 4 * q, xr + 4 * q);
+    for (int j = 4 * nv + t; j < len; j += kThreads) cp_async_4(buf + j, xr + j);
+  };
+  int64_t r = unit;
+  if (kDouble) {
+    if (r < rows) copy_row(stage, r);
+    cp_async_commit();
+  }
+  for (int it = 0; r < rows; r += units, ++it) {
+    float *row = stage + (kDouble ? (it & 1) * chunk_pad : 0);
+    if (kDouble) {
+      const int64_t rn = r + units;
+      if (rn < rows) copy_row(stage + ((it + 1) & 1) * chunk_pad, rn);
+      cp_async_commit();
+      cp_async_wait<1>();        // this thread's copies of row r have landed
+    } else {
+      copy_row(row, r);
+      cp_async_commit();
+      cp_async_wait<0>();
+    }
+    // Pass 1: the maximum (of this block's columns).
     float m = -INFINITY;
     for (int q = t; q < nv; q += kThreads) {
-      const float4 a = __ldcs(reinterpret_cast<const float4 *>(xr) + q);
-      reinterpret_cast<float4 *>(row)[q] = a;
+      const float4 a = reinterpret_cast<const float4 *>(row)[q];
       m = fmaxf(fmaxf(m, fmaxf(a.x, a.y)), fmaxf(a.z, a.w));
     }
-    for (int j = 4 * nv + t; j < cols; j += kThreads) {
-      const float a = __ldcs(xr + j);
-      row[j] = a;
-      m = fmaxf(m, a);
-    }
+    for (int j = 4 * nv + t; j < len; j += kThreads) m = fmaxf(m, row[j]);
     m = block_reduce<true>(m, scratch);
+    // In a cluster, an all -inf chunk takes 0 as its reference: its terms are 0 either way.
+    const float ref = (kCluster && m == -INFINITY) ? 0.0f : m;
     // Pass 2: exponentials in place, and their sum.
     float s = 0.0f;
     for (int q = t; q < nv; q += kThreads) {
       float4 a = reinterpret_cast<float4 *>(row)[q];
-      a.x = expf(a.x - m); s += a.x;
-      a.y = expf(a.y - m); s += a.y;
-      a.z = expf(a.z - m); s += a.z;
-      a.w = expf(a.w - m); s += a.w;
+      a.x = expf(a.x - ref); s += a.x;
+      a.y = expf(a.y - ref); s += a.y;
+      a.z = expf(a.z - ref); s += a.z;
+      a.w = expf(a.w - ref); s += a.w;
       reinterpret_cast<float4 *>(row)[q] = a;
     }
-    for (int j = 4 * nv + t; j < cols; j += kThreads) {
-      const float e = expf(row[j] - m);
+    for (int j = 4 * nv + t; j < len; j += kThreads) {
+      const float e = expf(row[j] - ref);
       row[j] = e;
       s += e;
     }
     s = block_reduce<false>(s, scratch);
-    const float inv = 1.0f / s;
+    float scale;
+    if (kCluster) {
+      cg::cluster_group cl = cg::this_cluster();
+      float2 *set = slots[it & 1];
+      if (t < C) *cl.map_shared_rank(&set[c], t) = make_float2(m, s);
+      cl.sync();
+      float mm = -INFINITY;
+      for (int k = 0; k < C; ++k) mm = fmaxf(mm, set[k].x);
+      float ss = 0.0f;
+      for (int k = 0; k < C; ++k)
+        if (set[k].y != 0.0f) ss += set[k].y * expf(set[k].x - mm);
+      if (mm == -INFINITY) scale = __int_as_float(0x7fc00000);   // all -inf: NaN, as the formula
+      else scale = s != 0.0f ? expf(m - mm) / ss : 0.0f;
+    } else {
+      scale = 1.0f / s;
+    }
+    float *yr = y + r * ldy + c0;
     for (int q = t; q < nv; q += kThreads) {
       float4 a = reinterpret_cast<const float4 *>(row)[q];
-      a.x *= inv; a.y *= inv; a.z *= inv; a.w *= inv;
+      a.x *= scale; a.y *= scale; a.z *= scale; a.w *= scale;
       __stcs(reinterpret_cast<float4 *>(yr) + q, a);
     }
-    for (int j = 4 * nv + t; j < cols; j += kThreads) __stcs(yr + j, row[j] * inv);
+    for (int j = 4 * nv + t; j < len; j += kThreads) __stcs(yr + j, row[j] * scale);
   }
+  cp_async_wait<0>();
+  if (kCluster) cg::this_cluster().sync();
 }
 
 constexpr int kLongRowThreads = 1024;
@@ -235,12 +405,55 @@ softmax_long_kernel(int64_t rows, int cols, const float *x, int64_t ldx, float *
 // Per-device launch facts for one kernel instantiation, set up on first use.
 struct KernelSetup {
   std::atomic<uint64_t> configured{0};
-  std::atomic<int> blocks_per_sm[64];
 };
 
-template <class Kernel>
-cudaError_t blocks_per_sm(KernelSetup &st, Kernel kernel, int threads, int smem,
-                          const DeviceInfo &dev, int *out) {
+// Stage plan for rows too long for a warp: how many blocks share a row, how
+// many columns each stages, and whether two buffers fit.
+struct StagePlan {
+  int cluster;   // blocks per row (1, 2, 4, 8 or 16)
+  int chunk;     // columns per block, a multiple of 4 when cluster > 1
+  bool dbl;      // double-buffered
+};
+
+constexpr int kSingleBlockCols = 16384;   // rows up to this length: one block per row
+constexpr int kChunkTarget = 8192;        // longer rows: chunks of at most this many columns ...
+constexpr int kClusterLimit = 8;          // ... over at most this many blocks
+constexpr int kMaxChunk = kMaxStagedRowBytes / int(sizeof(float));
+static_assert(kClusterLimit <= kMaxCluster, "exchange slots are sized for kMaxCluster blocks");
+
+bool plan_stage(int cols, StagePlan *p) {
+  int C = 1, chunk = cols;
+  if (cols > kSingleBlockCols) {
+    while (chunk > kChunkTarget && C < kClusterLimit) {
+      C *= 2;
+      chunk = (((cols + C - 1) / C) + 3) & ~3;
+    }
+  }
+  if (chunk > kMaxChunk) return false;
+  p->cluster = C;
+  p->chunk = chunk;
+  p->dbl = 2 * ((chunk + 3) & ~3) * int(sizeof(float)) <= kMaxStagedRowBytes;
+  return true;
+}
+
+// Threads per block for a chunk of the given length (measured on GB300 over
+// rows of 2048 to 393216 columns: a lone block wants 8-16 columns per thread,
+// a block in a cluster about 32, since it also waits at the cluster barrier).
+int staged_threads(int chunk, int cluster) {
+  if (cluster > 1) return chunk <= 8192 ? 256 : (chunk <= 16384 ? 512 : 1024);
+  if (chunk <= 4096) return 128;
+  if (chunk <= 16384) return 512;
+  return 1024;
+}
+
+template <int kThreads, bool kVec, bool kDouble, bool kCluster>
+cudaError_t launch_staged(int64_t rows, int cols, const StagePlan &plan, const float *x,
+                          int64_t ldx, float *y, int64_t ldy, const DeviceInfo &dev,
+                          cudaStream_t stream) {
+  static KernelSetup st;
+  auto kernel = softmax_staged_kernel<kThreads, kVec, kDouble, kCluster>;
+  const int chunk_pad = (plan.chunk + 3) & ~3;
+  const int smem = (kDouble ? 2 : 1) * chunk_pad * int(sizeof(float));
   const uint64_t bit = uint64_t(1) << (dev.id & 63);
   if (!(st.configured.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -249,45 +462,78 @@ cudaError_t blocks_per_sm(KernelSetup &st, Kernel kernel, int threads, int smem,
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
+    if (kCluster) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     st.configured.fetch_or(bit, std::memory_order_release);
   }
-  int nb = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem);
-  if (e != cudaSuccess) return e;
-  *out = nb > 0 ? nb : 1;
-  return cudaSuccess;
-}
-
-template <int kThreads, bool kVec>
-cudaError_t launch_staged(int64_t rows, int cols, const float *x, int64_t ldx, float *y,
-                          int64_t ldy, const DeviceInfo &dev, cudaStream_t stream) {
-  static KernelSetup st;
-  auto kernel = softmax_staged_kernel<kThreads, kVec>;
-  const int smem = ((cols + 3) & ~3) * int(sizeof(float));
-  int nb = 1;
-  cudaError_t e = blocks_per_sm(st, kernel, kThreads, smem, dev, &nb);
-  if (e != cudaSuccess) return e;
-  const int64_t grid = std::min<int64_t>(rows, int64_t(dev.sm_count) * nb);
-  kernel<<<unsigned(grid), kThreads, smem, stream>>>(rows, cols, x, ldx, y, ldy);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = size_t(smem);
+  cfg.stream = stream;
+  int64_t units = 0;
+  if (kCluster) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(plan.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(unsigned(plan.cluster) * 64, 1, 1);   // shape only, for the query
+    int clusters = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters <= 0) return cudaErrorInvalidConfiguration;
+    units = std::min<int64_t>(rows, clusters);
+    cfg.gridDim = dim3(unsigned(units * plan.cluster), 1, 1);
+  } else {
+    int nb = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    units = std::min<int64_t>(rows, int64_t(dev.sm_count) * (nb > 0 ? nb : 1));
+    cfg.gridDim = dim3(unsigned(units), 1, 1);
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, rows, cols, plan.chunk, x, ldx, y, ldy);
 }
 
 template <int kThreads>
-cudaError_t launch_staged_any(int64_t rows, int cols, const float *x, int64_t ldx, float *y,
-                              int64_t ldy, bool vec, const DeviceInfo &dev,
+cudaError_t launch_staged_any(int64_t rows, int cols, const StagePlan &plan, const float *x,
+                              int64_t ldx, float *y, int64_t ldy, bool vec, const DeviceInfo &dev,
                               cudaStream_t stream) {
-  return vec ? launch_staged<kThreads, true>(rows, cols, x, ldx, y, ldy, dev, stream)
-             : launch_staged<kThreads, false>(rows, cols, x, ldx, y, ldy, dev, stream);
+#define TMM_STAGED(V, D, K) \
+  launch_staged<kThreads, V, D, K>(rows, cols, plan, x, ldx, y, ldy, dev, stream)
+  if (plan.cluster > 1) {
+    if (vec) return plan.dbl ? TMM_STAGED(true, true, true) : TMM_STAGED(true, false, true);
+    return plan.dbl ? TMM_STAGED(false, true, true) : TMM_STAGED(false, false, true);
+  }
+  if (vec) return plan.dbl ? TMM_STAGED(true, true, false) : TMM_STAGED(true, false, false);
+  return plan.dbl ? TMM_STAGED(false, true, false) : TMM_STAGED(false, false, false);
+#undef TMM_STAGED
 }
 
-template <int kPer>
+int64_t warp_grid(int64_t units, const DeviceInfo &dev) {
+  constexpr int kWarps = kWarpRowThreads / 32;
+  return std::max<int64_t>(1, std::min<int64_t>((units + kWarps - 1) / kWarps,
+                                                int64_t(dev.sm_count) * 8));
+}
+
+template <int kW, int kPer>
 cudaError_t launch_warp_rows(int64_t rows, int cols, const float *x, int64_t ldx, float *y,
                              int64_t ldy, const DeviceInfo &dev, cudaStream_t stream) {
-  constexpr int kRowsPerBlock = kWarpRowThreads / 32;
-  const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-  const int64_t grid = std::min<int64_t>(blocks, int64_t(dev.sm_count) * 8);
-  softmax_warp_kernel<kPer><<<unsigned(grid), kWarpRowThreads, 0, stream>>>(rows, cols, x, ldx,
-                                                                           y, ldy);
+  const int64_t grid = warp_grid((rows + 32 / kW - 1) / (32 / kW), dev);
+  softmax_warp_kernel<kW, kPer><<<unsigned(grid), kWarpRowThreads, 0, stream>>>(
+      rows, cols, x, ldx, y, ldy);
+  return cudaGetLastError();
+}
+
+template <int kW, int kVec>
+cudaError_t launch_warp_vec(int64_t rows, int cols, const float *x, int64_t ldx, float *y,
+                            int64_t ldy, const DeviceInfo &dev, cudaStream_t stream) {
+  const int64_t grid = warp_grid((rows + 32 / kW - 1) / (32 / kW), dev);
+  softmax_warp_vec_kernel<kW, kVec><<<unsigned(grid), kWarpRowThreads, 0, stream>>>(
+      rows, cols, x, ldx, y, ldy);
   return cudaGetLastError();
 }
 
@@ -319,21 +565,43 @@ cudaError_t launch_sum(int64_t n, const float *x, float *out, float *partials,
 
 cudaError_t launch_softmax_rows(int64_t rows, int cols, const float *x, int64_t ldx, float *y,
                                 int64_t ldy, const DeviceInfo &dev, cudaStream_t stream) {
-  if (cols <= 32) return launch_warp_rows<1>(rows, cols, x, ldx, y, ldy, dev, stream);
-  if (cols <= 64) return launch_warp_rows<2>(rows, cols, x, ldx, y, ldy, dev, stream);
-  if (cols <= 128) return launch_warp_rows<4>(rows, cols, x, ldx, y, ldy, dev, stream);
-  if (cols <= 256) return launch_warp_rows<8>(rows, cols, x, ldx, y, ldy, dev, stream);
-  if (cols <= 512) return launch_warp_rows<16>(rows, cols, x, ldx, y, ldy, dev, stream);
-  if (cols <= 1024) return launch_warp_rows<32>(rows, cols, x, ldx, y, ldy, dev, stream);
-  if (cols <= kMaxStagedRowBytes / int(sizeof(float))) {
-    const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) ==
-                         0 &&
-                     (ldx & 3) == 0 && (ldy & 3) == 0;
-    if (cols <= 2048) return launch_staged_any<128>(rows, cols, x, ldx, y, ldy, vec, dev, stream);
-    if (cols <= 8192) return launch_staged_any<256>(rows, cols, x, ldx, y, ldy, vec, dev, stream);
-    if (cols <= 16384)
-      return launch_staged_any<512>(rows, cols, x, ldx, y, ldy, vec, dev, stream);
-    return launch_staged_any<1024>(rows, cols, x, ldx, y, ldy, vec, dev, stream);
+  // Rows that start on 16-byte boundaries and hold whole vectors.
+  const bool aligned =
+      ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
+      (ldx & 3) == 0 && (ldy & 3) == 0;
+#define TMM_WARP(W, P) launch_warp_rows<W, P>(rows, cols, x, ldx, y, ldy, dev, stream)
+#define TMM_WVEC(W, V) launch_warp_vec<W, V>(rows, cols, x, ldx, y, ldy, dev, stream)
+  if (aligned && (cols & 3) == 0 && cols <= 2048) {
+    if (cols <= 4) return TMM_WVEC(1, 1);
+    if (cols <= 8) return TMM_WVEC(2, 1);
+    if (cols <= 16) return TMM_WVEC(4, 1);
+    if (cols <= 32) return TMM_WVEC(8, 1);
+    if (cols <= 64) return TMM_WVEC(16, 1);
+    if (cols <= 128) return TMM_WVEC(32, 1);
+    if (cols <= 256) return TMM_WVEC(32, 2);
+    if (cols <= 512) return TMM_WVEC(32, 4);
+    if (cols <= 1024) return TMM_WVEC(32, 8);
+    return TMM_WVEC(32, 16);
+  }
+  if (cols <= 4) return TMM_WARP(1, 4);
+  if (cols <= 8) return TMM_WARP(2, 4);
+  if (cols <= 16) return TMM_WARP(4, 4);
+  if (cols <= 32) return TMM_WARP(8, 4);
+  if (cols <= 64) return TMM_WARP(16, 4);
+  if (cols <= 128) return TMM_WARP(32, 4);
+  if (cols <= 256) return TMM_WARP(32, 8);
+  if (cols <= 512) return TMM_WARP(32, 16);
+  if (cols <= 1024) return TMM_WARP(32, 32);
+#undef TMM_WARP
+#undef TMM_WVEC
+  StagePlan plan;
+  if (plan_stage(cols, &plan)) {
+    switch (staged_threads(plan.chunk, plan.cluster)) {
+      case 128: return launch_staged_any<128>(rows, cols, plan, x, ldx, y, ldy, aligned, dev, stream);
+      case 256: return launch_staged_any<256>(rows, cols, plan, x, ldx, y, ldy, aligned, dev, stream);
+      case 512: return launch_staged_any<512>(rows, cols, plan, x, ldx, y, ldy, aligned, dev, stream);
+      default: return launch_staged_any<1024>(rows, cols, plan, x, ldx, y, ldy, aligned, dev, stream);
+    }
   }
   const int64_t grid = std::min<int64_t>(rows, int64_t(dev.sm_count) * 2);
   softmax_long_kernel<<<unsigned(grid), kLongRowThreads, 0, stream>>>(rows, cols, x, ldx, y, ldy);
