@@ -165,11 +165,17 @@ def ffma_peak_tflops(sm_count: int, peaks: dict) -> tuple[float, str]:
         f"{sm_count} SMs x 128 FFMA/clk x 2 FLOP x {mhz:.0f} MHz ({src})"
 
 
-KERNEL_SOURCES = {"gemm_simt": ["gemm_simt.cu"], "gemm_tc3": ["gemm_tc3.cu"]}
+KERNEL_SOURCES = {"gemm_simt": ["gemm_simt.cu"], "gemm_tc3": ["gemm_tc3.cu"],
+                  "window_sum": ["window_sum.cu"], "sum_partials": ["reduce_softmax.cu"],
+                  "softmax_staged": ["reduce_softmax.cu"]}
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu capture, if the kernel is unchanged since."""
+def recorded_traffic(kernel: str, workload: str, units: int | None = None):
+    """DRAM bytes per launch from the committed ncu capture, if the kernel is unchanged since.
+
+    A capture taken on a smaller case of a bandwidth-bound kernel records the
+    units (elements) it processed; its traffic is scaled to `units`, since
+    such a kernel's traffic grows in proportion to its input."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -180,7 +186,10 @@ def recorded_traffic(kernel: str, workload: str):
     from tiled_matrix_multiply_gb300 import build
     if rec.get("source_sha") != build.source_digest(KERNEL_SOURCES[kernel]):
         return None
-    return rec.get("dram_bytes_per_launch")
+    traffic = rec.get("dram_bytes_per_launch")
+    if traffic is not None and units is not None and rec.get("units"):
+        traffic = traffic * units / rec["units"]
+    return traffic
 
 
 # -- the oracle as the CPU baseline / reference arm ---------------------------------------------
@@ -476,7 +485,7 @@ def layouts_leg(args, w, A, B, C, flush, stream) -> dict:
     return {"steps": steps, "transa_transb": {"tn": [1, 0], "nt": [0, 1], "tt": [1, 1]}, **out}
 
 
-WINDOW_N = 1 << 28
+AUX_LOG2N = 28     # the window, sum and softmax legs each move 2^28 floats per call by default
 
 
 def window_leg(args, flush, stream, peaks) -> dict:
@@ -486,7 +495,7 @@ def window_leg(args, flush, stream, peaks) -> dict:
     from tiled_matrix_multiply_gb300 import _abi
     lib = _abi.load()
     W = 5
-    n = WINDOW_N
+    n = 1 << args.aux_log2n
     g = torch.Generator(device="cuda").manual_seed(5)
     x = torch.rand(n + W - 1, device="cuda", generator=g)
     y = torch.empty(n, device="cuda")
@@ -499,23 +508,25 @@ def window_leg(args, flush, stream, peaks) -> dict:
     nbytes = 4 * (n + W - 1) + 4 * n
     gbs = nbytes / (ms / 1e3) / 1e9
     peak = peaks.get("hbm_gbs") or 6800.0
-    return {"workload": f"window sum W={W}, n=2^28 outputs, uniform[0,1) floats",
+    del x, y
+    torch.cuda.empty_cache()
+    return {"workload": f"window sum W={W}, n=2^{args.aux_log2n} outputs, uniform[0,1) floats",
             "ms_per_step": ms, "value": gbs, "unit": "GB/s", "steps": steps,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                         "frac": gbs / peak, "traffic": None,
+                         "frac": gbs / peak,
+                         "traffic": recorded_traffic("window_sum", "w5", n),
                          "peak_source": ("MEASURED_PEAKS.json hbm_gbs" if peaks.get("hbm_gbs")
                                          else "fallback 6.8 TB/s"),
                          "algorithmic": f"4 (n + W - 1) + 4 n = {nbytes} bytes per call"}}
 
 
-SUM_N = 1 << 28
-SOFTMAX_SHAPE = (65536, 4096)
+SOFTMAX_COLS = 4096
 
 
-def _hbm_roofline(gbs, peaks, nbytes, what):
+def _hbm_roofline(gbs, peaks, nbytes, what, traffic=None):
     peak = peaks.get("hbm_gbs") or 6800.0
     return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-            "traffic": None,
+            "traffic": traffic,
             "peak_source": ("MEASURED_PEAKS.json hbm_gbs" if peaks.get("hbm_gbs")
                             else "fallback 6.8 TB/s"),
             "algorithmic": f"{what} = {nbytes} bytes per call"}
@@ -531,24 +542,29 @@ def reduction_legs(args, flush, stream, peaks) -> dict:
     g = torch.Generator(device="cuda").manual_seed(6)
     out = {}
 
-    x = torch.randn(SUM_N, device="cuda", generator=g)
+    n = 1 << args.aux_log2n
+    x = torch.randn(n, device="cuda", generator=g)
     res = torch.empty(1, device="cuda")
-    need = int(lib.sum_f32_workspace_size(SUM_N))
+    need = int(lib.sum_f32_workspace_size(n))
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
 
     def sum_step():
-        rc = lib.sum_f32(SUM_N, x.data_ptr(), res.data_ptr(), ws.data_ptr(), need,
+        rc = lib.sum_f32(n, x.data_ptr(), res.data_ptr(), ws.data_ptr(), need,
                          stream.cuda_stream)
         assert rc == _abi.TMM_OK, _abi.last_error()
     ms = statistics.mean(time_device(sum_step, flush, steps, args.warmup, stream, None))
-    nbytes = 4 * SUM_N
+    nbytes = 4 * n
     gbs = nbytes / (ms / 1e3) / 1e9
-    out["sum"] = {"workload": "array sum, n = 2^28 standard-normal floats", "ms_per_step": ms,
+    out["sum"] = {"workload": f"array sum, n = 2^{args.aux_log2n} standard-normal floats",
+                  "ms_per_step": ms,
                   "value": gbs, "unit": "GB/s", "steps": steps, "launches_per_step": 2,
-                  "roofline": _hbm_roofline(gbs, peaks, nbytes, "4 n")}
-    del x
+                  "roofline": _hbm_roofline(gbs, peaks, nbytes, "4 n",
+                                            recorded_traffic("sum_partials", "normal", n))}
+    del x, ws, res
+    torch.cuda.empty_cache()
 
-    rows, cols = SOFTMAX_SHAPE
+    cols = SOFTMAX_COLS
+    rows = (1 << args.aux_log2n) // cols
     xs = torch.randn(rows, cols, device="cuda", generator=g) * 4
     ys = torch.empty_like(xs)
 
@@ -562,7 +578,9 @@ def reduction_legs(args, flush, stream, peaks) -> dict:
     out["softmax"] = {"workload": f"row softmax, {rows} rows x {cols} cols, N(0, 16) logits",
                       "ms_per_step": ms, "value": gbs, "unit": "GB/s", "steps": steps,
                       "rows_per_s": rows / (ms / 1e3),
-                      "roofline": _hbm_roofline(gbs, peaks, nbytes, "4 rows cols read + 4 rows cols written")}
+                      "roofline": _hbm_roofline(
+                          gbs, peaks, nbytes, "4 rows cols read + 4 rows cols written",
+                          recorded_traffic("softmax_staged", f"cols{cols}", rows * cols))}
     return out
 
 
@@ -595,6 +613,9 @@ def main(argv=None):
     ap.add_argument("--no-tc3", action="store_true", help="skip the tensor-core (3xTF32) leg")
     ap.add_argument("--no-window", action="store_true", help="skip the window-sum leg")
     ap.add_argument("--no-reduce", action="store_true", help="skip the sum and softmax legs")
+    ap.add_argument("--aux-log2n", type=int, default=AUX_LOG2N,
+                    help="log2 of the floats each window/sum/softmax call moves (default 28; "
+                         "smaller for profiler captures)")
     ap.add_argument("--no-layouts", action="store_true",
                     help="skip the transposed-layout (gemm_f32_ex, gemm_f32_tc3_ex) leg")
     args = ap.parse_args(argv)
