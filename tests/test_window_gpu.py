@@ -54,7 +54,7 @@ def test_page_worked_example():
     assert np.array_equal(gpu_window(x, 5), [15, 20, 25, 30])
 
 
-@pytest.mark.parametrize("W", [1, 2, 3, 5, 7, 33, 129])
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 6, 7, 9, 11, 13, 15, 17, 18, 33, 129])
 @pytest.mark.parametrize("n", [1, 5, 4095, 4096, 4097, 12289, 100003])
 def test_random_float_bit_exact(W, n):
     rng = np.random.default_rng(90 + W)
