@@ -69,7 +69,7 @@ constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
 constexpr int kTcBK = 16;                          // floats per K-slice: one 64-byte swizzle row
 constexpr int kTcStages = 4;
-constexpr int kTcChunk = 128;                      // K values per tensor-memory sum
+constexpr int kTcChunk = 256;                      // K values per tensor-memory sum
 constexpr int kTcAccWarps = 8;                     // accumulate / epilogue warps
 constexpr int kTcThreads = 32 * (2 + kTcAccWarps); // copy warp, tensor-core warp, 8 more
 constexpr int kKPad = 32;                          // workspace K is a multiple of this
@@ -262,11 +262,11 @@ __device__ __forceinline__ void tc3_tile_coords(int tile, int tiles_n, int &tm, 
 struct Tc3Work {
   bool done;
   __device__ __forceinline__ void init(const Tc3Params &) { done = false; }
-  __device__ __forceinline__ bool next(const Tc3Params &p, int &tile, int &kb, int &ke,
+  // b: this block's index (one-CTA kernel) or its pair's (two-CTA kernel).
+  __device__ __forceinline__ bool next(const Tc3Params &p, int b, int &tile, int &kb, int &ke,
                                        int &unit) {
     if (done) return false;
     done = true;
-    const int b = blockIdx.x;
     if (b < p.dp_tiles) {
       tile = b;
       kb = 0;
@@ -351,7 +351,7 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
   if (threadIdx.x == 0) {
     // Copy role: TMA loads of each work item's slices into the ring.
     int r = 0;   // ring position (slices issued so far)
-    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
+    while (!timed_out && work.next(p, blockIdx.x, tile, kb, ke, unit)) {
       int tm, tn;
       tc3_tile_coords(tile, p.tiles_n, tm, tn);
       const int m0 = tm * kTcBM, n0 = tn * kTcBN;
@@ -382,7 +382,7 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
     // each chunk of kSlicesPerChunk slices into accumulator (chunk count % 2).
     int r = 0;   // ring position
     int q = 0;   // chunks started so far
-    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
+    while (!timed_out && work.next(p, blockIdx.x, tile, kb, ke, unit)) {
       for (int i = kb; i < ke && !timed_out; ++i, ++r) {
         const int s = r % kTcStages;
         const bool chunk_start = ((i - kb) % kSlicesPerChunk) == 0;
@@ -430,7 +430,7 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
     const int half = (warp - 2) >> 2;
     const int acc_warp = warp - 2;
     int q = 0;   // chunks consumed so far
-    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
+    while (!timed_out && work.next(p, blockIdx.x, tile, kb, ke, unit)) {
       float acc[kTcBN / 2];
 #pragma unroll
       for (int j = 0; j < kTcBN / 2; ++j) acc[j] = 0.0f;
@@ -523,6 +523,349 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
                  : "memory");
 }
 
+// ---- two-SM product kernel ----------------------------------------------------------
+//
+// The same product on CTA pairs (a cluster of two blocks on two SMs) with
+// tcgen05.mma.cta_group::2: one M = 256, N = 256, K = 8 instruction, issued by
+// the pair's first block (the leader), multiplies the 256 rows of A held by
+// the two blocks (128 each) with the 256 rows of B^T, also held 128 per block,
+// and writes rows 0-127 of the result into the leader's tensor memory and rows
+// 128-255 into the other block's.  Each block stages 128 rows of A and 128 of
+// B^T per K-slice (32 KiB, against 48 KiB for a 128 x 256 tile alone), so the
+// shared-memory traffic per SM, which bounds the one-block kernel, drops by a
+// third; the saved space deepens the ring to six stages.
+//
+// Synchronisation across the pair:
+//   * each block's copy thread loads its own halves into its own ring; the
+//     copies of both blocks complete on the leader's "full" barrier of the
+//     stage (cta_group::2 bulk copies may signal the peer's barrier), and the
+//     leader's copy thread announces the bytes of both;
+//   * the leader's commits arrive on the "empty" and "chunk done" barriers of
+//     both blocks at once (multicast), so each block's copy thread and
+//     accumulate warps wait on their own barriers;
+//   * the accumulate warps of both blocks release an accumulator on the
+//     leader's barrier (eight local arrivals and eight remote ones);
+//   * tensor memory is allocated and freed by one warp of each block together
+//     (cta_group::2), and cluster barriers separate the barrier set-up from the
+//     first remote arrival and the last remote arrival from the release.
+// Every wait is bounded as in the one-block kernel.
+
+constexpr int kT2Rows = 128;                       // rows of A and of B^T staged per block
+constexpr int kT2BM = 2 * kT2Rows;                 // rows of C per pair tile
+constexpr int kT2BN = 256;                         // columns of C per pair tile
+constexpr int kT2Stages = 6;
+constexpr uint32_t kT2TileBytes = kT2Rows * kTcBK * 4;    // 8 KiB
+constexpr uint32_t kT2StageBytes = 4 * kT2TileBytes;      // A hi, A lo, B^T hi, B^T lo
+constexpr uint32_t kT2BarrierBytes = 8 * (2 * kT2Stages + 5) + 8;
+constexpr uint32_t kT2SmemBytes = 1024 + kT2Stages * kT2StageBytes + kT2BarrierBytes;
+static_assert(kT2StageBytes % 1024 == 0 && kT2TileBytes % 1024 == 0, "tiles stay 1024-byte aligned");
+static_assert(kT2BN == kTcBN, "each block's accumulator keeps the one-block layout");
+
+// M = 256 (the pair), N = 256.
+constexpr uint32_t kIdescTf32Pair = (1u << 4) | (2u << 7) | (2u << 10) |
+                                    (uint32_t(kT2BN >> 3) << 17) | (uint32_t(kT2BM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of both blocks of the pair.
+__device__ __forceinline__ void pair_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// The shared::cluster address of `addr` (this block's shared memory) in block `rank`.
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  int64_t limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = timer_ns();
+  while (!mbar_try_wait_cluster(bar, parity))
+    if (int64_t(timer_ns() - t0) > limit_ns) return false;
+  return true;
+}
+// Bulk tensor copy into this block's shared memory whose completion is
+// counted on `bar`, a shared::cluster address in either block of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x,
+                                                 int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %3, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %4, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(accumulate), "r"(kIdescTf32Pair)
+      : "memory");
+}
+// Arrive on the barrier at offset `bar` of every block in `mask` once the pair
+// products issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+gemm_tc3_pair_kernel(const __grid_constant__ CUtensorMap map_ahi,
+                     const __grid_constant__ CUtensorMap map_alo,
+                     const __grid_constant__ CUtensorMap map_bhi,
+                     const __grid_constant__ CUtensorMap map_blo, const Tc3Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;            // same offsets in both blocks
+  const uint32_t bar_full = base + kT2Stages * kT2StageBytes;
+  const uint32_t bar_empty = bar_full + 8 * kT2Stages;
+  const uint32_t bar_tfull = bar_empty + 8 * kT2Stages;
+  const uint32_t bar_tempty = bar_tfull + 16;              // used in the leader
+  const uint32_t bar_drain = bar_tempty + 16;              // used in the leader
+  const uint32_t tmem_slot = bar_drain + 8;
+  volatile uint32_t *tmem_slot_ptr =
+      reinterpret_cast<volatile uint32_t *>(smem_raw + (tmem_slot - raw));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = int(blockIdx.x >> 1);
+  constexpr int kSlicesPerChunk = kTcChunk / kTcBK;
+  unsigned int *flags =
+      g_tc3_flags + (p.epoch % kTc3FlagRegions) * (kTc3MaxBlocks * kTc3FlagsPerBlock);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kT2Stages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);     // used in the leader
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 2 * kTcAccWarps);
+    }
+    mbar_init(bar_drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     tmem_slot),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  pair_sync();          // both blocks' barriers exist before any arrival crosses the pair
+  tc_fence_after();
+  const uint32_t tmem_d = *tmem_slot_ptr;
+
+  bool timed_out = false;
+  Tc3Work work;
+  work.init(p);
+  int tile, kb, ke, unit;
+  if (threadIdx.x == 0) {
+    // Copy role (both blocks): this block's 128 rows of A and of B^T per slice.
+    const uint32_t leader_full = map_rank(bar_full, 0);
+    int r = 0;
+    while (!timed_out && work.next(p, pair, tile, kb, ke, unit)) {
+      int tm, tn;
+      tc3_tile_coords(tile, p.tiles_n, tm, tn);
+      const int m0 = tm * kT2BM + int(rank) * kT2Rows;
+      const int nb0 = tn * kT2BN + int(rank) * kT2Rows;
+      for (int i = kb; i < ke; ++i, ++r) {
+        const int s = r % kT2Stages;
+        if (r >= kT2Stages &&
+            !mbar_wait_cluster(bar_empty + 8 * s, uint32_t((r / kT2Stages) - 1) & 1u,
+                               p.wait_limit_ns)) {
+          timed_out = true;
+          break;
+        }
+        const uint32_t full = leader_full + 8 * s;
+        const uint32_t st = base + s * kT2StageBytes;
+        const int kx = i * kTcBK;
+        if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * kT2StageBytes);
+        tma_load_2d_pair(st, &map_ahi, kx, m0, full);
+        tma_load_2d_pair(st + kT2TileBytes, &map_alo, kx, m0, full);
+        tma_load_2d_pair(st + 2 * kT2TileBytes, &map_bhi, kx, nb0, full);
+        tma_load_2d_pair(st + 3 * kT2TileBytes, &map_blo, kx, nb0, full);
+      }
+    }
+    if (timed_out && leader) {
+      // The leader's barriers count both blocks' copies: once they complete,
+      // nothing is in flight into either block.
+      for (int i = r > kT2Stages ? r - kT2Stages : 0; i < r; ++i)
+        mbar_wait_cluster(bar_full + 8 * (i % kT2Stages), uint32_t(i / kT2Stages) & 1u,
+                          p.wait_limit_ns);
+    }
+  } else if (threadIdx.x == 32 && leader) {
+    // Tensor-core role (leader): as in the one-block kernel, on pair instructions.
+    int r = 0;
+    int q = 0;
+    while (!timed_out && work.next(p, pair, tile, kb, ke, unit)) {
+      for (int i = kb; i < ke && !timed_out; ++i, ++r) {
+        const int s = r % kT2Stages;
+        const bool chunk_start = ((i - kb) % kSlicesPerChunk) == 0;
+        if (chunk_start) {
+          if (q >= 2 && !mbar_wait_cluster(bar_tempty + 8 * (q & 1),
+                                           uint32_t((q >> 1) - 1) & 1u, p.wait_limit_ns)) {
+            timed_out = true;
+            break;
+          }
+          ++q;
+        }
+        const int buf = (q - 1) & 1;
+        if (!mbar_wait_cluster(bar_full + 8 * s, uint32_t(r / kT2Stages) & 1u,
+                               p.wait_limit_ns)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = base + s * kT2StageBytes;
+        const uint32_t d = tmem_d + uint32_t(buf * kT2BN);
+#pragma unroll
+        for (int kk = 0; kk < kTcBK / 8; ++kk) {
+          const uint32_t koff = 32u * kk;
+          const uint64_t a_hi = sw64_desc(st + koff);
+          const uint64_t a_lo = sw64_desc(st + kT2TileBytes + koff);
+          const uint64_t b_hi = sw64_desc(st + 2 * kT2TileBytes + koff);
+          const uint64_t b_lo = sw64_desc(st + 3 * kT2TileBytes + koff);
+          mma_tf32_pair(d, a_lo, b_hi, (chunk_start && kk == 0) ? 0u : 1u);
+          mma_tf32_pair(d, a_hi, b_lo, 1u);
+          mma_tf32_pair(d, a_hi, b_hi, 1u);
+        }
+        mma_commit_pair(bar_empty + 8 * s, 3);          // both blocks' stage s is free
+        if ((i - kb) % kSlicesPerChunk == kSlicesPerChunk - 1 || i == ke - 1)
+          mma_commit_pair(bar_tfull + 8 * buf, 3);      // both halves of accumulator buf ready
+      }
+    }
+    mma_commit_pair(bar_drain, 1);
+    if (!mbar_wait(bar_drain, 0u, p.wait_limit_ns)) timed_out = true;
+  } else if (warp >= 2) {
+    // Accumulate role (both blocks): this block's 128 rows of the pair tile.
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int acc_warp = warp - 2;
+    const uint32_t tempty = leader ? bar_tempty : map_rank(bar_tempty, 0);
+    int q = 0;
+    while (!timed_out && work.next(p, pair, tile, kb, ke, unit)) {
+      float acc[kT2BN / 2];
+#pragma unroll
+      for (int j = 0; j < kT2BN / 2; ++j) acc[j] = 0.0f;
+      const int chunks = (ke - kb + kSlicesPerChunk - 1) / kSlicesPerChunk;
+      for (int c = 0; c < chunks; ++c, ++q) {
+        const int buf = q & 1;
+        const bool ready =
+            mbar_wait_cluster(bar_tfull + 8 * buf, uint32_t(q >> 1) & 1u, p.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, ready)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_d + (uint32_t(32 * quarter) << 16) +
+                               uint32_t(buf * kT2BN + half * (kT2BN / 2));
+#pragma unroll
+        for (int cc = 0; cc < kT2BN / 2; cc += 8) {
+          float v[8];
+          __syncwarp();
+          tmem_load_8(taddr + uint32_t(cc), v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[cc + j] += v[j];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(tempty + 8 * buf);
+          else mbar_arrive_remote(tempty + 8 * buf);
+        }
+      }
+      if (timed_out) break;
+      int tm, tn;
+      tc3_tile_coords(tile, p.tiles_n, tm, tn);
+      const int row = tm * kT2BM + int(rank) * kT2Rows + 32 * quarter + lane;
+      const int col0 = tn * kT2BN + half * (kT2BN / 2);
+      const int flag = int(rank) * kTcAccWarps + acc_warp;   // per block of the pair and warp
+      const bool owner_of_split = kb == 0 && ke < p.slices;
+      if (owner_of_split) {
+        if (lane == 0) {
+          const unsigned int *f = &flags[(unit + 1) * 2 * kTcAccWarps + flag];
+          const uint64_t t0 = timer_ns();
+          while (ld_acquire_u32(f) != p.epoch) {
+            if (int64_t(timer_ns() - t0) > p.wait_limit_ns) {
+              atomicOr(&g_tc3_status, 2u);
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+        __syncwarp();
+      }
+      if (row < p.M) {
+        float *c_row = p.C + int64_t(row) * p.ldc;
+#pragma unroll
+        for (int c = 0; c < kT2BN / 2; c += 4) {
+          const int col = col0 + c;
+          if (p.vec_store && col + 4 <= p.N) {
+            float4 v = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+            if (owner_of_split) {
+              const float4 w = __ldcg(reinterpret_cast<const float4 *>(c_row + col));
+              v.x = w.x + v.x; v.y = w.y + v.y; v.z = w.z + v.z; v.w = w.w + v.w;
+            }
+            *reinterpret_cast<float4 *>(c_row + col) = v;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (col + j < p.N) {
+                float v = acc[c + j];
+                if (owner_of_split) v = __ldcg(c_row + col + j) + v;
+                c_row[col + j] = v;
+              }
+          }
+        }
+      }
+      if (kb > 0) {
+        __syncwarp();
+        if (lane == 0 && unit != p.drop_signal_block) {
+          __threadfence();
+          st_release_u32(&flags[unit * 2 * kTcAccWarps + flag], p.epoch);
+        }
+      }
+    }
+  }
+  __syncwarp();
+  if (timed_out) atomicOr(&g_tc3_status, 2u);
+
+  tc_fence_before();
+  __syncthreads();
+  pair_sync();          // every remote arrival has landed; neither block uses tensor memory
+  tc_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_d),
+                 "r"(kTmemCols)
+                 : "memory");
+}
+
 // ---- host side ------------------------------------------------------------------
 
 int64_t pad_k(int64_t K) { return (K + kKPad - 1) / kKPad * kKPad; }
@@ -564,6 +907,81 @@ std::atomic<int> g_tc3_blocks_per_sm[64];
 std::atomic<int64_t> g_tc3_wait_limit_ns{int64_t(10) * 1000 * 1000 * 1000};
 std::atomic<unsigned int> g_tc3_epoch{0};
 std::atomic<int> g_tc3_drop_signal_block{-1};
+
+// Work split shared by both kernels: whole tiles, and when the last wave is at
+// most half full, its tiles in two K halves (units 2t, 2t + 1).
+void plan_tiles(Tc3Params &prm, int64_t tiles, int64_t slots, int max_units, int slices) {
+  constexpr int kSlicesPerChunk = kTcChunk / kTcBK;
+  const int64_t rem = slots > 0 ? tiles % slots : 0;
+  const bool split_tail = tiles > slots && rem > 0 && 2 * rem <= slots &&
+                          2 * rem <= max_units && slices >= 2 * kSlicesPerChunk;
+  prm.slices = slices;
+  prm.split = std::max(kSlicesPerChunk, (slices / 2) / kSlicesPerChunk * kSlicesPerChunk);
+  prm.dp_tiles = int(split_tail ? tiles - rem : tiles);
+}
+
+unsigned int next_epoch() {
+  unsigned int ep = g_tc3_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (ep == 0) ep = g_tc3_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  return ep;
+}
+
+std::atomic<uint64_t> g_tc3_pair_configured{0};
+std::atomic<int> g_tc3_pair_slots[64];
+
+cudaError_t launch_tc3_pairs(const GemmProblem &p, const DeviceInfo &dev, int64_t Kp,
+                             const CUtensorMap (&maps)[4], cudaStream_t stream) {
+  auto kernel = gemm_tc3_pair_kernel;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = kT2SmemBytes;
+  cfg.stream = stream;
+  const uint64_t bit = uint64_t(1) << (dev.id & 63);
+  if (!(g_tc3_pair_configured.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kT2SmemBytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * 64, 1, 1);   // shape only, for the query
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorLaunchOutOfResources;
+    g_tc3_pair_slots[dev.id & 63].store(clusters, std::memory_order_relaxed);
+    g_tc3_pair_configured.fetch_or(bit, std::memory_order_release);
+  }
+  const int64_t slots = g_tc3_pair_slots[dev.id & 63].load(std::memory_order_relaxed);
+  const int64_t tiles_m = (p.M + kT2BM - 1) / kT2BM;
+  const int64_t tiles_n = (p.N + kT2BN - 1) / kT2BN;
+  const int64_t tiles = tiles_m * tiles_n;
+  Tc3Params prm = {};
+  prm.M = int(p.M);
+  prm.N = int(p.N);
+  prm.Kp = int(Kp);
+  prm.C = p.C;
+  prm.ldc = p.ldc;
+  prm.tiles_m = int(tiles_m);
+  prm.tiles_n = int(tiles_n);
+  // Split units use flags per (unit, block of the pair, warp): half as many units fit.
+  plan_tiles(prm, tiles, slots, kTc3MaxBlocks / 2, int(Kp / kTcBK));
+  prm.vec_store = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0) ? 1 : 0;
+  prm.wait_limit_ns = g_tc3_wait_limit_ns.load(std::memory_order_relaxed);
+  prm.drop_signal_block = g_tc3_drop_signal_block.load(std::memory_order_relaxed);
+  prm.epoch = next_epoch();
+  const int64_t items = prm.dp_tiles + 2 * (tiles - prm.dp_tiles);
+  if (2 * items > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  cfg.gridDim = dim3(unsigned(2 * items), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], maps[3], prm);
+}
 
 }  // namespace
 
@@ -610,13 +1028,18 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
     if (e != cudaSuccess) return e;
   }
 
-  // 2. product kernel.
+  // 2. product kernel: on block pairs once A has more rows than one block's
+  // tile and K is long enough to amortise the pair's deeper pipeline (each
+  // block then stages 128 rows of B^T as well), else one block per tile.
+  const bool pairs = p.M > kTcBM && Kp >= 1024;
   CUtensorMap maps[4];
+  const uint32_t b_box = pairs ? uint32_t(kT2Rows) : uint32_t(kTcBN);
   if ((e = encode_operand(&maps[0], a_hi, p.M, Kp, kTcBM)) != cudaSuccess ||
       (e = encode_operand(&maps[1], a_lo, p.M, Kp, kTcBM)) != cudaSuccess ||
-      (e = encode_operand(&maps[2], b_hi, p.N, Kp, kTcBN)) != cudaSuccess ||
-      (e = encode_operand(&maps[3], b_lo, p.N, Kp, kTcBN)) != cudaSuccess)
+      (e = encode_operand(&maps[2], b_hi, p.N, Kp, b_box)) != cudaSuccess ||
+      (e = encode_operand(&maps[3], b_lo, p.N, Kp, b_box)) != cudaSuccess)
     return e;
+  if (pairs) return launch_tc3_pairs(p, dev, Kp, maps, stream);
   const uint64_t bit = uint64_t(1) << (dev.id & 63);
   if (!(g_tc3_configured.load(std::memory_order_acquire) & bit)) {
     e = cudaFuncSetAttribute(gemm_tc3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -637,14 +1060,8 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
   const int64_t tiles_m = (p.M + kTcBM - 1) / kTcBM;
   const int64_t tiles_n = (p.N + kTcBN - 1) / kTcBN;
   const int64_t tiles = tiles_m * tiles_n;
-  const int slices = int(Kp / kTcBK);
-  constexpr int kSlicesPerChunk = kTcChunk / kTcBK;
   const int64_t slots =
       int64_t(g_tc3_blocks_per_sm[dev.id & 63].load(std::memory_order_relaxed)) * dev.sm_count;
-  const int64_t rem = slots > 0 ? tiles % slots : 0;
-  const bool split_tail = tiles > slots && rem > 0 && 2 * rem <= slots &&
-                          2 * rem <= kTc3MaxBlocks && slices >= 2 * kSlicesPerChunk;
-  if (tiles + (split_tail ? rem : 0) > 0x7fffffff) return cudaErrorInvalidConfiguration;
   Tc3Params prm = {};
   prm.M = int(p.M);
   prm.N = int(p.N);
@@ -653,17 +1070,13 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
   prm.ldc = p.ldc;
   prm.tiles_m = int(tiles_m);
   prm.tiles_n = int(tiles_n);
-  prm.slices = slices;
+  plan_tiles(prm, tiles, slots, kTc3MaxBlocks, int(Kp / kTcBK));
   prm.vec_store = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0) ? 1 : 0;
   prm.wait_limit_ns = g_tc3_wait_limit_ns.load(std::memory_order_relaxed);
   prm.drop_signal_block = g_tc3_drop_signal_block.load(std::memory_order_relaxed);
-  // The halves meet at a chunk boundary near the middle of K.
-  prm.split = std::max(kSlicesPerChunk, (slices / 2) / kSlicesPerChunk * kSlicesPerChunk);
-  prm.dp_tiles = int(split_tail ? tiles - rem : tiles);
-  const int64_t grid = split_tail ? (tiles - rem) + 2 * rem : tiles;
-  unsigned int ep = g_tc3_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
-  if (ep == 0) ep = g_tc3_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
-  prm.epoch = ep;
+  prm.epoch = next_epoch();
+  const int64_t grid = prm.dp_tiles + 2 * (tiles - prm.dp_tiles);
+  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
 
   gemm_tc3_kernel<<<unsigned(grid), kTcThreads, kTcSmemBytes, stream>>>(maps[0], maps[1],
                                                                        maps[2], maps[3], prm);
