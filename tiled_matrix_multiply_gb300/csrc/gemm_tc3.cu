@@ -246,6 +246,7 @@ struct Tc3Params {
   int slices;            // K-slices per tile
   int dp_tiles;          // blocks [0, dp_tiles) each process tile blockIdx.x whole
   int split;             // blocks from dp_tiles on: tail tile halves [0, split), [split, S)
+  int items;             // dp_tiles + 2 x (split tiles): the work list
   unsigned int epoch;    // this call's flag value (never 0)
   int vec_store;         // C 16-byte aligned and ldc % 4 == 0
   int64_t wait_limit_ns;
@@ -257,16 +258,24 @@ __device__ __forceinline__ void tc3_tile_coords(int tile, int tiles_n, int &tm, 
   tn = tile - tm * tiles_n;
 }
 
-// This block's single work item (tile, K-slice range); `unit` >= 0 numbers
-// the blocks that share a split tile (even: lower half, owner; odd: upper half).
+// This block's work items (tile, K-slice range): items b, b + stride, ...
+// of the list [whole tiles, split units]; `unit` >= 0 numbers the items that
+// share a split tile (even: lower half, owner; odd: upper half).  The one-block
+// kernel launches one block per item; the pair kernel one pair per resident
+// slot, each pair walking its items in order.  Whole tiles are a multiple of
+// the stride whenever units exist, so all units fall in the last round, each on
+// its own pair and alongside its partner.
 struct Tc3Work {
-  bool done;
-  __device__ __forceinline__ void init(const Tc3Params &) { done = false; }
-  // b: this block's index (one-CTA kernel) or its pair's (two-CTA kernel).
-  __device__ __forceinline__ bool next(const Tc3Params &p, int b, int &tile, int &kb, int &ke,
+  int idx, stride;
+  __device__ __forceinline__ void init(const Tc3Params &, int first, int step) {
+    idx = first;
+    stride = step;
+  }
+  __device__ __forceinline__ bool next(const Tc3Params &p, int &tile, int &kb, int &ke,
                                        int &unit) {
-    if (done) return false;
-    done = true;
+    if (idx >= p.items) return false;
+    const int b = idx;
+    idx += stride;
     if (b < p.dp_tiles) {
       tile = b;
       kb = 0;
@@ -346,12 +355,12 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
 
   bool timed_out = false;
   Tc3Work work;
-  work.init(p);
+  work.init(p, int(blockIdx.x), int(gridDim.x));
   int tile, kb, ke, unit;
   if (threadIdx.x == 0) {
     // Copy role: TMA loads of each work item's slices into the ring.
     int r = 0;   // ring position (slices issued so far)
-    while (!timed_out && work.next(p, blockIdx.x, tile, kb, ke, unit)) {
+    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
       int tm, tn;
       tc3_tile_coords(tile, p.tiles_n, tm, tn);
       const int m0 = tm * kTcBM, n0 = tn * kTcBN;
@@ -382,7 +391,7 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
     // each chunk of kSlicesPerChunk slices into accumulator (chunk count % 2).
     int r = 0;   // ring position
     int q = 0;   // chunks started so far
-    while (!timed_out && work.next(p, blockIdx.x, tile, kb, ke, unit)) {
+    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
       for (int i = kb; i < ke && !timed_out; ++i, ++r) {
         const int s = r % kTcStages;
         const bool chunk_start = ((i - kb) % kSlicesPerChunk) == 0;
@@ -430,7 +439,7 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
     const int half = (warp - 2) >> 2;
     const int acc_warp = warp - 2;
     int q = 0;   // chunks consumed so far
-    while (!timed_out && work.next(p, blockIdx.x, tile, kb, ke, unit)) {
+    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
       float acc[kTcBN / 2];
 #pragma unroll
       for (int j = 0; j < kTcBN / 2; ++j) acc[j] = 0.0f;
@@ -683,13 +692,13 @@ gemm_tc3_pair_kernel(const __grid_constant__ CUtensorMap map_ahi,
 
   bool timed_out = false;
   Tc3Work work;
-  work.init(p);
+  work.init(p, pair, int(gridDim.x >> 1));
   int tile, kb, ke, unit;
   if (threadIdx.x == 0) {
     // Copy role (both blocks): this block's 128 rows of A and of B^T per slice.
     const uint32_t leader_full = map_rank(bar_full, 0);
     int r = 0;
-    while (!timed_out && work.next(p, pair, tile, kb, ke, unit)) {
+    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
       int tm, tn;
       tc3_tile_coords(tile, p.tiles_n, tm, tn);
       const int m0 = tm * kT2BM + int(rank) * kT2Rows;
@@ -723,7 +732,7 @@ gemm_tc3_pair_kernel(const __grid_constant__ CUtensorMap map_ahi,
     // Tensor-core role (leader): as in the one-block kernel, on pair instructions.
     int r = 0;
     int q = 0;
-    while (!timed_out && work.next(p, pair, tile, kb, ke, unit)) {
+    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
       for (int i = kb; i < ke && !timed_out; ++i, ++r) {
         const int s = r % kT2Stages;
         const bool chunk_start = ((i - kb) % kSlicesPerChunk) == 0;
@@ -769,7 +778,7 @@ gemm_tc3_pair_kernel(const __grid_constant__ CUtensorMap map_ahi,
     const int acc_warp = warp - 2;
     const uint32_t tempty = leader ? bar_tempty : map_rank(bar_tempty, 0);
     int q = 0;
-    while (!timed_out && work.next(p, pair, tile, kb, ke, unit)) {
+    while (!timed_out && work.next(p, tile, kb, ke, unit)) {
       float acc[kT2BN / 2];
 #pragma unroll
       for (int j = 0; j < kT2BN / 2; ++j) acc[j] = 0.0f;
@@ -918,6 +927,7 @@ void plan_tiles(Tc3Params &prm, int64_t tiles, int64_t slots, int max_units, int
   prm.slices = slices;
   prm.split = std::max(kSlicesPerChunk, (slices / 2) / kSlicesPerChunk * kSlicesPerChunk);
   prm.dp_tiles = int(split_tail ? tiles - rem : tiles);
+  prm.items = int(prm.dp_tiles + 2 * (tiles - prm.dp_tiles));
 }
 
 unsigned int next_epoch() {
@@ -978,8 +988,10 @@ cudaError_t launch_tc3_pairs(const GemmProblem &p, const DeviceInfo &dev, int64_
   prm.drop_signal_block = g_tc3_drop_signal_block.load(std::memory_order_relaxed);
   prm.epoch = next_epoch();
   const int64_t items = prm.dp_tiles + 2 * (tiles - prm.dp_tiles);
-  if (2 * items > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  cfg.gridDim = dim3(unsigned(2 * items), 1, 1);
+  if (items > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  // Persistent: one pair per resident slot, each walking its items; the next
+  // tile's copies and products start while the previous tile is being stored.
+  cfg.gridDim = dim3(unsigned(2 * std::min<int64_t>(items, slots)), 1, 1);
   return cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], maps[3], prm);
 }
 
@@ -1075,7 +1087,7 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
   prm.wait_limit_ns = g_tc3_wait_limit_ns.load(std::memory_order_relaxed);
   prm.drop_signal_block = g_tc3_drop_signal_block.load(std::memory_order_relaxed);
   prm.epoch = next_epoch();
-  const int64_t grid = prm.dp_tiles + 2 * (tiles - prm.dp_tiles);
+  const int64_t grid = prm.dp_tiles + 2 * (tiles - prm.dp_tiles);   // one block per item
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
 
   gemm_tc3_kernel<<<unsigned(grid), kTcThreads, kTcSmemBytes, stream>>>(maps[0], maps[1],
