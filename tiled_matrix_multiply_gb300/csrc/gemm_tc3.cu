@@ -188,8 +188,11 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
 
 // Rows of K values (M x K, ld) -> hi, lo (M x Kp), zeros for k >= K.  Thread
 // handles 4 consecutive k of one row; rows advance with the grid's y extent.
+// write_hi = 0: only lo is written (the product then reads hi from the operand
+// itself -- see launch_tc3).
 __global__ void tc3_split_a_kernel(int M, int K, int Kp, const float *__restrict__ A, int64_t lda,
-                                   int vec_load, float *__restrict__ hi, float *__restrict__ lo) {
+                                   int vec_load, int write_hi, float *__restrict__ hi,
+                                   float *__restrict__ lo) {
   const int k = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (k >= Kp) return;
   for (int m = blockIdx.y; m < M; m += gridDim.y) {
@@ -206,7 +209,7 @@ __global__ void tc3_split_a_kernel(int M, int K, int Kp, const float *__restrict
 #pragma unroll
     for (int j = 0; j < 4; ++j) split_tf32(x[j], h[j], l[j]);
     const int64_t o = int64_t(m) * Kp + k;
-    *reinterpret_cast<float4 *>(hi + o) = make_float4(h[0], h[1], h[2], h[3]);
+    if (write_hi) *reinterpret_cast<float4 *>(hi + o) = make_float4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<float4 *>(lo + o) = make_float4(l[0], l[1], l[2], l[3]);
   }
 }
@@ -897,11 +900,12 @@ cudaError_t get_encoder() {
   return g_encode_status;
 }
 
-// K-major operand of `rows` x Kp floats; box of kTcBK x box_rows, 64-byte swizzle.
-cudaError_t encode_operand(CUtensorMap *map, const float *base, int64_t rows, int64_t Kp,
-                           uint32_t box_rows) {
-  const cuuint64_t dims[2] = {cuuint64_t(Kp), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(Kp) * 4};
+// K-major operand: `rows` rows of `kdim` floats, `ld` floats apart; box of
+// kTcBK x box_rows, 64-byte swizzle.  Reads past kdim or rows return zeros.
+cudaError_t encode_operand(CUtensorMap *map, const float *base, int64_t rows, int64_t kdim,
+                           int64_t ld, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cuuint64_t(kdim), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(ld) * 4};
   const cuuint32_t box[2] = {cuuint32_t(kTcBK), box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base),
@@ -1014,15 +1018,26 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
   float *b_lo = reinterpret_cast<float *>(ws + 2 * round256(size_t(p.M) * Kp * 4) +
                                           round256(size_t(p.N) * Kp * 4));
 
+  // The tensor core reads a TF32 operand from an FP32 word by ignoring its low
+  // 13 mantissa bits -- exactly the hi of the split (measured: products from
+  // raw FP32 words and from masked ones agree bit for bit).  So an operand
+  // already stored K-major (A as M x K, B as N x K) whose rows start on
+  // 16-byte boundaries serves as its own hi: only lo is written for it.
+  const bool raw_a = !p.transa && p.K > 0 &&
+                     (reinterpret_cast<uintptr_t>(p.A) & 15u) == 0 && p.lda % 4 == 0;
+  const bool raw_b = p.transb && p.K > 0 &&
+                     (reinterpret_cast<uintptr_t>(p.B) & 15u) == 0 && p.ldb % 4 == 0;
+
   // 1. split pre-pass: op(A) -> M x Kp and op(B)^T -> N x Kp, K-major.  An
   // operand stored with K contiguous (A as M x K, B as N x K) is split row by
   // row; one stored with K as its rows (A as K x M, B as K x N) is transposed.
   {
-    auto split_rows = [&](const float *src, int64_t ld, int64_t rows, float *hi, float *lo) {
+    auto split_rows = [&](const float *src, int64_t ld, int64_t rows, float *hi, float *lo,
+                          bool write_hi) {
       const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && ld % 4 == 0;
       const dim3 grid(unsigned((Kp / 4 + 255) / 256), unsigned(std::min<int64_t>(rows, 65535)));
       tc3_split_a_kernel<<<grid, 256, 0, stream>>>(int(rows), int(p.K), int(Kp), src, ld,
-                                                   vec ? 1 : 0, hi, lo);
+                                                   vec ? 1 : 0, write_hi ? 1 : 0, hi, lo);
       return cudaGetLastError();
     };
     auto split_transposed = [&](const float *src, int64_t ld, int64_t cols, float *hi,
@@ -1033,9 +1048,9 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
       return cudaGetLastError();
     };
     e = p.transa ? split_transposed(p.A, p.lda, p.M, a_hi, a_lo)
-                 : split_rows(p.A, p.lda, p.M, a_hi, a_lo);
+                 : split_rows(p.A, p.lda, p.M, a_hi, a_lo, !raw_a);
     if (e != cudaSuccess) return e;
-    e = p.transb ? split_rows(p.B, p.ldb, p.N, b_hi, b_lo)
+    e = p.transb ? split_rows(p.B, p.ldb, p.N, b_hi, b_lo, !raw_b)
                  : split_transposed(p.B, p.ldb, p.N, b_hi, b_lo);
     if (e != cudaSuccess) return e;
   }
@@ -1046,10 +1061,14 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
   const bool pairs = p.M > kTcBM && Kp >= 1024;
   CUtensorMap maps[4];
   const uint32_t b_box = pairs ? uint32_t(kT2Rows) : uint32_t(kTcBN);
-  if ((e = encode_operand(&maps[0], a_hi, p.M, Kp, kTcBM)) != cudaSuccess ||
-      (e = encode_operand(&maps[1], a_lo, p.M, Kp, kTcBM)) != cudaSuccess ||
-      (e = encode_operand(&maps[2], b_hi, p.N, Kp, b_box)) != cudaSuccess ||
-      (e = encode_operand(&maps[3], b_lo, p.N, Kp, b_box)) != cudaSuccess)
+  e = raw_a ? encode_operand(&maps[0], p.A, p.M, p.K, p.lda, kTcBM)
+            : encode_operand(&maps[0], a_hi, p.M, Kp, Kp, kTcBM);
+  if (e != cudaSuccess) return e;
+  e = raw_b ? encode_operand(&maps[2], p.B, p.N, p.K, p.ldb, b_box)
+            : encode_operand(&maps[2], b_hi, p.N, Kp, Kp, b_box);
+  if (e != cudaSuccess) return e;
+  if ((e = encode_operand(&maps[1], a_lo, p.M, Kp, Kp, kTcBM)) != cudaSuccess ||
+      (e = encode_operand(&maps[3], b_lo, p.N, Kp, Kp, b_box)) != cudaSuccess)
     return e;
   if (pairs) return launch_tc3_pairs(p, dev, Kp, maps, stream);
   const uint64_t bit = uint64_t(1) << (dev.id & 63);
