@@ -218,6 +218,9 @@ __global__ void tc3_split_a_kernel(int M, int K, int Kp, const float *__restrict
 // k >= K; 32 x 32 tiles through shared memory.
 __global__ void tc3_split_bt_kernel(int K, int N, int Kp, const float *__restrict__ B, int64_t ldb,
                                     float *__restrict__ hi, float *__restrict__ lo) {
+  // The product kernel may be scheduled now; it waits for this grid to finish
+  // before its first read of the split operands.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float tile[32][33];
   const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
   const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
@@ -699,6 +702,9 @@ gemm_tc3_pair_kernel(const __grid_constant__ CUtensorMap map_ahi,
   int tile, kb, ke, unit;
   if (threadIdx.x == 0) {
     // Copy role (both blocks): this block's 128 rows of A and of B^T per slice.
+    // The launch may overlap the split pre-pass (programmatic dependent launch):
+    // wait until it has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t leader_full = map_rank(bar_full, 0);
     int r = 0;
     while (!timed_out && work.next(p, tile, kb, ke, unit)) {
@@ -947,7 +953,7 @@ cudaError_t launch_tc3_pairs(const GemmProblem &p, const DeviceInfo &dev, int64_
                              const CUtensorMap (&maps)[4], cudaStream_t stream) {
   auto kernel = gemm_tc3_pair_kernel;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
@@ -996,6 +1002,11 @@ cudaError_t launch_tc3_pairs(const GemmProblem &p, const DeviceInfo &dev, int64_
   // Persistent: one pair per resident slot, each walking its items; the next
   // tile's copies and products start while the previous tile is being stored.
   cfg.gridDim = dim3(unsigned(2 * std::min<int64_t>(items, slots)), 1, 1);
+  // Start the blocks (barriers, tensor memory) while the split pre-pass
+  // finishes; the copy thread waits for it before reading (griddepcontrol.wait).
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], maps[3], prm);
 }
 
