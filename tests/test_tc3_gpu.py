@@ -180,15 +180,14 @@ def test_python_binding_side_stream():
     parity.assert_close(C.cpu().numpy(), oracle.gemm(A, B), 200, "binding")
 
 
-@pytest.mark.parametrize("K", [512, 1024])
-def test_stream_k_wait_timeout_is_reported_and_recovers(K):
-    # 2560 x 2560 leaves a partial last wave, so the tail tiles are split along
-    # K: at K = 512 on the one-block kernel (200 tiles of 128 x 256, 152 per
-    # wave), at K = 1024 on the block-pair kernel (100 tiles of 256 x 256, 76
-    # pairs per wave).  Block 1 (pair unit 1) never raises its flags.
+@pytest.mark.parametrize("M,N,K", [(128, 51200, 512), (2560, 2560, 512), (2560, 2560, 1024)])
+def test_stream_k_wait_timeout_is_reported_and_recovers(M, N, K):
+    # Each shape leaves a partial last wave, so the tail tiles are split along
+    # K: 128 rows run on the one-block kernel (200 tiles of 128 x 256, 152 per
+    # wave); 2560 x 2560 on the block-pair kernel (100 tiles of 256 x 256, 76
+    # pairs per wave).  Split unit 1 never raises its flags.
     lib = _abi.load()
     stream = torch.cuda.current_stream().cuda_stream
-    M, N = 2560, 2560
     rng = np.random.default_rng(58)
     A = rng.integers(-4, 5, (M, K)).astype(np.float32)
     B = rng.integers(-4, 5, (K, N)).astype(np.float32)

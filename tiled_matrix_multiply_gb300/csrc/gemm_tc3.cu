@@ -1067,9 +1067,9 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
   }
 
   // 2. product kernel: on block pairs once A has more rows than one block's
-  // tile and K is long enough to amortise the pair's deeper pipeline (each
-  // block then stages 128 rows of B^T as well), else one block per tile.
-  const bool pairs = p.M > kTcBM && Kp >= 1024;
+  // tile (each block then stages 128 rows of B^T as well), else one block per
+  // tile.  (Measured: pairs are faster at every K from 128 up once M > 128.)
+  const bool pairs = p.M > kTcBM;
   CUtensorMap maps[4];
   const uint32_t b_box = pairs ? uint32_t(kT2Rows) : uint32_t(kTcBN);
   e = raw_a ? encode_operand(&maps[0], p.A, p.M, p.K, p.lda, kTcBM)
