@@ -10,17 +10,22 @@
 // integers (|x| < 2^11) are exact TF32 values (lo = 0), so integer-valued
 // inputs stay exact.
 //
-// Structure (two launches per call):
+// Structure (two pre-pass launches and one product launch per call):
 //   1. split pre-pass -- A into A_hi, A_lo (M x Kp, K-major) and B, transposed,
 //      into B_hi, B_lo (N x Kp, K-major), in the caller's workspace; Kp is K
-//      rounded up to 32 with zeros, so every K-slice is whole;
-//   2. product kernel -- one 128 x 256 tile of C per block, three roles:
+//      rounded up to 32 with zeros, so every K-slice is whole.  The tensor
+//      core reads a TF32 operand by ignoring the low 13 bits of an FP32 word,
+//      which is exactly hi, so an operand already stored K-major with aligned
+//      rows is read as its own hi and only its lo is written;
+//   2. product kernel, for M > 128 on block pairs (gemm_tc3_pair_kernel,
+//      described before it: 256 x 256 tiles, tcgen05.mma.cta_group::2,
+//      persistent), else one 128 x 256 tile per block (gemm_tc3_kernel), with
+//      three roles in each block:
 //      * copy (one thread): TMA (tensor-map bulk copies, 64-byte swizzle)
-//        loads K-slices of 16 of the four operands into a 4-stage ring;
-//      * tensor core (one thread): tcgen05.mma.kind::tf32 (M=128, N=256, K=8),
-//        three per K-step, into one of two tensor-memory accumulators
-//        (128 lanes x 256 FP32 columns each), switching buffers every
-//        kTcChunk values of K;
+//        loads K-slices of 16 of the four operands into a ring of stages;
+//      * tensor core (one thread): tcgen05.mma.kind::tf32, three per K-step,
+//        into one of two tensor-memory accumulators (128 lanes x 256 FP32
+//        columns each), switching buffers every kTcChunk values of K;
 //      * accumulate (eight warps): as each chunk completes, read it with
 //        tcgen05.ld and add it into FP32 registers (round to nearest), then
 //        release the buffer; after the last chunk, store C.
@@ -28,14 +33,14 @@
 //      (measured: error growing linearly in K); bounding each tensor-memory
 //      sum to kTcChunk values of K and adding the chunks on the CUDA cores
 //      keeps the product within FP32 accuracy at any K.
-// Scheduling: one block per tile, tiles in row-major order, so the blocks of
-// a wave move through K together and share the A and B panels in L2.  When
-// the tile count leaves the last wave at most half full, each of its tiles is
-// split into two halves of the K range, run side by side by two blocks: the
-// block holding the upper half stores its partial sums into C and raises a
-// flag (one per accumulate warp), the block holding the lower half waits for
-// it (bounded), adds, and stores the total -- in that fixed order, so results
-// are deterministic.  The last wave then takes half the time.
+// Scheduling: tiles in row-major order, so the tiles in flight move through K
+// together and share the A and B panels in L2.  When the tile count leaves the
+// last wave at most half full, each of its tiles is split into two halves of
+// the K range, run side by side: the unit holding the upper half stores its
+// partial sums into C and raises a flag (one per accumulate warp), the unit
+// holding the lower half waits for it (bounded), adds, and stores the total --
+// in that fixed order, so results are deterministic.  The last wave then takes
+// half the time.
 // This follows the block-tile / staged-slab schedule of "CMU DLSys Lecture 12"
 // section 5 and the double buffering of "Tiling Strategies" section 3; the
 // register tile is replaced by a tensor-memory accumulator.
@@ -549,6 +554,13 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
 // B^T per K-slice (32 KiB, against 48 KiB for a 128 x 256 tile alone), so the
 // shared-memory traffic per SM, which bounds the one-block kernel, drops by a
 // third; the saved space deepens the ring to six stages.
+//
+// The grid is persistent: one pair per resident slot, each walking its work
+// items (Tc3Work), so the ring, the accumulator buffers and the chunk count
+// run on from one tile to the next and a tile's stores overlap the next
+// tile's first copies and products.  The copy thread starts with
+// griddepcontrol.wait: the launch may begin while the split pre-pass is
+// finishing (programmatic dependent launch).
 //
 // Synchronisation across the pair:
 //   * each block's copy thread loads its own halves into its own ring; the
