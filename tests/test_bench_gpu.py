@@ -1,0 +1,73 @@
+"""bench.py on the GPU: one JSON line that keeps the benchmark contract.
+
+Runs the headline leg and every extra leg with few steps (and the window, sum
+and softmax legs on 2^22 floats) in a subprocess, then checks the keys, the
+units and that the numbers are consistent with each other.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def line():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "5",
+                          "--warmup", "3", "--cpu-seconds", "1", "--aux-log2n", "22"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, out.stdout
+    return json.loads(lines[0])
+
+
+def test_contract_keys(line):
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "roofline", "cpu_baseline", "clocks", "e2e", "gpu_launches"):
+        assert k in line, k
+    assert line["unit"] == "TFLOP/s" and line["n_gpus"] == 1 and line["higher_is_better"]
+    assert line["steps"] == 5 and line["warmup"] == 3
+    assert line["config"]["workload"].startswith("square4096")
+    assert line["gpu_launches"] == line["steps"]
+
+
+def test_value_matches_time_and_roofline(line):
+    flops = 2 * 4096 ** 3
+    assert line["value"] == pytest.approx(flops / (line["ms_per_step"] / 1e3) / 1e12, rel=1e-6)
+    r = line["roofline"]
+    assert r["bound"] == "alu" and r["unit"] == "TFLOP/s"
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], rel=1e-6)
+    assert 0.3 < r["frac"] < 1.1
+
+
+def test_e2e_and_cpu_baseline(line):
+    e = line["e2e"]
+    assert e["unit"] == "TFLOP/s"
+    assert e["h2d_bytes_per_step"] == 2 * 4096 * 4096 * 4
+    assert e["d2h_bytes_per_step"] == 4096 * 4096 * 4
+    assert 0 < e["value"] <= line["value"] * 1.05
+    assert e["serial_value"] < e["value"]
+    c = line["cpu_baseline"]
+    assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0
+
+
+def test_extra_legs(line):
+    t = line["tc3"]
+    assert t["unit"] == "TFLOP/s" and t["roofline"]["bound"] == "tensor" and t["value"] > 0
+    for leg in ("window5", "sum", "softmax"):
+        r = line[leg]["roofline"]
+        assert r["bound"] == "hbm" and r["unit"] == "GB/s" and 0.05 < r["frac"] < 1.2, leg
+    for lay in ("tn", "nt", "tt"):
+        assert line["layouts"][lay]["gemm_f32_ex"]["value"] > 0
+        assert line["layouts"][lay]["gemm_f32_tc3_ex"]["value"] > 0
+    assert line["contrast"]["gemm_f32_naive"]["value"] < line["value"]
