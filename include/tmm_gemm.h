@@ -204,11 +204,11 @@ int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K,
 
 /*
  * tmm_check_device -- synchronise `stream`, then read and clear the current
- * device's status word.  Returns TMM_OK, or TMM_ERR_DEVICE_TIMEOUT when a
- * bounded wait inside gemm_f32 (between the two blocks sharing a split tile)
- * or gemm_f32_tc3 (between the copy, tensor-core and epilogue roles of a
- * block) ran out of time since the last check; results written since then are
- * not valid.  The pages have no counterpart: this is the library's failure
+ * device's status words.  Returns TMM_OK, or TMM_ERR_DEVICE_TIMEOUT when a
+ * bounded wait inside gemm_f32 (between the two blocks sharing a split tile),
+ * gemm_f32_tc3 (between the copy, tensor-core and epilogue roles of a block
+ * or block pair) or window_sum_f32 (for a tile's bulk copy) ran out of time
+ * since the last check; results written since then are not valid.  The pages have no counterpart: this is the library's failure
  * detection ("CMU DLSys Lecture 12" section 2 only asks that API and launch
  * errors be checked).  TMM_ERR_CUDA if the synchronisation itself failed.
  */
@@ -218,8 +218,10 @@ int tmm_check_device(tmm_stream_t stream);
  * tmm_testing_set_wait_hooks -- testing only; no counterpart in the pages.
  * drop_signal_block >= 0 makes that block of later stream-K launches (of
  * gemm_f32 and gemm_f32_tc3) skip raising its flags, so the block waiting on
- * it runs into the time limit;
- * wait_limit_ns > 0 sets the limit of every bounded wait of both kernels
+ * it runs into the time limit, and makes that block of later window_sum_f32
+ * launches (16-byte-aligned x) wait for 16 bytes more than its first tile
+ * copy brings;
+ * wait_limit_ns > 0 sets the limit of every bounded wait of these kernels
  * (default, and for values <= 0, 10 s).
  * Process-wide; pass (-1, 0) to restore the defaults.  Always TMM_OK.
  */

@@ -87,3 +87,24 @@ def test_rejects_bad_arguments():
     assert lib.window_sum_f32(10, 130, x.data_ptr(), x.data_ptr() + 400, s) == _abi.TMM_ERR_INVALID_ARG
     assert lib.window_sum_f32(50, 5, x.data_ptr(), x.data_ptr() + 40, s) == _abi.TMM_ERR_ALIAS
     assert lib.window_sum_f32(0, 5, 0, 0, s) == _abi.TMM_OK
+
+
+def test_bulk_copy_wait_timeout_is_reported_and_recovers():
+    # Block 0 is armed for 16 bytes more than its first tile copy brings, so its
+    # bounded wait runs out (2 ms); the status is reported once and the next call
+    # is correct again.
+    lib = _abi.load()
+    s = torch.cuda.current_stream().cuda_stream
+    x = np.arange(1 << 20, dtype=np.float32) % 7
+    assert lib.tmm_check_device(s) == _abi.TMM_OK
+    try:
+        assert lib.tmm_testing_set_wait_hooks(0, 2_000_000) == _abi.TMM_OK
+        xb = torch.from_numpy(x).cuda()
+        yb = torch.empty(x.shape[0] - 4, device="cuda")
+        assert lib.window_sum_f32(x.shape[0] - 4, 5, xb.data_ptr(), yb.data_ptr(), s) == _abi.TMM_OK
+        assert lib.tmm_check_device(s) == _abi.TMM_ERR_DEVICE_TIMEOUT
+        assert "window_sum_f32" in _abi.last_error()
+    finally:
+        lib.tmm_testing_set_wait_hooks(-1, 0)
+    assert lib.tmm_check_device(s) == _abi.TMM_OK
+    check(x, 5)

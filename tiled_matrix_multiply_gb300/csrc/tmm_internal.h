@@ -49,6 +49,8 @@ void tc3_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns);
 
 // Sliding-window sums (y_i = sum_{d<W} x_{i+d}, i < n); 1 <= W <= kMaxWindow.
 constexpr int kMaxWindow = 129;
+cudaError_t window_device_status(unsigned int *status, bool clear);
+void window_set_test_hooks(int drop_block, int64_t wait_limit_ns);
 cudaError_t launch_window_sum(int64_t n, int W, const float *x, float *y,
                               const DeviceInfo &dev, cudaStream_t stream);
 

@@ -11,10 +11,11 @@
 // GB300 layout: the work is bound by HBM bandwidth (8 bytes moved per
 // output), so the kernel is shaped for bandwidth, not arithmetic:
 //   * tiles of T = 256 x 16 = 4096 outputs; a grid of a few blocks per SM
-//     strides over them.  Each block stages its tiles with cp.async (16-byte
-//     copies when x is 16-byte aligned) two buffers deep: the next tile's
-//     copies are in flight while this one is summed (the halo is re-read by
-//     the next tile, an L2 hit);
+//     strides over them.  Each block stages its tiles two buffers deep, the
+//     next tile's copy in flight while this one is summed (the halo is re-read
+//     by the next tile, an L2 hit): one bulk copy (the TMA unit's
+//     cp.async.bulk, counted on an mbarrier) per tile when x is 16-byte
+//     aligned, 4-byte cp.async copies by every thread otherwise;
 //   * thread t owns outputs t, t + 256, ..., so a warp's shared-memory reads
 //     and global stores are consecutive words (no bank conflicts, full
 //     128-byte store lines);
@@ -26,6 +27,10 @@
 #include "tmm_internal.h"
 
 namespace tmm {
+
+// Device status word (bit 0: a bounded wait for a bulk copy ran out of time).
+__device__ unsigned int g_win_status;
+
 namespace {
 
 constexpr int kWinThreads = 256;
@@ -35,17 +40,53 @@ constexpr int kWinMaxHalo = kMaxWindow - 1;
 constexpr int kWinBuf = kWinTile + kWinMaxHalo + 4;  // floats per staging buffer (16-byte multiple)
 constexpr int kWinSmemBytes = 2 * kWinBuf * int(sizeof(float));
 
-__device__ __forceinline__ void win_cp16(float *dst, const float *src) {
-  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
-}
-
 __device__ __forceinline__ void win_cp4(float *dst, const float *src) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
 }
 
 __device__ __forceinline__ void win_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+
+__device__ __forceinline__ void win_bar_init(uint32_t bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+// One bulk copy of `bytes` (a multiple of 16) from global to shared memory,
+// counted on `bar`, which this thread arms for exactly those bytes.
+// `expect` is the byte count the barrier is armed for (bytes, except under the
+// testing hook that makes one block wait for bytes that never come).
+__device__ __forceinline__ void win_bulk(float *dst, const float *src, uint32_t bytes,
+                                         uint32_t expect, uint32_t bar) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(expect)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(d),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ bool win_bar_try(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Bounded wait for phase `parity`; false after limit_ns.
+__device__ __forceinline__ bool win_bar_wait(uint32_t bar, uint32_t parity, int64_t limit_ns) {
+  if (win_bar_try(bar, parity)) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    if (win_bar_try(bar, parity)) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (int64_t(t - t0) > limit_ns) return false;
+  }
+}
 
 template <int N>
 __device__ __forceinline__ void win_wait() {
@@ -55,8 +96,9 @@ __device__ __forceinline__ void win_wait() {
 template <int kW>   // kW > 0: compile-time width; 0: runtime width
 __global__ void __launch_bounds__(kWinThreads)
 window_sum_kernel(int64_t n, int W_rt, const float *__restrict__ x, float *__restrict__ y,
-                  int vec) {
+                  int vec, int64_t wait_limit_ns, int drop_block) {
   extern __shared__ __align__(16) float stage[];   // two buffers of kWinBuf floats
+  __shared__ __align__(8) uint64_t bars[2];         // bulk copies into buffer b (vec)
   const int W = kW > 0 ? kW : W_rt;
   const int64_t len = n + W - 1;                  // valid input elements
   const int64_t tiles = (n + kWinTile - 1) / kWinTile;
@@ -64,29 +106,61 @@ window_sum_kernel(int64_t n, int W_rt, const float *__restrict__ x, float *__res
   const int t = threadIdx.x;
   // Copy tile tl's inputs (the tile and its halo; nothing past the input's end:
   // those slots only feed outputs >= n, which are not stored).
-  auto copy_tile = [&](float *buf, int64_t tl) {
+  // With x 16-byte aligned (vec), one thread moves the whole 16-byte-aligned
+  // part with a single bulk copy counted on the buffer's barrier, and the at
+  // most three elements after it are plain loads (seen by the other threads
+  // after the barrier that precedes the tile's use).  Otherwise every thread
+  // issues 4-byte asynchronous copies.
+  const uint32_t bar0 = static_cast<uint32_t>(__cvta_generic_to_shared(&bars[0]));
+  if (vec && t == 0) {
+    win_bar_init(bar0);
+    win_bar_init(bar0 + 8);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (vec) __syncthreads();
+  auto copy_tile = [&](int b, int64_t tl) {
+    float *buf = stage + b * kWinBuf;
     const int64_t base = tl * kWinTile;
     const int64_t rem = len - base;
     const int avail = rem < need ? int(rem) : need;
     if (vec) {
-      const int nv = avail >> 2;
-      for (int q = t; q < nv; q += kWinThreads) win_cp16(buf + 4 * q, x + base + 4 * q);
-      for (int j = 4 * nv + t; j < avail; j += kWinThreads) win_cp4(buf + j, x + base + j);
+      const int body = avail & ~3;
+      if (t == 0) {
+        const uint32_t bar = bar0 + 8u * uint32_t(b);
+        const uint32_t bytes = uint32_t(body) * 4u;
+        // Testing hook: block drop_block waits for 16 bytes more than its first copy brings.
+        const uint32_t extra = (int(blockIdx.x) == drop_block && tl == blockIdx.x) ? 16u : 0u;
+        if (body > 0) win_bulk(buf, x + base, bytes, bytes + extra, bar);
+        else asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+      }
+      if (t < avail - body) buf[body + t] = x[base + body + t];
     } else {
       for (int j = t; j < avail; j += kWinThreads) win_cp4(buf + j, x + base + j);
     }
   };
+  bool timed_out = false;
+  int stop_it = -1;            // the iteration a timeout ended (vec)
+  bool next_issued = false;
   int64_t tl = blockIdx.x;
-  if (tl < tiles) copy_tile(stage, tl);
+  if (tl < tiles) copy_tile(0, tl);
   win_commit();
   for (int it = 0; tl < tiles; tl += gridDim.x, ++it) {
     const float *tile = stage + (it & 1) * kWinBuf;
     const int64_t next = tl + gridDim.x;
     // The other buffer was last read before the barrier that ended the previous tile.
-    if (next < tiles) copy_tile(stage + ((it + 1) & 1) * kWinBuf, next);
+    next_issued = next < tiles;
+    if (next_issued) copy_tile((it + 1) & 1, next);
     win_commit();
-    win_wait<1>();       // this thread's copies of tile tl have landed ...
-    __syncthreads();     // ... and every thread's
+    if (vec) {
+      if (!win_bar_wait(bar0 + 8u * uint32_t(it & 1), uint32_t(it >> 1) & 1u, wait_limit_ns))
+        timed_out = true;
+    } else {
+      win_wait<1>();     // this thread's copies of tile tl have landed ...
+    }
+    if (__syncthreads_or(timed_out)) {   // ... and every thread's
+      stop_it = it;
+      break;
+    }
     const int64_t base = tl * kWinTile;
 #pragma unroll 4
     for (int j = 0; j < kWinItems; ++j) {
@@ -103,7 +177,20 @@ window_sum_kernel(int64_t n, int W_rt, const float *__restrict__ x, float *__res
     __syncthreads();     // every thread is done with this buffer before it is refilled
   }
   win_wait<0>();
+  if (stop_it >= 0 && t == 0) {
+    // Record the timeout, and give the bulk copies that may still be in flight
+    // (this tile's and the next one's) a bounded time to land before the
+    // block's shared memory goes away.
+    atomicOr(&g_win_status, 1u);
+    win_bar_wait(bar0 + 8u * uint32_t(stop_it & 1), uint32_t(stop_it >> 1) & 1u, wait_limit_ns);
+    if (next_issued)
+      win_bar_wait(bar0 + 8u * uint32_t((stop_it + 1) & 1), uint32_t((stop_it + 1) >> 1) & 1u,
+                   wait_limit_ns);
+  }
 }
+
+std::atomic<int64_t> g_win_wait_limit_ns{int64_t(10) * 1000 * 1000 * 1000};
+std::atomic<int> g_win_drop_block{-1};
 
 template <int kW>
 cudaError_t launch_width(int64_t n, int W, const float *x, float *y, int vec,
@@ -123,11 +210,26 @@ cudaError_t launch_width(int64_t n, int W, const float *x, float *y, int vec,
   if (e != cudaSuccess) return e;
   const int64_t tiles = (n + kWinTile - 1) / kWinTile;
   const int64_t grid = std::min<int64_t>(tiles, int64_t(dev.sm_count) * (nb > 0 ? nb : 1));
-  kernel<<<unsigned(grid), kWinThreads, kWinSmemBytes, stream>>>(n, W, x, y, vec);
+  kernel<<<unsigned(grid), kWinThreads, kWinSmemBytes, stream>>>(
+      n, W, x, y, vec, g_win_wait_limit_ns.load(std::memory_order_relaxed),
+      g_win_drop_block.load(std::memory_order_relaxed));
   return cudaGetLastError();
 }
 
 }  // namespace
+
+void window_set_test_hooks(int drop_block, int64_t wait_limit_ns) {
+  g_win_drop_block.store(drop_block, std::memory_order_relaxed);
+  g_win_wait_limit_ns.store(wait_limit_ns > 0 ? wait_limit_ns : int64_t(10) * 1000 * 1000 * 1000,
+                            std::memory_order_relaxed);
+}
+
+cudaError_t window_device_status(unsigned int *status, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, g_win_status, sizeof(unsigned int));
+  if (e != cudaSuccess || !clear) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_win_status, &zero, sizeof(unsigned int));
+}
 
 cudaError_t launch_window_sum(int64_t n, int W, const float *x, float *y,
                               const DeviceInfo &dev, cudaStream_t stream) {
