@@ -135,8 +135,12 @@ int gemm_f32_naive(int64_t M, int64_t N, int64_t K,
  * operand split into two TF32 values, x = hi + lo (hi: x with its low 13
  * mantissa bits cleared; lo: the exact remainder rounded to TF32), and
  *     A B ~ A_hi B_hi + A_hi B_lo + A_lo B_hi
- * accumulated in FP32 tensor memory (the dropped A_lo B_lo term is about
- * 2^-22 of each product).  The pages do not go beyond FP32 FMA units ("CMU
+ * accumulated in FP32: each 256 values of K in tensor memory, the chunks
+ * added in FP32 registers (the dropped A_lo B_lo term is about 2^-22 of each
+ * product; normwise error about 2e-6 at any K).  An operand stored K-major
+ * (A as M x K here) whose rows start on 16-byte boundaries is read in place as
+ * its own hi (the tensor core ignores the low 13 bits of an FP32 word), so
+ * only its lo is written to the workspace.  The pages do not go beyond FP32 FMA units ("CMU
  * DLSys Lecture 12" section 6 notes that tensor instructions change the
  * implementation); the tiling is that of section 5 with the register tile
  * replaced by a tensor-memory accumulator.  Same contract as gemm_f32, plus:
