@@ -1,13 +1,16 @@
 """GPU tests of the persistent stream-K schedule of gemm_f32 and of its bounded waits.
 
-Shapes are chosen so that the tile count (128 x 128 tiles) leaves a partial
+Shapes are chosen so that the tile count (64 x 256 tiles) leaves a partial
 last wave on a 152-SM GB300 with two resident blocks per SM, which sends
 gemm_f32 down the persistent stream-K path: split tiles are summed by two
-blocks that meet through a flag.  The timeout test makes one block skip its
-flag (a testing hook of the library) with a 2 ms limit: the waiting block
-must give up, the library must report TMM_ERR_DEVICE_TIMEOUT through
-tmm_check_device, and the next call must be correct again.  No kernel faults
-or hangs: every wait is bounded and the kernel always runs to completion.
+blocks that meet through a flag.  The small shapes have fewer tiles than
+resident blocks: every tile is split over several consecutive blocks, each
+adding the next block's running sum (a chain of up to five).  The timeout
+tests make one block skip its flag (a testing hook of the library) with a
+2 ms limit: the waiting block must give up, the library must report
+TMM_ERR_DEVICE_TIMEOUT through tmm_check_device, and the next call must be
+correct again.  No kernel faults or hangs: every wait is bounded and the
+kernel always runs to completion.
 """
 import numpy as np
 import pytest
@@ -35,8 +38,14 @@ def _run(*a, **k):
 
 
 # (M, N, K): all tiles split (400 tiles); data-parallel waves plus split tiles
-# (1089 tiles); ragged K; ragged M and N with odd leading dimensions.
-SK_SHAPES = [(2560, 2560, 1000), (4224, 4224, 256), (2600, 2700, 1001), (3001, 2999, 777)]
+# (1122 tiles); ragged K; ragged M and N with odd leading dimensions.  Then
+# fewer tiles than resident blocks: 64 tiles in four equal shares each; 64
+# tiles of 187 slices in shares that straddle tiles; one tile over four
+# blocks; single rows and columns; 4 tiles of 16 slices; 200 tiles (shares of
+# two thirds of a tile).
+SK_SHAPES = [(2560, 2560, 1000), (4224, 4224, 256), (2600, 2700, 1001), (3001, 2999, 777),
+             (1024, 1024, 1024), (1000, 1000, 2990), (64, 256, 4096), (1, 1, 1024),
+             (37, 1000, 2000), (256, 256, 256), (1280, 2560, 1024)]
 
 
 @pytest.mark.parametrize("shape", SK_SHAPES)
@@ -65,10 +74,13 @@ def test_stream_k_shapes_integer_exact_and_deterministic(shape):
     assert np.array_equal(D1.view(np.uint32), D2.view(np.uint32))
 
 
-def test_stream_k_wait_timeout_is_reported_and_recovers():
+@pytest.mark.parametrize("shape", [(2560, 2560, 256), (1024, 1024, 1024)])
+def test_stream_k_wait_timeout_is_reported_and_recovers(shape):
+    # 2560^2 x 256: block 1 holds the tail of a two-block tile.  1024^3: block 1
+    # holds the second of four shares of tile 0, so block 0 waits for it.
     lib = _abi.load()
     stream = torch.cuda.current_stream().cuda_stream
-    M, N, K = 2560, 2560, 256
+    M, N, K = shape
     rng = np.random.default_rng(42)
     A = rng.integers(-4, 5, (M, K)).astype(np.float32)
     B = rng.integers(-4, 5, (K, N)).astype(np.float32)

@@ -113,6 +113,27 @@ def test_float_odd_shapes(shape):
     parity.assert_close(_run(A, B), oracle.gemm(A, B), K, f"{shape}")
 
 
+# Fewer tiles than half the slots: every tile is cut into K-parts of at least
+# two 256-value chunks, each part adding the next part's running sum.  Block
+# pairs: 6 tiles in 4 parts; 16 tiles in 2 parts, the last chunk 32 values long.
+# One-block kernel: 4 tiles of K = 2000 in 4 parts; one tile of K = 8192 in 4 parts.
+PART_SHAPES = [(512, 768, 3000), (1024, 1024, 1050), (100, 1000, 2000), (64, 256, 8192)]
+
+
+@pytest.mark.parametrize("shape", PART_SHAPES)
+def test_k_parts_float_integer_and_deterministic(shape):
+    M, N, K = shape
+    rng = np.random.default_rng(59)
+    A = rng.random((M, K), dtype=np.float32) * 2 - 1
+    B = rng.random((K, N), dtype=np.float32) * 2 - 1
+    C1 = _run(A, B)
+    parity.assert_close(C1, oracle.gemm(A, B), K, f"parts {shape}")
+    assert np.array_equal(C1.view(np.uint32), _run(A, B).view(np.uint32))
+    Ai = rng.integers(-4, 5, (M, K)).astype(np.float32)
+    Bi = rng.integers(-4, 5, (K, N)).astype(np.float32)
+    parity.assert_bit_exact(_run(Ai, Bi), oracle.gemm(Ai, Bi), f"parts {shape} integer")
+
+
 @pytest.mark.parametrize("layout", [(4, 8, 12, 4, 8, 4), (1, 3, 5, 0, 0, 0), (5, 7, 9, 3, 1, 1)])
 def test_layouts(layout):
     pa, pb, pc, oa, ob, oc = layout
@@ -180,12 +201,15 @@ def test_python_binding_side_stream():
     parity.assert_close(C.cpu().numpy(), oracle.gemm(A, B), 200, "binding")
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 51200, 512), (2560, 2560, 512), (2560, 2560, 1024)])
+@pytest.mark.parametrize("M,N,K", [(128, 51200, 512), (2560, 2560, 512), (2560, 2560, 1024),
+                                   (512, 768, 3000), (100, 1000, 2000)])
 def test_stream_k_wait_timeout_is_reported_and_recovers(M, N, K):
-    # Each shape leaves a partial last wave, so the tail tiles are split along
-    # K: 128 rows run on the one-block kernel (200 tiles of 128 x 256, 152 per
-    # wave); 2560 x 2560 on the block-pair kernel (100 tiles of 256 x 256, 76
-    # pairs per wave).  Split unit 1 never raises its flags.
+    # The first three shapes leave a partial last wave, so the tail tiles are
+    # split along K: 128 rows run on the one-block kernel (200 tiles of
+    # 128 x 256, 152 per wave); 2560 x 2560 on the block-pair kernel (100 tiles
+    # of 256 x 256, 76 pairs per wave).  The last two have few tiles, each cut
+    # into four K-parts (pairs; one-block kernel), so unit 1 is a middle part.
+    # Split unit 1 never raises its flags.
     lib = _abi.load()
     stream = torch.cuda.current_stream().cuda_stream
     rng = np.random.default_rng(58)

@@ -47,9 +47,13 @@
 // contributors: the block holding slices [x, S) stores its partial sums into
 // C and raises a flag; the block holding slices [0, x) -- which reaches the
 // tile last -- waits for the flag, adds the partial to its own sums and
-// stores the total.  The order of that addition is fixed, so results are
-// deterministic.  The wait is bounded: past the time limit the block records
-// a timeout in the device status word and finishes.
+// stores the total.  With fewer tiles than slots, all tiles are split this way
+// over more blocks than tiles, and a tile can have up to about five
+// contributors: each block waits for the next block's flag, adds C (the sum
+// of the slices after its own) to its sums, stores, and raises its own flag
+// for the block before it.  The order of the additions is fixed, so results
+// are deterministic.  The wait is bounded: past the time limit the block
+// records a timeout in the device status word and finishes.
 #include <atomic>
 #include <cstdint>
 
@@ -430,16 +434,40 @@ struct SimtBlock {
     const int row0 = m0 + a_off;
     const int col0 = n0 + b_off;
     float *c_base = p.C + int64_t(row0) * p.ldc + col0;
+    // kAdd: the partial sums of kAddRows rows are all loaded before the first
+    // store, so the loads are in flight together (a store before a load of the
+    // same array would order them one after another).
+    constexpr int kAddRows = 4;
+    static_assert(Cf::TM % kAddRows == 0, "whole row groups");
 #pragma unroll
-    for (int t = 0; t < Cf::TM / 4; ++t) {
+    for (int r0 = 0; r0 < Cf::TM; r0 += kAddRows) {
+      float4 w[kAddRows][Cf::TN / 4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int dr = 4 * Cf::LM * t + i;
+      for (int i = 0; i < kAddRows; ++i)
+#pragma unroll
+        for (int c = 0; c < Cf::TN / 4; ++c) w[i][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (kAdd && p.vec_store) {
+#pragma unroll
+        for (int i = 0; i < kAddRows; ++i) {
+          const int r = r0 + i;
+          const int dr = 4 * Cf::LM * (r / 4) + r % 4;
+          if (row0 + dr >= p.M) continue;
+          const float *c_row = c_base + int64_t(dr) * p.ldc;
+#pragma unroll
+          for (int c = 0; c < Cf::TN / 4; ++c)
+            if (col0 + 4 * Cf::LN * c < p.N)
+              w[i][c] = __ldcg(reinterpret_cast<const float4 *>(c_row + 4 * Cf::LN * c));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kAddRows; ++i) {
+        const int r = r0 + i;
+        const int dr = 4 * Cf::LM * (r / 4) + r % 4;
         if (row0 + dr >= p.M) continue;
         float *c_row = c_base + int64_t(dr) * p.ldc;
         float a[Cf::TN];
 #pragma unroll
-        for (int j = 0; j < Cf::TN / 2; ++j) unpack2(acc[4 * t + i][j], a[2 * j], a[2 * j + 1]);
+        for (int j = 0; j < Cf::TN / 2; ++j) unpack2(acc[r][j], a[2 * j], a[2 * j + 1]);
 #pragma unroll
         for (int c = 0; c < Cf::TN / 4; ++c) {
           const int dc = 4 * Cf::LN * c;
@@ -447,8 +475,8 @@ struct SimtBlock {
             if (col0 + dc < p.N) {
               float4 v = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
               if (kAdd) {
-                const float4 w = __ldcg(reinterpret_cast<const float4 *>(c_row + dc));
-                v.x = w.x + v.x; v.y = w.y + v.y; v.z = w.z + v.z; v.w = w.w + v.w;
+                v.x = w[i][c].x + v.x; v.y = w[i][c].y + v.y;
+                v.z = w[i][c].z + v.z; v.w = w[i][c].w + v.w;
               }
               *reinterpret_cast<float4 *>(c_row + dc) = v;
             }
@@ -498,7 +526,7 @@ gemm_simt_kernel(const SimtParams p) {
     blk.mainloop(p, smem, m0, n0, s_begin, s_end);
     if (s_begin == 0 && s_end == p.slices) {
       blk.template epilogue<false>(p, m0, n0);
-    } else if (s_begin > 0) {
+    } else if (s_end == p.slices) {
       // Slices [s_begin, S): store the partial sums, then raise this block's flag.
       blk.template epilogue<false>(p, m0, n0);
       __syncthreads();
@@ -507,7 +535,8 @@ gemm_simt_kernel(const SimtParams p) {
         store_release(&flags[b], p.epoch);
       }
     } else {
-      // Slices [0, s_end): the next block holds [s_end, S); wait for its partial.
+      // Slices [s_begin, s_end) with s_end < S: the next block holds the slices
+      // from s_end on and has stored their sum into C; wait for it, add.
       if (threadIdx.x == 0) {
         const uint64_t t0 = global_timer_ns();
         while (load_acquire(&flags[b + 1]) != p.epoch) {
@@ -520,6 +549,15 @@ gemm_simt_kernel(const SimtParams p) {
       }
       __syncthreads();
       blk.template epilogue<true>(p, m0, n0);
+      if (s_begin > 0) {
+        // A middle share (small problems only): C now holds the sum of slices
+        // [s_begin, S), which the previous block waits for.
+        __syncthreads();
+        if (threadIdx.x == 0 && int(b) != p.drop_signal_block) {
+          __threadfence();
+          store_release(&flags[b], p.epoch);
+        }
+      }
     }
     it += s_end - s_begin;
   }
@@ -586,19 +624,31 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStre
   const int64_t rem = slots > 0 ? tiles % slots : 0;
   const bool stream_k = slots > 0 && slots <= kMaxPersistentBlocks && tiles > slots &&
                         rem != 0 && rem * 10 < slots * 9 && slices >= 4;
+  // Fewer tiles than slots: every tile's K-slices are shared by up to about
+  // five consecutive blocks (a share is at least a quarter of a tile and four
+  // slices), when that gives at least an eighth more blocks than tiles.
+  int64_t small_blocks = 0;
+  if (!stream_k && slots > 0 && slots <= kMaxPersistentBlocks && tiles < slots) {
+    const int64_t iters = tiles * slices;
+    int64_t share = (iters + slots - 1) / slots;
+    share = share > (slices + 3) / 4 ? share : (slices + 3) / 4;
+    share = share > 4 ? share : 4;
+    const int64_t g = (iters + share - 1) / share;
+    if (g * 8 >= tiles * 9) small_blocks = g;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(Cf::kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  if (stream_k) {
-    const int64_t sk_tiles = rem + slots;
+  if (stream_k || small_blocks > 0) {
+    const int64_t sk_tiles = stream_k ? rem + slots : tiles;
     prm.dp_tiles = int(tiles - sk_tiles);
     prm.sk_iters = sk_tiles * slices;
     unsigned int e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
     if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
     prm.epoch = e;
-    cfg.gridDim = dim3(unsigned(slots), 1, 1);
+    cfg.gridDim = dim3(unsigned(stream_k ? slots : small_blocks), 1, 1);
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;

@@ -40,7 +40,13 @@
 // partial sums into C and raises a flag (one per accumulate warp), the unit
 // holding the lower half waits for it (bounded), adds, and stores the total --
 // in that fixed order, so results are deterministic.  The last wave then takes
-// half the time.
+// half the time.  With at most half as many tiles as slots, every tile is cut
+// into up to four K-parts on chunk boundaries in the same way: the last part
+// stores, and each earlier part waits for the next one's flag, adds C, stores
+// and (unless it is the first) raises its own flag.
+// Epilogue: each accumulate warp holds 32 rows (one per lane) of 128 columns;
+// it stores them through a 4 KiB staging buffer in shared memory, transposed
+// so that every store instruction writes whole 128-byte lines of C.
 // This follows the block-tile / staged-slab schedule of "CMU DLSys Lecture 12"
 // section 5 and the double buffering of "Tiling Strategies" section 3; the
 // register tile is replaced by a tensor-memory accumulator.
@@ -83,7 +89,11 @@ constexpr uint32_t kBTileBytes = kTcBN * kTcBK * 4;   // 16 KiB
 constexpr uint32_t kStageBytes = 2 * kATileBytes + 2 * kBTileBytes;
 constexpr uint32_t kTmemCols = 2 * kTcBN;         // two FP32 accumulators of kTcBN columns
 constexpr uint32_t kBarrierBytes = 8 * (2 * kTcStages + 5) + 8;
-constexpr uint32_t kTcSmemBytes = 1024 + kTcStages * kStageBytes + kBarrierBytes;
+constexpr uint32_t kStagingBytes = kTcAccWarps * 32 * 32 * 4;   // 4 KiB per accumulate warp
+constexpr uint32_t kTcSmemBytes =
+    1024 + kTcStages * kStageBytes + kBarrierBytes + 128 + kStagingBytes;
+constexpr uint32_t kMaxSmemPerBlock = 232448;   // 227 KiB, the opt-in limit of one block
+static_assert(kTcSmemBytes <= kMaxSmemPerBlock, "ring, barriers and staging fit one block");
 
 static_assert(kTcBK * 4 == 64, "one K-slice row is one 64-byte swizzle row");
 static_assert(kTcChunk % kTcBK == 0 && kKPad % kTcBK == 0, "chunks are whole slices");
@@ -255,9 +265,10 @@ struct Tc3Params {
   int64_t ldc;
   int tiles_m, tiles_n;
   int slices;            // K-slices per tile
-  int dp_tiles;          // blocks [0, dp_tiles) each process tile blockIdx.x whole
-  int split;             // blocks from dp_tiles on: tail tile halves [0, split), [split, S)
-  int items;             // dp_tiles + 2 x (split tiles): the work list
+  int dp_tiles;          // items [0, dp_tiles) are whole tiles
+  int parts;             // K-parts of each tile from dp_tiles on (1: none split)
+  int chunks;            // ceil(slices / slices per chunk); parts end on chunk bounds
+  int items;             // dp_tiles + parts x (split tiles): the work list
   unsigned int epoch;    // this call's flag value (never 0)
   int vec_store;         // C 16-byte aligned and ldc % 4 == 0
   int64_t wait_limit_ns;
@@ -271,11 +282,12 @@ __device__ __forceinline__ void tc3_tile_coords(int tile, int tiles_n, int &tm, 
 
 // This block's work items (tile, K-slice range): items b, b + stride, ...
 // of the list [whole tiles, split units]; `unit` >= 0 numbers the items that
-// share a split tile (even: lower half, owner; odd: upper half).  The one-block
-// kernel launches one block per item; the pair kernel one pair per resident
-// slot, each pair walking its items in order.  Whole tiles are a multiple of
-// the stride whenever units exist, so all units fall in the last round, each on
-// its own pair and alongside its partner.
+// share a split tile, `parts` consecutive units per tile (part 0, the owner,
+// holds the lowest K-range).  The one-block kernel launches one block per item;
+// the pair kernel one pair per resident slot, each pair walking its items in
+// order.  Whole tiles are a multiple of the stride whenever units exist, so
+// all units fall in the last round, each on its own pair and alongside its
+// partners.
 struct Tc3Work {
   int idx, stride;
   __device__ __forceinline__ void init(const Tc3Params &, int first, int step) {
@@ -295,9 +307,11 @@ struct Tc3Work {
       return true;
     }
     unit = b - p.dp_tiles;
-    tile = p.dp_tiles + unit / 2;
-    kb = (unit & 1) ? p.split : 0;
-    ke = (unit & 1) ? p.slices : p.split;
+    const int part = unit % p.parts;
+    tile = p.dp_tiles + unit / p.parts;
+    constexpr int kSlicesPerChunk = kTcChunk / kTcBK;
+    kb = (part * p.chunks / p.parts) * kSlicesPerChunk;
+    ke = part + 1 == p.parts ? p.slices : ((part + 1) * p.chunks / p.parts) * kSlicesPerChunk;
     return true;
   }
 };
@@ -316,6 +330,91 @@ __device__ __forceinline__ void st_release_u32(unsigned int *p, unsigned int v) 
 }
 static_assert(kTc3FlagsPerBlock == kTcAccWarps, "one flag per accumulate warp");
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float f4_get(const float4 &v, int j) {
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+// Stores one accumulate warp's 32 x 128 block of C -- lane l holds row
+// row_base + l, acc[j] its column col0 + j -- through the warp's 4 KiB staging
+// buffer `stg` in shared memory.  Each 32 x 32 part is written there row by
+// row and read back transposed, so that 8 lanes cover 128 contiguous bytes of
+// one row and one instruction stores 4 whole cache lines (a direct store from
+// the row-per-lane layout touches 32 lines with 16 bytes each).  16-byte
+// chunk q of staged row r sits at position q ^ (r % 8), which keeps both the
+// row-wise writes and the transposed reads free of bank conflicts.
+// adds_next: add the partial sums that C already holds (from the next K-part),
+// loaded kStoreBatch vectors at a time before the first of their stores.
+__device__ __forceinline__ void store_c_block(const Tc3Params &p, const float (&acc)[kTcBN / 2],
+                                              int row_base, int col0, uint32_t stg, int lane,
+                                              bool adds_next) {
+  const int rsub = lane >> 3;   // row within each group of four
+  const int cq = lane & 7;      // 16-byte chunk within the 32 columns
+  constexpr int kStoreBatch = 2;   // groups of four rows loaded and stored together
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    __syncwarp();   // the previous part's transposed reads are done
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      st_shared_v4(stg + uint32_t(lane * 128 + ((q ^ (lane & 7)) << 4)), acc[32 * b + 4 * q],
+                   acc[32 * b + 4 * q + 1], acc[32 * b + 4 * q + 2], acc[32 * b + 4 * q + 3]);
+    __syncwarp();
+    const int col = col0 + 32 * b + 4 * cq;
+    const bool vec = p.vec_store && col + 4 <= p.N;
+#pragma unroll
+    for (int h = 0; h < 8 / kStoreBatch; ++h) {
+      float4 v[kStoreBatch], w[kStoreBatch];
+#pragma unroll
+      for (int u = 0; u < kStoreBatch; ++u) {
+        const int r = 4 * (kStoreBatch * h + u) + rsub;
+        v[u] = ld_shared_v4(stg + uint32_t(r * 128 + ((cq ^ (r & 7)) << 4)));
+        w[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (adds_next && vec) {
+#pragma unroll
+        for (int u = 0; u < kStoreBatch; ++u) {
+          const int row = row_base + 4 * (kStoreBatch * h + u) + rsub;
+          if (row < p.M)
+            w[u] = __ldcg(reinterpret_cast<const float4 *>(p.C + int64_t(row) * p.ldc + col));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kStoreBatch; ++u) {
+        const int row = row_base + 4 * (kStoreBatch * h + u) + rsub;
+        if (row >= p.M) continue;
+        float *c_row = p.C + int64_t(row) * p.ldc;
+        if (vec) {
+          float4 o = v[u];
+          if (adds_next) {
+            o.x = w[u].x + o.x; o.y = w[u].y + o.y; o.z = w[u].z + o.z; o.w = w[u].w + o.w;
+          }
+          *reinterpret_cast<float4 *>(c_row + col) = o;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (col + j < p.N) {
+              float o = f4_get(v[u], j);
+              if (adds_next) o = __ldcg(c_row + col + j) + o;
+              c_row[col + j] = o;
+            }
+        }
+      }
+    }
+  }
+}
+
 // 320 threads: with 3 warps on some SM sub-partitions (16K registers each),
 // at most 168 registers per thread.
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -332,6 +431,7 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
   const uint32_t bar_tempty = bar_tfull + 16;              // accumulator b drained
   const uint32_t bar_drain = bar_tempty + 16;              // every product issued has completed
   const uint32_t tmem_slot = bar_drain + 8;
+  const uint32_t staging = (tmem_slot + 8 + 127u) & ~127u;  // kTcAccWarps x 4 KiB
   volatile uint32_t *tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t *>(smem_raw + (tmem_slot - raw));
 
@@ -482,10 +582,9 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
       if (timed_out) break;
       int tm, tn;
       tc3_tile_coords(tile, p.tiles_n, tm, tn);
-      const int row = tm * kTcBM + 32 * quarter + lane;
       const int col0 = tn * kTcBN + half * (kTcBN / 2);
-      const bool owner_of_split = kb == 0 && ke < p.slices;   // slices [ke, S): unit + 1
-      if (owner_of_split) {
+      const bool adds_next = ke < p.slices;   // slices [ke, S) are unit + 1's, summed in C
+      if (adds_next) {
         if (lane == 0) {
           const unsigned int *f = &flags[(unit + 1) * kTc3FlagsPerBlock + acc_warp];
           const uint64_t t0 = timer_ns();
@@ -499,29 +598,8 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
         }
         __syncwarp();
       }
-      if (row < p.M) {
-        float *c_row = p.C + int64_t(row) * p.ldc;
-#pragma unroll
-        for (int c = 0; c < kTcBN / 2; c += 4) {
-          const int col = col0 + c;
-          if (p.vec_store && col + 4 <= p.N) {
-            float4 v = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-            if (owner_of_split) {
-              const float4 w = __ldcg(reinterpret_cast<const float4 *>(c_row + col));
-              v.x = w.x + v.x; v.y = w.y + v.y; v.z = w.z + v.z; v.w = w.w + v.w;
-            }
-            *reinterpret_cast<float4 *>(c_row + col) = v;
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (col + j < p.N) {
-                float v = acc[c + j];
-                if (owner_of_split) v = __ldcg(c_row + col + j) + v;
-                c_row[col + j] = v;
-              }
-          }
-        }
-      }
+      store_c_block(p, acc, tm * kTcBM + 32 * quarter, col0,
+                    staging + uint32_t(acc_warp) * 4096u, lane, adds_next);
       if (kb > 0) {
         // Slices [kb, S) of a split tile: this warp's partial sums are in C.
         __syncwarp();
@@ -584,7 +662,9 @@ constexpr int kT2Stages = 6;
 constexpr uint32_t kT2TileBytes = kT2Rows * kTcBK * 4;    // 8 KiB
 constexpr uint32_t kT2StageBytes = 4 * kT2TileBytes;      // A hi, A lo, B^T hi, B^T lo
 constexpr uint32_t kT2BarrierBytes = 8 * (2 * kT2Stages + 5) + 8;
-constexpr uint32_t kT2SmemBytes = 1024 + kT2Stages * kT2StageBytes + kT2BarrierBytes;
+constexpr uint32_t kT2SmemBytes =
+    1024 + kT2Stages * kT2StageBytes + kT2BarrierBytes + 128 + kStagingBytes;
+static_assert(kT2SmemBytes <= kMaxSmemPerBlock, "ring, barriers and staging fit one block");
 static_assert(kT2StageBytes % 1024 == 0 && kT2TileBytes % 1024 == 0, "tiles stay 1024-byte aligned");
 static_assert(kT2BN == kTcBN, "each block's accumulator keeps the one-block layout");
 
@@ -672,6 +752,7 @@ gemm_tc3_pair_kernel(const __grid_constant__ CUtensorMap map_ahi,
   const uint32_t bar_tempty = bar_tfull + 16;              // used in the leader
   const uint32_t bar_drain = bar_tempty + 16;              // used in the leader
   const uint32_t tmem_slot = bar_drain + 8;
+  const uint32_t staging = (tmem_slot + 8 + 127u) & ~127u;  // kTcAccWarps x 4 KiB
   volatile uint32_t *tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t *>(smem_raw + (tmem_slot - raw));
 
@@ -833,11 +914,10 @@ gemm_tc3_pair_kernel(const __grid_constant__ CUtensorMap map_ahi,
       if (timed_out) break;
       int tm, tn;
       tc3_tile_coords(tile, p.tiles_n, tm, tn);
-      const int row = tm * kT2BM + int(rank) * kT2Rows + 32 * quarter + lane;
       const int col0 = tn * kT2BN + half * (kT2BN / 2);
       const int flag = int(rank) * kTcAccWarps + acc_warp;   // per block of the pair and warp
-      const bool owner_of_split = kb == 0 && ke < p.slices;
-      if (owner_of_split) {
+      const bool adds_next = ke < p.slices;   // slices [ke, S) are unit + 1's, summed in C
+      if (adds_next) {
         if (lane == 0) {
           const unsigned int *f = &flags[(unit + 1) * 2 * kTcAccWarps + flag];
           const uint64_t t0 = timer_ns();
@@ -851,29 +931,8 @@ gemm_tc3_pair_kernel(const __grid_constant__ CUtensorMap map_ahi,
         }
         __syncwarp();
       }
-      if (row < p.M) {
-        float *c_row = p.C + int64_t(row) * p.ldc;
-#pragma unroll
-        for (int c = 0; c < kT2BN / 2; c += 4) {
-          const int col = col0 + c;
-          if (p.vec_store && col + 4 <= p.N) {
-            float4 v = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-            if (owner_of_split) {
-              const float4 w = __ldcg(reinterpret_cast<const float4 *>(c_row + col));
-              v.x = w.x + v.x; v.y = w.y + v.y; v.z = w.z + v.z; v.w = w.w + v.w;
-            }
-            *reinterpret_cast<float4 *>(c_row + col) = v;
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (col + j < p.N) {
-                float v = acc[c + j];
-                if (owner_of_split) v = __ldcg(c_row + col + j) + v;
-                c_row[col + j] = v;
-              }
-          }
-        }
-      }
+      store_c_block(p, acc, tm * kT2BM + int(rank) * kT2Rows + 32 * quarter, col0,
+                    staging + uint32_t(acc_warp) * 4096u, lane, adds_next);
       if (kb > 0) {
         __syncwarp();
         if (lane == 0 && unit != p.drop_signal_block) {
@@ -940,16 +999,33 @@ std::atomic<unsigned int> g_tc3_epoch{0};
 std::atomic<int> g_tc3_drop_signal_block{-1};
 
 // Work split shared by both kernels: whole tiles, and when the last wave is at
-// most half full, its tiles in two K halves (units 2t, 2t + 1).
-void plan_tiles(Tc3Params &prm, int64_t tiles, int64_t slots, int max_units, int slices) {
+// most half full, its tiles in two K-parts; with at most half as many tiles as
+// slots, every tile in up to kTc3MaxParts K-parts of at least two chunks each,
+// one slot each (measured: each hand-over of a running sum costs about half a
+// chunk's products, so one-chunk parts lose more than they gain).
+constexpr int kTc3MaxParts = 4;
+// Returns the item count (the caller rejects one past the int range).
+int64_t plan_tiles(Tc3Params &prm, int64_t tiles, int64_t slots, int max_units, int slices) {
   constexpr int kSlicesPerChunk = kTcChunk / kTcBK;
+  const int64_t chunks = (slices + kSlicesPerChunk - 1) / kSlicesPerChunk;
   const int64_t rem = slots > 0 ? tiles % slots : 0;
-  const bool split_tail = tiles > slots && rem > 0 && 2 * rem <= slots &&
-                          2 * rem <= max_units && slices >= 2 * kSlicesPerChunk;
   prm.slices = slices;
-  prm.split = std::max(kSlicesPerChunk, (slices / 2) / kSlicesPerChunk * kSlicesPerChunk);
-  prm.dp_tiles = int(split_tail ? tiles - rem : tiles);
-  prm.items = int(prm.dp_tiles + 2 * (tiles - prm.dp_tiles));
+  prm.chunks = int(chunks);
+  prm.parts = 1;
+  prm.dp_tiles = int(tiles);
+  if (tiles > slots && rem > 0 && 2 * rem <= slots && 2 * rem <= max_units && chunks >= 2) {
+    prm.parts = 2;
+    prm.dp_tiles = int(tiles - rem);
+  } else if (tiles > 0 && 2 * tiles <= slots && chunks >= 4) {
+    int64_t parts = std::min<int64_t>({slots / tiles, chunks / 2, int64_t(kTc3MaxParts)});
+    if (parts * tiles <= max_units) {
+      prm.parts = int(parts);
+      prm.dp_tiles = 0;
+    }
+  }
+  const int64_t items = prm.dp_tiles + prm.parts * (tiles - prm.dp_tiles);
+  prm.items = int(items);
+  return items;
 }
 
 unsigned int next_epoch() {
@@ -1004,13 +1080,12 @@ cudaError_t launch_tc3_pairs(const GemmProblem &p, const DeviceInfo &dev, int64_
   prm.tiles_m = int(tiles_m);
   prm.tiles_n = int(tiles_n);
   // Split units use flags per (unit, block of the pair, warp): half as many units fit.
-  plan_tiles(prm, tiles, slots, kTc3MaxBlocks / 2, int(Kp / kTcBK));
+  const int64_t items = plan_tiles(prm, tiles, slots, kTc3MaxBlocks / 2, int(Kp / kTcBK));
+  if (tiles > 0x7fffffff || items > 0x7fffffff) return cudaErrorInvalidConfiguration;
   prm.vec_store = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0) ? 1 : 0;
   prm.wait_limit_ns = g_tc3_wait_limit_ns.load(std::memory_order_relaxed);
   prm.drop_signal_block = g_tc3_drop_signal_block.load(std::memory_order_relaxed);
   prm.epoch = next_epoch();
-  const int64_t items = prm.dp_tiles + 2 * (tiles - prm.dp_tiles);
-  if (items > 0x7fffffff) return cudaErrorInvalidConfiguration;
   // Persistent: one pair per resident slot, each walking its items; the next
   // tile's copies and products start while the previous tile is being stored.
   cfg.gridDim = dim3(unsigned(2 * std::min<int64_t>(items, slots)), 1, 1);
@@ -1124,13 +1199,12 @@ cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *worksp
   prm.ldc = p.ldc;
   prm.tiles_m = int(tiles_m);
   prm.tiles_n = int(tiles_n);
-  plan_tiles(prm, tiles, slots, kTc3MaxBlocks, int(Kp / kTcBK));
+  const int64_t grid = plan_tiles(prm, tiles, slots, kTc3MaxBlocks, int(Kp / kTcBK));   // one block per item
+  if (tiles > 0x7fffffff || grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   prm.vec_store = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0) ? 1 : 0;
   prm.wait_limit_ns = g_tc3_wait_limit_ns.load(std::memory_order_relaxed);
   prm.drop_signal_block = g_tc3_drop_signal_block.load(std::memory_order_relaxed);
   prm.epoch = next_epoch();
-  const int64_t grid = prm.dp_tiles + 2 * (tiles - prm.dp_tiles);   // one block per item
-  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
 
   gemm_tc3_kernel<<<unsigned(grid), kTcThreads, kTcSmemBytes, stream>>>(maps[0], maps[1],
                                                                        maps[2], maps[3], prm);
