@@ -87,9 +87,11 @@ typedef struct CUstream_st *tmm_stream_t;
  *
  * When the tile count leaves the last wave of blocks partly empty, the call
  * runs persistent and cooperative (one block per resident slot) and splits
- * the K range of the last tiles between pairs of blocks; the pair meets
- * through a flag in library-owned device memory, with a bounded wait (see
- * tmm_check_device).  Up to 16 such calls may be in flight at once (for
+ * the K range of the last tiles between pairs of blocks; with fewer tiles
+ * than resident blocks, the K range of every tile is split over up to about
+ * five consecutive blocks, each adding the next block's running sum.  Blocks
+ * meet through flags in library-owned device memory, with a bounded wait
+ * (see tmm_check_device).  Up to 16 such calls may be in flight at once (for
  * example on different streams); results are deterministic either way.
  */
 int gemm_f32(int64_t M, int64_t N, int64_t K,
@@ -143,7 +145,11 @@ int gemm_f32_naive(int64_t M, int64_t N, int64_t K,
  * only its lo is written to the workspace.  The pages do not go beyond FP32 FMA units ("CMU
  * DLSys Lecture 12" section 6 notes that tensor instructions change the
  * implementation); the tiling is that of section 5 with the register tile
- * replaced by a tensor-memory accumulator.  Same contract as gemm_f32, plus:
+ * replaced by a tensor-memory accumulator.  The tiles of a partial last wave,
+ * and every tile of a problem with few tiles, are split along K into parts
+ * that add each other's partial sums in a fixed order (bounded waits, see
+ * tmm_check_device), so results are deterministic.  Same contract as
+ * gemm_f32, plus:
  *   workspace        DEVICE pointer, 256-byte aligned, caller-owned, at least
  *                    gemm_f32_tc3_workspace_size(M, N, K) bytes; holds the
  *                    split operands (its contents are scratch, not preserved);
@@ -209,7 +215,7 @@ int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K,
 /*
  * tmm_check_device -- synchronise `stream`, then read and clear the current
  * device's status words.  Returns TMM_OK, or TMM_ERR_DEVICE_TIMEOUT when a
- * bounded wait inside gemm_f32 (between the two blocks sharing a split tile),
+ * bounded wait inside gemm_f32 (between the blocks sharing a split tile),
  * gemm_f32_tc3 (between the copy, tensor-core and epilogue roles of a block
  * or block pair) or window_sum_f32 (for a tile's bulk copy) ran out of time
  * since the last check; results written since then are not valid.  The pages have no counterpart: this is the library's failure
