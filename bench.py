@@ -421,6 +421,13 @@ def run_ours(args, world, rank, local):
                "serial_ms_per_step": serial_ms,
                "serial_value": serial_flops / (serial_ms / 1e3) / 1e12}
 
+    # The same steps with L2 left warm (no flush), after the timed region.
+    warm_times = time_device(step, lambda: None, max(3, min(args.steps, 50)), args.warmup,
+                             stream, dist)
+    warm_ms, warm_flops = reduce_over_ranks(dist, statistics.mean(warm_times), float(w.flops))
+    warm = {"value": warm_flops / (warm_ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": warm_ms,
+            "steps": len(warm_times), "l2": "not flushed between steps"}
+
     # Roofline of the one kernel a step launches.
     peaks = measured_peaks()
     peak, peak_src = ffma_peak_tflops(props.multi_processor_count, peaks)
@@ -461,6 +468,8 @@ def run_ours(args, world, rank, local):
             "e2e": e2e,
             "gpu_launches": timed_launches,
             "ms_per_step_min": min(times), "ms_per_step_max": max(times),
+            "ms_per_step_median": statistics.median(times),
+            "warm_l2": warm,
         }
         line.update(extra)
         print(json.dumps(line), flush=True)

@@ -39,6 +39,8 @@ def test_contract_keys(line):
     assert line["steps"] == 5 and line["warmup"] == 3
     assert line["config"]["workload"].startswith("square4096")
     assert line["gpu_launches"] == line["steps"]
+    assert line["warm_l2"]["unit"] == "TFLOP/s" and line["warm_l2"]["value"] > 0
+    assert line["ms_per_step_min"] <= line["ms_per_step_median"] <= line["ms_per_step_max"]
 
 
 def test_value_matches_time_and_roofline(line):
