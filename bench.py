@@ -168,7 +168,7 @@ def ffma_peak_tflops(sm_count: int, peaks: dict) -> tuple[float, str]:
 
 KERNEL_SOURCES = {"gemm_simt": ["gemm_simt.cu"], "gemm_tc3": ["gemm_tc3.cu"],
                   "window_sum": ["window_sum.cu"], "sum_partials": ["reduce_softmax.cu"],
-                  "softmax_staged": ["reduce_softmax.cu"]}
+                  "softmax_staged": ["reduce_softmax.cu"], "softmax_grid": ["reduce_softmax.cu"]}
 
 
 def recorded_traffic(kernel: str, workload: str, units: int | None = None):
@@ -592,6 +592,7 @@ def window_leg(args, flush, stream, peaks) -> dict:
 
 
 SOFTMAX_COLS = 4096
+GRID_ROW_COLS = 98304   # rows this long or longer run softmax_grid_kernel
 
 
 def _hbm_roofline(gbs, peaks, nbytes, what, traffic=None):
@@ -604,7 +605,7 @@ def _hbm_roofline(gbs, peaks, nbytes, what, traffic=None):
 
 
 def reduction_legs(args, flush, stream, peaks) -> dict:
-    """sum_f32 over 2^28 floats and softmax_rows_f32 over 65536 rows of 4096 logits
+    """sum_f32 over 2^28 floats and softmax_rows_f32 over 65536 rows of 4096 logits (by default)
     ("Tiling Strategies" section 5): HBM-bound, each input read once."""
     import torch
     from tiled_matrix_multiply_gb300 import _abi
@@ -634,8 +635,8 @@ def reduction_legs(args, flush, stream, peaks) -> dict:
     del x, ws, res
     torch.cuda.empty_cache()
 
-    cols = SOFTMAX_COLS
-    rows = (1 << args.aux_log2n) // cols
+    cols = args.softmax_cols
+    rows = max(1, (1 << args.aux_log2n) // cols)
     xs = torch.randn(rows, cols, device="cuda", generator=g) * 4
     ys = torch.empty_like(xs)
 
@@ -651,7 +652,8 @@ def reduction_legs(args, flush, stream, peaks) -> dict:
                       "rows_per_s": rows / (ms / 1e3),
                       "roofline": _hbm_roofline(
                           gbs, peaks, nbytes, "4 rows cols read + 4 rows cols written",
-                          recorded_traffic("softmax_staged", f"cols{cols}", rows * cols))}
+                          recorded_traffic("softmax_grid" if cols >= GRID_ROW_COLS
+                                           else "softmax_staged", f"cols{cols}", rows * cols))}
     return out
 
 
@@ -687,6 +689,8 @@ def main(argv=None):
     ap.add_argument("--aux-log2n", type=int, default=AUX_LOG2N,
                     help="log2 of the floats each window/sum/softmax call moves (default 28; "
                          "smaller for profiler captures)")
+    ap.add_argument("--softmax-cols", type=int, default=SOFTMAX_COLS,
+                    help="row length of the softmax leg (default 4096)")
     ap.add_argument("--no-layouts", action="store_true",
                     help="skip the transposed-layout (gemm_f32_ex, gemm_f32_tc3_ex) leg")
     args = ap.parse_args(argv)

@@ -12,7 +12,10 @@ Tolerances follow from the arithmetic the header states:
     by their shares Y_k), 1/s and the product one each, so to first order
     |y_j - Y_j| <= (|t_j| + 4 + sum_k Y_k (|t_k| + 4) + ceil(cols/32) + 18) 2^-24 Y_j
                    + 2^-146
-    (the last term for results in the subnormal range).
+    (the last term for results in the subnormal range).  Rows of 98304 columns
+    or more keep running sums: each rise of a thread's maximum costs one expf
+    and one product (at most cols / (4 * 512 * G) of them per thread, G >= 3
+    blocks per row), well inside the ceil(cols/32) additions allowed.
 """
 import math
 
@@ -171,7 +174,8 @@ def test_softmax_contiguous(cols):
     check_softmax(logits(rows_for(cols), cols, 120 + cols % 1000))
 
 
-@pytest.mark.parametrize("cols", [3, 17, 33, 1000, 1025, 4096, 8193, 49152, 65536, 262147])
+@pytest.mark.parametrize("cols", [3, 17, 33, 1000, 1025, 4096, 8193, 49152, 65536, 262147,
+                                  400003, 1048576])
 def test_softmax_strided_and_unaligned(cols):
     x = logits(min(37, rows_for(cols)), cols, 121)
     check_softmax(x, ldx=cols + 3, ldy=cols + 5)      # row starts off 16-byte boundaries
@@ -179,7 +183,7 @@ def test_softmax_strided_and_unaligned(cols):
     check_softmax(x, ldx=cols + 8, ldy=cols + 12)     # padded, aligned rows
 
 
-@pytest.mark.parametrize("cols", [100, 1024, 4096, 30000, 70000])
+@pytest.mark.parametrize("cols", [100, 1024, 4096, 30000, 70000, 600000])
 def test_softmax_in_place(cols):
     x = logits(min(21, rows_for(cols)), cols, 122)
     y = gpu_softmax(x, ldx=cols + 4, in_place=True)
@@ -187,7 +191,7 @@ def test_softmax_in_place(cols):
     assert np.all(np.abs(y - want) <= softmax_tolerance(x, want))
 
 
-@pytest.mark.parametrize("cols", [7, 700, 7000, 70000])
+@pytest.mark.parametrize("cols", [7, 700, 7000, 70000, 500000])
 def test_softmax_special_rows(cols):
     x = logits(6, cols, 123)
     x[0, :] = 2.5                       # constant row: 1 / cols everywhere
@@ -199,6 +203,23 @@ def test_softmax_special_rows(cols):
     y, want = check_softmax(x)
     assert np.all(y[2, ::3] == 0.0)
     assert np.all(np.abs(y[0] - 1.0 / cols) <= (math.ceil(cols / 32) + 40) * 2.0 ** -24 / cols)
+
+
+@pytest.mark.parametrize("cols", [4096, 200000, 1000000])
+def test_softmax_monotone_rows(cols):
+    # Ascending rows raise the running maximum at every step (the most rescales
+    # of a running sum); descending rows never do.
+    base = np.linspace(-30.0, 30.0, cols, dtype=np.float32)
+    x = np.stack([base, base[::-1].copy(), np.sort(logits(1, cols, 126)[0])])
+    check_softmax(x)
+
+
+@pytest.mark.parametrize("cols,pad", [(4194304, 0), (4000037, 1)])
+def test_softmax_very_long_rows(cols, pad):
+    # 128 (123) blocks of the cooperative grid per row, at most 3 rows in
+    # flight at once; pad = 1 takes the scalar (unaligned) form.
+    x = logits(2, cols, 128)
+    check_softmax(x, ldx=cols + pad, ldy=cols + pad)
 
 
 def test_softmax_rows_sum_to_one_at_full_size():
@@ -237,3 +258,29 @@ def test_python_wrappers():
     assert torch.equal(tmm.softmax_rows_f32(m), torch.full((2, 2), 0.5, device="cuda"))
     tmm.softmax_rows_f32(m, m)
     assert torch.equal(m, torch.full((2, 2), 0.5, device="cuda"))
+
+
+@pytest.mark.parametrize("rows,cols", [(64, 98304), (64, 300000), (4, 4194304)])
+def test_softmax_grid_wait_timeout_is_reported_and_recovers(rows, cols):
+    # Rows of 98304 columns or more are shared by several blocks that meet
+    # through a counter in global memory (3 blocks per row; 10; 128).  Block 1
+    # never counts itself in, so the other blocks of its row run into the
+    # (2 ms) limit.
+    lib = _abi.load()
+    stream = _stream()
+    x = logits(rows, cols, 127)
+    assert lib.tmm_check_device(stream) == _abi.TMM_OK
+    try:
+        assert lib.tmm_testing_set_wait_hooks(1, 2_000_000) == _abi.TMM_OK
+        xd = torch.from_numpy(x).cuda()
+        yd = torch.empty_like(xd)
+        assert lib.softmax_rows_f32(rows, cols, xd.data_ptr(), cols, yd.data_ptr(), cols,
+                                    stream) == _abi.TMM_OK
+        rc = lib.tmm_check_device(stream)
+        assert rc == _abi.TMM_ERR_DEVICE_TIMEOUT, rc
+        assert "softmax_rows_f32" in _abi.last_error()
+    finally:
+        lib.tmm_testing_set_wait_hooks(-1, 0)
+    assert lib.tmm_check_device(stream) == _abi.TMM_OK
+    check_softmax(x)
+    assert lib.tmm_check_device(stream) == _abi.TMM_OK

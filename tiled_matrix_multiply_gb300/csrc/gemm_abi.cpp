@@ -183,17 +183,19 @@ int tmm_check_device(tmm_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return fail(TMM_ERR_CUDA, "tmm_check_device: cudaStreamSynchronize: %s", cudaGetErrorString(e));
-  unsigned int simt = 0, tc3 = 0, win = 0;
+  unsigned int simt = 0, tc3 = 0, win = 0, sm = 0;
   e = tmm::simt_device_status(&simt, true);
   if (e == cudaSuccess) e = tmm::tc3_device_status(&tc3, true);
   if (e == cudaSuccess) e = tmm::window_device_status(&win, true);
+  if (e == cudaSuccess) e = tmm::softmax_device_status(&sm, true);
   if (e != cudaSuccess)
     return fail(TMM_ERR_CUDA, "tmm_check_device: status read: %s", cudaGetErrorString(e));
-  if (simt | tc3 | win)
+  if (simt | tc3 | win | sm)
     return fail(TMM_ERR_DEVICE_TIMEOUT,
                 "tmm_check_device: a bounded wait inside %s ran out of time; the affected "
                 "results are not valid",
-                simt ? "gemm_f32" : (tc3 ? "gemm_f32_tc3" : "window_sum_f32"));
+                simt ? "gemm_f32"
+                     : (tc3 ? "gemm_f32_tc3" : (win ? "window_sum_f32" : "softmax_rows_f32")));
   return TMM_OK;
 }
 
@@ -201,6 +203,7 @@ int tmm_testing_set_wait_hooks(int drop_signal_block, int64_t wait_limit_ns) {
   tmm::simt_set_test_hooks(drop_signal_block, wait_limit_ns);
   tmm::tc3_set_test_hooks(drop_signal_block, wait_limit_ns);
   tmm::window_set_test_hooks(drop_signal_block, wait_limit_ns);
+  tmm::softmax_set_test_hooks(drop_signal_block, wait_limit_ns);
   return TMM_OK;
 }
 

@@ -22,8 +22,9 @@
 //   to the result (P >= 2^18 whenever the grid is capped).
 //
 // Row softmax (softmax_rows_f32): y_{r,j} = e^{x_{r,j} - m_r} / sum_k e^{x_{r,k} - m_r}
-// with m_r the row maximum.  Each row is read from HBM once and written once;
-// what holds it on chip between the two passes depends on its length:
+// with m_r the row maximum.  Rows of up to 98303 columns are read from HBM once
+// and written once; what holds them on chip between the two passes depends on
+// their length:
 //   * up to 2048 columns (rows on 16-byte boundaries, cols % 4 == 0; 1024
 //     otherwise): a group of 1-32 lanes per row, the row in registers (lane s
 //     holds columns or 16-byte vectors s, s + group, ...); group shuffles
@@ -33,16 +34,19 @@
 //     flight while this one is reduced; pass 1 takes the maximum, pass 2
 //     replaces each staged value by e^{x - m} and sums them, and the stores
 //     scale by 1 / s.
-//   * up to 8 x 49152 columns: a cluster of 2-8 blocks per row, each staging
-//     one chunk, the partial maxima and sums combined through distributed
-//     shared memory (softmax_staged_kernel describes the exchange).
-//   * longer rows: one block of 1024 threads per row, three passes over
-//     global memory (max, sum, normalise); the second and third reads of a row
-//     come from L2 when the rows in flight fit there.
+//   * up to 98303 columns: a cluster of 2-8 blocks per row, each staging one
+//     chunk, the partial maxima and sums combined through distributed shared
+//     memory (softmax_staged_kernel describes the exchange).
+//   * longer rows: G blocks per row of a cooperative grid, meeting through
+//     global memory; each reads its columns twice, a running (maximum, sum)
+//     pass and the normalise pass, whose reads come from L2 because the rows
+//     in flight are sized to fit there (softmax_grid_kernel).
 // Arithmetic: t = fl(x - m), e = expf(t) (CUDA's, within 2 ulp), s summed in
 // FP32 in a fixed order (each thread in ascending column order, then a shuffle
 // tree, then the cluster's chunks in rank order), y = e * fl(1 / s) (in a
-// cluster, e^{x - m_c} * fl(e^{m_c - m} / s)).
+// cluster, e^{x - m_c} * fl(e^{m_c - m} / s)).  Past 98303 columns the sum is
+// a running one (each rise of a thread's maximum rescales its sum, one more
+// product and one more expf), and the G parts merge in a fixed order.
 // y may be x itself (in place): every row (chunk) is read completely before
 // any of its outputs is written, and only coherent loads are used.
 #include <atomic>
@@ -259,6 +263,101 @@ softmax_warp_vec_kernel(int64_t rows, int cols, const float *x, int64_t ldx, flo
   }
 }
 
+// Rows shared by G blocks that meet through global memory (softmax_grid_kernel).
+constexpr int kGridThreads = 512;
+constexpr int kGridChunk = 32768;          // columns per block, at most (a multiple of 4)
+constexpr int kGridMaxBlocks = 2048;       // blocks of one launch, at most
+constexpr int kGridKeep = 4;               // vectors per thread kept in shared memory
+constexpr int kGridRegions = 16;           // calls in flight at once, at most
+__device__ unsigned int g_sm_counters[kGridRegions][2 * kGridMaxBlocks];
+__device__ float2 g_sm_pairs[kGridRegions][2 * kGridMaxBlocks];
+__device__ unsigned int g_softmax_status;
+
+// How the G blocks sharing a row meet: block b takes part b % G of row unit
+// b / G; U units are in flight.  Slot (it % 2) U + unit of a call's region
+// holds a counter and G (maximum, sum) pairs.
+struct RowExchange {
+  int G, U;                  // blocks per row, rows in flight
+  unsigned int *counters;    // 2 U row slots of this call's region, zeroed before launch
+  float2 *pairs;             // 2 U x G partial (maximum, sum) pairs
+  int64_t wait_limit_ns;
+  int drop_block;            // testing hook: this block never counts itself in (-1: none)
+};
+
+struct GridRowsParams {
+  int64_t rows;
+  int cols, chunk;
+  const float *x;
+  int64_t ldx;
+  float *y;
+  int64_t ldy;
+  RowExchange ex;
+};
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// The row's (m, s) from the pairs of the G blocks sharing it, for iteration
+// `it` of row unit `unit`; (m, s) is this block's pair (needed in thread 0
+// only).  Thread 0 stores the pair in the row's slot, counts the block in
+// (fence, then an atomic increment) and waits (bounded) until all G blocks
+// have; the first warp then merges the G pairs -- lane l takes parts l,
+// l + 32, ... in order, then a fixed shuffle tree -- so every block of the row
+// gets the same result.  Slots alternate between two sets by iteration
+// parity, and a slot's counter grows by G per use: a block stores into a slot
+// again only after the following row's wait, which every block of its row
+// passes only after reading the slot.  On timeout thread 0 records bit 0 of
+// g_softmax_status and stops waiting (the results are then not valid).  All
+// threads must call; one barrier; *row_pair is rewritten by the next call, so
+// the block must pass another barrier in between.
+__device__ __forceinline__ float2 exchange_row_pair(const RowExchange &ex, int unit, int part,
+                                                    int it, float m, float s, bool &timed_out,
+                                                    float2 *row_pair) {
+  const int t = threadIdx.x, lane = t & 31;
+  if (t < 32) {
+    const int slot = (it & 1) * ex.U + unit;
+    float2 *pairs = ex.pairs + int64_t(slot) * ex.G;
+    if (t == 0) {
+      pairs[part] = make_float2(m, s);
+      if (int(blockIdx.x) != ex.drop_block) {
+        __threadfence();
+        atomicAdd(&ex.counters[slot], 1u);
+      }
+      const unsigned int target = unsigned(ex.G) * unsigned(it / 2 + 1);
+      const uint64_t t0 = globaltimer_ns();
+      while (!timed_out && ld_acquire_gpu(&ex.counters[slot]) < target) {
+        if (int64_t(globaltimer_ns() - t0) > ex.wait_limit_ns) {
+          atomicOr(&g_softmax_status, 1u);
+          timed_out = true;
+        }
+        __nanosleep(64);
+      }
+    }
+    __syncwarp();
+    float mm = -INFINITY;
+    for (int k = lane; k < ex.G; k += 32) mm = fmaxf(mm, __ldcg(&pairs[k].x));
+    mm = warp_max(mm);
+    float ss = 0.0f;
+    for (int k = lane; k < ex.G; k += 32) {
+      const float2 q = __ldcg(&pairs[k]);
+      if (q.y != 0.0f) ss += q.y * expf(q.x - mm);
+    }
+    ss = warp_sum(ss);
+    if (t == 0) *row_pair = make_float2(mm, ss);
+  }
+  __syncthreads();
+  return *row_pair;
+}
+
 // Rows staged in shared memory, one row per block, or per cluster of C blocks
 // (kCluster) for rows longer than one block should hold.
 //
@@ -378,28 +477,165 @@ softmax_staged_kernel(int64_t rows, int cols, int chunk, const float *x, int64_t
   if (kCluster) cg::this_cluster().sync();
 }
 
-constexpr int kLongRowThreads = 1024;
-
-// Rows too long to stage: three passes over global memory.
-__global__ void __launch_bounds__(kLongRowThreads)
-softmax_long_kernel(int64_t rows, int cols, const float *x, int64_t ldx, float *y,
-                    int64_t ldy) {
-  __shared__ float scratch[32];
-  const int t = threadIdx.x;
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const float *xr = x + r * ldx;
-    float *yr = y + r * ldy;
-    float m = -INFINITY;
-    for (int j = t; j < cols; j += kLongRowThreads) m = fmaxf(m, xr[j]);
-    m = block_reduce<true>(m, scratch);
-    float s = 0.0f;
-    for (int j = t; j < cols; j += kLongRowThreads) s += expf(xr[j] - m);
-    s = block_reduce<false>(s, scratch);
-    const float inv = 1.0f / s;
-    // Same thread, same columns, same order as the sum: every x_j is read
-    // before this thread writes y_j, so y may be x.
-    for (int j = t; j < cols; j += kLongRowThreads) yr[j] = expf(xr[j] - m) * inv;
+// Running (maximum, sum) of one thread's terms: s = sum e^{x - m}.  When the
+// maximum rises to m', s is first scaled by e^{m - m'}; while m is -inf every
+// term is e^{-inf} = 0 (reference 0), so s stays 0.
+__device__ __forceinline__ void online_add(float &m, float &s, float mx, const float *v, int n) {
+  if (mx > m) {
+    s = s != 0.0f ? s * expf(m - mx) : s;
+    m = mx;
   }
+  const float ref = m == -INFINITY ? 0.0f : m;
+  for (int i = 0; i < n; ++i) s += expf(v[i] - ref);
+}
+
+// (m, s) <- the pair for the union of two sets of terms: m = max, s = sum of
+// s_i e^{m_i - m}.  Symmetric bit for bit (IEEE addition commutes), so both
+// lanes of a shuffle exchange hold the same result.
+__device__ __forceinline__ void online_merge(float &m, float &s, float m2, float s2) {
+  const float mm = fmaxf(m, m2);
+  float r = s != 0.0f ? s * expf(m - mm) : 0.0f;
+  if (s2 != 0.0f) r += s2 * expf(m2 - mm);
+  m = mm;
+  s = r;
+}
+
+// Long rows: a cooperative grid of resident blocks, G blocks per row (block b
+// takes part b % G of row unit b / G), U = grid / G rows in flight, so that
+// the rows in flight -- about grid x kGridChunk floats -- fit in L2.  Pass 1
+// reads the block's columns once, each thread keeping a running (m, s)
+// (online_add: at most one rescale per four columns), and the block's threads
+// merge theirs (shuffle tree, then the warps' pairs in order); the G blocks
+// of the row then meet (exchange_row_pair).  Pass 2 re-reads the block's
+// columns -- mostly from L2 -- and writes y.  (Measured against staging the
+// chunks in shared memory with one double-buffered block per SM, meeting the
+// same way: 131072 columns 4950 against 3486 GB/s; several blocks per SM keep
+// more loads in flight than one staging block does.)
+template <bool kVec>
+__global__ void __launch_bounds__(kGridThreads)
+softmax_grid_kernel(const GridRowsParams p) {
+  constexpr int T = kGridThreads;
+  extern __shared__ __align__(16) float4 keep[];   // kGridKeep x T vectors (kVec only)
+  __shared__ float2 scratch[32];
+  __shared__ float2 row_pair;
+  const int b = blockIdx.x;
+  const int u = b / p.ex.G, part = b - u * p.ex.G;
+  if (u >= p.ex.U) return;
+  const int c0 = part * p.chunk;
+  const int len = max(0, min(p.cols - c0, p.chunk));
+  const int nv = kVec ? len >> 2 : 0;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  bool timed_out = false;   // thread 0: once a wait has run out, later ones are skipped
+  int it = 0;
+  for (int64_t r = u; r < p.rows; r += p.ex.U, ++it) {
+    const float *xr = p.x + r * p.ldx + c0;
+    float m = -INFINITY, s = 0.0f;
+    // This thread's vectors are t + i T, i < n; the first kGridKeep of them
+    // are kept in shared memory for pass 2 (keep[i T + t]).
+    const int n = nv > t ? (nv - 1 - t) / T + 1 : 0;
+    if (kVec) {
+      const float4 *xv = reinterpret_cast<const float4 *>(xr);
+      int i = 0;
+      for (; i + 3 < n; i += 4) {
+        float4 a[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) a[k] = xv[t + (i + k) * T];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (i + k < kGridKeep) keep[(i + k) * T + t] = a[k];
+          const float v[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+          online_add(m, s, fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), v, 4);
+        }
+      }
+      for (; i < n; ++i) {
+        const float4 a = xv[t + i * T];
+        if (i < kGridKeep) keep[i * T + t] = a;
+        const float v[4] = {a.x, a.y, a.z, a.w};
+        online_add(m, s, fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), v, 4);
+      }
+    }
+    {
+      int j = 4 * nv + t;
+      for (; j + 3 * T < len; j += 4 * T) {
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = xr[j + k * T];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) online_add(m, s, v[k], &v[k], 1);
+      }
+      for (; j < len; j += T) {
+        const float v = xr[j];
+        online_add(m, s, v, &v, 1);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      online_merge(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+    if (lane == 0) scratch[warp] = make_float2(m, s);
+    __syncthreads();
+    float bm = -INFINITY, bs = 0.0f;
+    if (t == 0)
+      for (int k = 0; k < T / 32; ++k) online_merge(bm, bs, scratch[k].x, scratch[k].y);
+    const float2 rp = exchange_row_pair(p.ex, u, part, it, bm, bs, timed_out, &row_pair);
+    const float mm = rp.x;
+    const float inv = mm == -INFINITY ? __int_as_float(0x7fc00000) : 1.0f / rp.y;
+    float *yr = p.y + r * p.ldy + c0;
+    auto out4 = [&](float4 a) {
+      return make_float4(expf(a.x - mm) * inv, expf(a.y - mm) * inv, expf(a.z - mm) * inv,
+                         expf(a.w - mm) * inv);
+    };
+    // Pass 2, each thread's vectors backwards: the latest read are the
+    // likeliest to be still in L2, and the earliest are in shared memory.
+    if (kVec) {
+      const float4 *xv = reinterpret_cast<const float4 *>(xr);
+      float4 *yv = reinterpret_cast<float4 *>(yr);
+      int i = n - 1;
+      for (; i - 3 >= kGridKeep; i -= 4) {
+        float4 a[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) a[k] = xv[t + (i - k) * T];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) __stcs(yv + t + (i - k) * T, out4(a[k]));
+      }
+      for (; i >= kGridKeep; --i) __stcs(yv + t + i * T, out4(xv[t + i * T]));
+      for (; i >= 0; --i) __stcs(yv + t + i * T, out4(keep[i * T + t]));
+    }
+    {
+      const int j0 = 4 * nv + t;
+      int i = len > j0 ? (len - 1 - j0) / T : -1;
+      for (; i >= 3; i -= 4) {
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = xr[j0 + (i - k) * T];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) __stcs(yr + j0 + (i - k) * T, expf(v[k] - mm) * inv);
+      }
+      for (; i >= 0; --i) __stcs(yr + j0 + i * T, expf(xr[j0 + i * T] - mm) * inv);
+    }
+  }
+}
+
+std::atomic<unsigned int> g_grid_epoch{0};
+std::atomic<int64_t> g_sm_wait_limit_ns{int64_t(10) * 1000 * 1000 * 1000};
+std::atomic<int> g_sm_drop_block{-1};
+
+// This call's exchange: the next of the kGridRegions regions, its 2 U counters
+// zeroed on `stream` ahead of the launch.
+cudaError_t make_exchange(int G, int64_t U, cudaStream_t stream, RowExchange *ex) {
+  const unsigned int region = g_grid_epoch.fetch_add(1, std::memory_order_relaxed) % kGridRegions;
+  unsigned int *counters = nullptr;
+  float2 *pairs = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&counters), g_sm_counters);
+  if (e != cudaSuccess) return e;
+  e = cudaGetSymbolAddress(reinterpret_cast<void **>(&pairs), g_sm_pairs);
+  if (e != cudaSuccess) return e;
+  ex->G = G;
+  ex->U = int(U);
+  ex->counters = counters + size_t(region) * 2 * kGridMaxBlocks;
+  ex->pairs = pairs + size_t(region) * 2 * kGridMaxBlocks;
+  ex->wait_limit_ns = g_sm_wait_limit_ns.load(std::memory_order_relaxed);
+  ex->drop_block = g_sm_drop_block.load(std::memory_order_relaxed);
+  return cudaMemsetAsync(ex->counters, 0, size_t(2) * size_t(U) * sizeof(unsigned int), stream);
 }
 
 // Per-device launch facts for one kernel instantiation, set up on first use.
@@ -410,7 +646,7 @@ struct KernelSetup {
 // Stage plan for rows too long for a warp: how many blocks share a row, how
 // many columns each stages, and whether two buffers fit.
 struct StagePlan {
-  int cluster;   // blocks per row (1, 2, 4, 8 or 16)
+  int cluster;   // blocks per row (1, 2, 4 or 8)
   int chunk;     // columns per block, a multiple of 4 when cluster > 1
   bool dbl;      // double-buffered
 };
@@ -513,6 +749,58 @@ cudaError_t launch_staged_any(int64_t rows, int cols, const StagePlan &plan, con
 #undef TMM_STAGED
 }
 
+// Rows from this length on take softmax_grid_kernel (measured on GB300: from
+// here on it beats a cluster staging the row; below, staging wins).
+constexpr int kGridRowCols = 98304;
+
+template <bool kVec>
+cudaError_t launch_grid_rows(int64_t rows, int cols, const float *x, int64_t ldx, float *y,
+                             int64_t ldy, const DeviceInfo &dev, cudaStream_t stream) {
+  static KernelSetup st;
+  static std::atomic<int> blocks_per_sm[64];
+  auto kernel = softmax_grid_kernel<kVec>;
+  const size_t smem = kVec ? size_t(kGridKeep) * kGridThreads * sizeof(float4) : 0;
+  const uint64_t bit = uint64_t(1) << (dev.id & 63);
+  if (!(st.configured.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+    if (e != cudaSuccess) return e;
+    // The default carveout: a larger L1 serves some of pass 2's re-reads
+    // (measured: the maximum shared carveout loses 10-15 %).
+    int nb = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kGridThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (nb < 1) return cudaErrorInvalidConfiguration;
+    blocks_per_sm[dev.id & 63].store(nb, std::memory_order_relaxed);
+    st.configured.fetch_or(bit, std::memory_order_release);
+  }
+  const int64_t grid = std::min<int64_t>(
+      int64_t(blocks_per_sm[dev.id & 63].load(std::memory_order_relaxed)) * dev.sm_count,
+      kGridMaxBlocks);
+  GridRowsParams prm = {};
+  prm.rows = rows;
+  prm.cols = cols;
+  const int G = int(std::min<int64_t>((int64_t(cols) + kGridChunk - 1) / kGridChunk, grid));
+  prm.chunk = int((((int64_t(cols) + G - 1) / G) + 3) & ~int64_t(3));
+  prm.x = x;
+  prm.ldx = ldx;
+  prm.y = y;
+  prm.ldy = ldy;
+  cudaError_t e = make_exchange(G, std::min<int64_t>(grid / G, rows), stream, &prm.ex);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(unsigned(int64_t(prm.ex.U) * prm.ex.G), 1, 1);
+  cfg.blockDim = dim3(kGridThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, prm);
+}
+
 int64_t warp_grid(int64_t units, const DeviceInfo &dev) {
   constexpr int kWarps = kWarpRowThreads / 32;
   return std::max<int64_t>(1, std::min<int64_t>((units + kWarps - 1) / kWarps,
@@ -538,6 +826,19 @@ cudaError_t launch_warp_vec(int64_t rows, int cols, const float *x, int64_t ldx,
 }
 
 }  // namespace
+
+cudaError_t softmax_device_status(unsigned int *status, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, g_softmax_status, sizeof(unsigned int));
+  if (e != cudaSuccess || !clear) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_softmax_status, &zero, sizeof(unsigned int));
+}
+
+void softmax_set_test_hooks(int drop_block, int64_t wait_limit_ns) {
+  g_sm_drop_block.store(drop_block, std::memory_order_relaxed);
+  g_sm_wait_limit_ns.store(wait_limit_ns > 0 ? wait_limit_ns : int64_t(10) * 1000 * 1000 * 1000,
+                           std::memory_order_relaxed);
+}
 
 int64_t sum_grid_blocks(int64_t n, const DeviceInfo &dev) {
   const int64_t per_block = int64_t(kSumThreads) * 4 * 4;   // four vectors per thread
@@ -594,6 +895,9 @@ cudaError_t launch_softmax_rows(int64_t rows, int cols, const float *x, int64_t 
   if (cols <= 1024) return TMM_WARP(32, 32);
 #undef TMM_WARP
 #undef TMM_WVEC
+  if (cols >= kGridRowCols)
+    return aligned ? launch_grid_rows<true>(rows, cols, x, ldx, y, ldy, dev, stream)
+                   : launch_grid_rows<false>(rows, cols, x, ldx, y, ldy, dev, stream);
   StagePlan plan;
   if (plan_stage(cols, &plan)) {
     switch (staged_threads(plan.chunk, plan.cluster)) {
@@ -603,9 +907,8 @@ cudaError_t launch_softmax_rows(int64_t rows, int cols, const float *x, int64_t 
       default: return launch_staged_any<1024>(rows, cols, plan, x, ldx, y, ldy, aligned, dev, stream);
     }
   }
-  const int64_t grid = std::min<int64_t>(rows, int64_t(dev.sm_count) * 2);
-  softmax_long_kernel<<<unsigned(grid), kLongRowThreads, 0, stream>>>(rows, cols, x, ldx, y, ldy);
-  return cudaGetLastError();
+  return aligned ? launch_grid_rows<true>(rows, cols, x, ldx, y, ldy, dev, stream)
+                 : launch_grid_rows<false>(rows, cols, x, ldx, y, ldy, dev, stream);
 }
 
 }  // namespace tmm

@@ -51,6 +51,8 @@ void tc3_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns);
 constexpr int kMaxWindow = 129;
 cudaError_t window_device_status(unsigned int *status, bool clear);
 void window_set_test_hooks(int drop_block, int64_t wait_limit_ns);
+cudaError_t softmax_device_status(unsigned int *status, bool clear);
+void softmax_set_test_hooks(int drop_block, int64_t wait_limit_ns);
 cudaError_t launch_window_sum(int64_t n, int W, const float *x, float *y,
                               const DeviceInfo &dev, cudaStream_t stream);
 
