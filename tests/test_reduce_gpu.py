@@ -284,3 +284,24 @@ def test_softmax_grid_wait_timeout_is_reported_and_recovers(rows, cols):
     assert lib.tmm_check_device(stream) == _abi.TMM_OK
     check_softmax(x)
     assert lib.tmm_check_device(stream) == _abi.TMM_OK
+
+
+def test_softmax_long_rows_on_concurrent_streams():
+    # Calls in flight at once on different streams take different regions of
+    # the library's exchange memory; every result must still be right.
+    lib = _abi.load()
+    shapes = [(16, 131072), (8, 300000), (3, 1048576), (32, 98304)]
+    xs = [logits(r, c, 129 + i) for i, (r, c) in enumerate(shapes)]
+    streams = [torch.cuda.Stream() for _ in shapes]
+    xd = [torch.from_numpy(x).cuda() for x in xs]
+    yd = [torch.empty_like(d) for d in xd]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for (r, c), x, y, st in zip(shapes, xd, yd, streams):
+            assert lib.softmax_rows_f32(r, c, x.data_ptr(), c, y.data_ptr(), c,
+                                        st.cuda_stream) == _abi.TMM_OK
+    torch.cuda.synchronize()
+    assert lib.tmm_check_device(_stream()) == _abi.TMM_OK
+    for x, y in zip(xs, yd):
+        want = oracle.softmax_rows(x)
+        assert np.all(np.abs(y.cpu().numpy() - want) <= softmax_tolerance(x, want))
