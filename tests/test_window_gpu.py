@@ -26,22 +26,23 @@ def _library():
     _abi.load()
 
 
-def gpu_window(x_host, W, x_off=0):
+def gpu_window(x_host, W, x_off=0, y_off=0):
     n = x_host.shape[0] - W + 1
     xb = torch.zeros(x_off + x_host.shape[0] + 8, dtype=torch.float32, device="cuda")
     xb[x_off:x_off + x_host.shape[0]] = torch.from_numpy(x_host).cuda()
-    yb = torch.from_numpy(np.full(n + 64, CANARY_BITS, np.uint32).view(np.float32)).cuda()
-    rc = _abi.load().window_sum_f32(n, W, xb.data_ptr() + 4 * x_off, yb.data_ptr(),
+    yb = torch.from_numpy(np.full(y_off + n + 64, CANARY_BITS, np.uint32).view(np.float32)).cuda()
+    rc = _abi.load().window_sum_f32(n, W, xb.data_ptr() + 4 * x_off, yb.data_ptr() + 4 * y_off,
                                     torch.cuda.current_stream().cuda_stream)
     assert rc == _abi.TMM_OK, _abi.last_error()
     torch.cuda.synchronize()
     out = yb.cpu().numpy()
-    assert np.all(out[n:].view(np.uint32) == CANARY_BITS), "wrote past the n outputs"
-    return out[:n]
+    assert np.all(out[:y_off].view(np.uint32) == CANARY_BITS), "wrote before the outputs"
+    assert np.all(out[y_off + n:].view(np.uint32) == CANARY_BITS), "wrote past the n outputs"
+    return out[y_off:y_off + n]
 
 
-def check(x, W, x_off=0):
-    y = gpu_window(x, W, x_off)
+def check(x, W, x_off=0, y_off=0):
+    y = gpu_window(x, W, x_off, y_off)
     want32 = oracle.window_sum_f32_ascending(x, W)
     assert np.array_equal(y.view(np.uint32), want32.view(np.uint32)), (W, x.shape)
     ref = oracle.window_sum(x, W)
@@ -65,6 +66,15 @@ def test_random_float_bit_exact(W, n):
 def test_unaligned_input(x_off):
     rng = np.random.default_rng(91)
     check(rng.standard_normal(50001, dtype=np.float32), 5, x_off)
+
+
+@pytest.mark.parametrize("W", [2, 5, 17])
+@pytest.mark.parametrize("x_off,y_off", [(0, 1), (0, 2), (1, 3), (2, 0), (3, 1)])
+def test_unaligned_output_and_input(W, x_off, y_off):
+    # y off a 16-byte boundary takes the one-output-per-thread form; n = 4097 + 2
+    # leaves a ragged group of four at the end.
+    rng = np.random.default_rng(92 + W)
+    check(rng.standard_normal(4099 + W - 1, dtype=np.float32), W, x_off, y_off)
 
 
 def test_integer_inputs_exact_against_definition():

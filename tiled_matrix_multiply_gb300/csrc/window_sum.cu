@@ -16,9 +16,13 @@
 //     by the next tile, an L2 hit): one bulk copy (the TMA unit's
 //     cp.async.bulk, counted on an mbarrier) per tile when x is 16-byte
 //     aligned, 4-byte cp.async copies by every thread otherwise;
-//   * thread t owns outputs t, t + 256, ..., so a warp's shared-memory reads
-//     and global stores are consecutive words (no bank conflicts, full
-//     128-byte store lines);
+//   * with a compile-time width and y 16-byte aligned, thread t owns groups of
+//     four consecutive outputs (4 g .. 4 g + 3, g = t, t + 256, ...), reads
+//     their inputs as ceil((W + 3) / 4) 16-byte vectors and stores the four
+//     sums with one 16-byte store: a warp's reads and stores are consecutive
+//     vectors (no bank conflicts, whole 128-byte lines), with a fifth of the
+//     shared-memory reads of one output per thread at W = 5; otherwise thread
+//     t owns outputs t, t + 256, ... (consecutive words per warp);
 //   * each sum starts from 0 and adds x_{i+d} in ascending d in FP32, the
 //     page's order, so results equal that sequence of roundings exactly.
 #include <atomic>
@@ -36,6 +40,7 @@ namespace {
 constexpr int kWinThreads = 256;
 constexpr int kWinItems = 16;
 constexpr int kWinTile = kWinThreads * kWinItems;   // outputs per tile
+static_assert(kWinItems % 4 == 0, "whole groups of four outputs per thread");
 constexpr int kWinMaxHalo = kMaxWindow - 1;
 constexpr int kWinBuf = kWinTile + kWinMaxHalo + 4;  // floats per staging buffer (16-byte multiple)
 constexpr int kWinSmemBytes = 2 * kWinBuf * int(sizeof(float));
@@ -96,7 +101,7 @@ __device__ __forceinline__ void win_wait() {
 template <int kW>   // kW > 0: compile-time width; 0: runtime width
 __global__ void __launch_bounds__(kWinThreads)
 window_sum_kernel(int64_t n, int W_rt, const float *__restrict__ x, float *__restrict__ y,
-                  int vec, int64_t wait_limit_ns, int drop_block) {
+                  int vec, int yvec, int64_t wait_limit_ns, int drop_block) {
   extern __shared__ __align__(16) float stage[];   // two buffers of kWinBuf floats
   __shared__ __align__(8) uint64_t bars[2];         // bulk copies into buffer b (vec)
   const int W = kW > 0 ? kW : W_rt;
@@ -162,17 +167,51 @@ window_sum_kernel(int64_t n, int W_rt, const float *__restrict__ x, float *__res
       break;
     }
     const int64_t base = tl * kWinTile;
-#pragma unroll 4
-    for (int j = 0; j < kWinItems; ++j) {
-      const int o = j * kWinThreads + t;
-      float s = 0.0f;
-      if (kW > 0) {
+    if (kW > 0 && yvec) {
+      // Thread t owns the groups of four outputs 4 g .. 4 g + 3, g = t, t + 256,
+      // ...: their inputs are ceil((kW + 3) / 4) consecutive 16-byte vectors of
+      // the tile (consecutive lanes, consecutive vectors: no bank conflicts),
+      // and one 16-byte store writes the four sums.
+      constexpr int kVecs = (kW + 3 + 3) / 4;
 #pragma unroll
-        for (int d = 0; d < kW; ++d) s += tile[o + d];
-      } else {
-        for (int d = 0; d < W; ++d) s += tile[o + d];
+      for (int j = 0; j < kWinItems / 4; ++j) {
+        const int g = j * kWinThreads + t;
+        float v[4 * kVecs];
+#pragma unroll
+        for (int k = 0; k < kVecs; ++k) {
+          const float4 a = reinterpret_cast<const float4 *>(tile)[g + k];
+          v[4 * k] = a.x; v[4 * k + 1] = a.y; v[4 * k + 2] = a.z; v[4 * k + 3] = a.w;
+        }
+        float o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float s = 0.0f;
+#pragma unroll
+          for (int d = 0; d < kW; ++d) s += v[i + d];
+          o[i] = s;
+        }
+        const int64_t i0 = base + 4 * g;
+        if (i0 + 3 < n) {
+          __stcs(reinterpret_cast<float4 *>(y + i0), make_float4(o[0], o[1], o[2], o[3]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i0 + i < n) __stcs(y + i0 + i, o[i]);
+        }
       }
-      if (base + o < n) __stcs(y + base + o, s);
+    } else {
+#pragma unroll 4
+      for (int j = 0; j < kWinItems; ++j) {
+        const int o = j * kWinThreads + t;
+        float s = 0.0f;
+        if (kW > 0) {
+#pragma unroll
+          for (int d = 0; d < kW; ++d) s += tile[o + d];
+        } else {
+          for (int d = 0; d < W; ++d) s += tile[o + d];
+        }
+        if (base + o < n) __stcs(y + base + o, s);
+      }
     }
     __syncthreads();     // every thread is done with this buffer before it is refilled
   }
@@ -210,8 +249,9 @@ cudaError_t launch_width(int64_t n, int W, const float *x, float *y, int vec,
   if (e != cudaSuccess) return e;
   const int64_t tiles = (n + kWinTile - 1) / kWinTile;
   const int64_t grid = std::min<int64_t>(tiles, int64_t(dev.sm_count) * (nb > 0 ? nb : 1));
+  const int yvec = (reinterpret_cast<uintptr_t>(y) & 15u) == 0 ? 1 : 0;
   kernel<<<unsigned(grid), kWinThreads, kWinSmemBytes, stream>>>(
-      n, W, x, y, vec, g_win_wait_limit_ns.load(std::memory_order_relaxed),
+      n, W, x, y, vec, yvec, g_win_wait_limit_ns.load(std::memory_order_relaxed),
       g_win_drop_block.load(std::memory_order_relaxed));
   return cudaGetLastError();
 }
