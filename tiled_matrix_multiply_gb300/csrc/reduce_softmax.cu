@@ -10,7 +10,7 @@
 //
 // Array sum (sum_f32): two launches, no atomics, so the result is the same bits
 // on every call.
-//   1. sum_partials_kernel: a grid of G <= max(4 x SMs, 512) blocks of 512
+//   1. sum_partials_kernel: a grid of G <= min(max(8 x SMs, 512), 1024) blocks of 512
 //      threads.  Thread g of the P = 512 G threads adds, in its four lanes, the
 //      16-byte vectors g, g + P, g + 2P, ... of the 16-byte-aligned body (four
 //      streaming loads in flight per step).  Of the at most six leading and
@@ -885,7 +885,8 @@ void softmax_set_test_hooks(int drop_block, int64_t wait_limit_ns) {
 
 int64_t sum_grid_blocks(int64_t n, const DeviceInfo &dev) {
   const int64_t per_block = int64_t(kSumThreads) * 4 * 4;   // four vectors per thread
-  const int64_t cap = std::max<int64_t>(int64_t(dev.sm_count) * 4, 512);
+  // 8 blocks per SM (at most kSumFinalThreads partials): measured 1 % over 4.
+  const int64_t cap = std::max<int64_t>(int64_t(dev.sm_count) * 8, 512);
   return std::max<int64_t>(1, std::min<int64_t>((n + per_block - 1) / per_block,
                                                 std::min<int64_t>(cap, kSumFinalThreads)));
 }
