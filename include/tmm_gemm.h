@@ -227,9 +227,10 @@ int tmm_check_device(tmm_stream_t stream);
 
 /*
  * tmm_testing_set_wait_hooks -- testing only; no counterpart in the pages.
- * drop_signal_block >= 0 makes that block of later stream-K launches (of
- * gemm_f32 and gemm_f32_tc3) skip raising its flags, so the block waiting on
- * it runs into the time limit, and makes that block of later window_sum_f32
+ * drop_signal_block >= 0 makes that block of later split-tile launches of
+ * gemm_f32 (and that split unit -- the K-part of a tile, numbered across the
+ * call's split tiles -- of gemm_f32_tc3) skip raising its flags, so the one
+ * waiting on it runs into the time limit, and makes that block of later window_sum_f32
  * launches (16-byte-aligned x) wait for 16 bytes more than its first tile
  * copy brings, and that block of later softmax_rows_f32 launches on rows of
  * 98304 or more columns skip counting itself in;

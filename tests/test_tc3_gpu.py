@@ -114,7 +114,7 @@ def test_float_odd_shapes(shape):
 
 
 # Fewer tiles than half the slots: every tile is cut into K-parts of at least
-# two 256-value chunks, each part adding the next part's running sum.  Block
+# two 256-value chunks, each part adding the running sum of the parts before it.  Block
 # pairs: 6 tiles in 4 parts; 16 tiles in 2 parts, the last chunk 32 values long.
 # One-block kernel: 4 tiles of K = 2000 in 4 parts; one tile of K = 8192 in 4 parts.
 PART_SHAPES = [(512, 768, 3000), (1024, 1024, 1050), (100, 1000, 2000), (64, 256, 8192)]
@@ -201,15 +201,17 @@ def test_python_binding_side_stream():
     parity.assert_close(C.cpu().numpy(), oracle.gemm(A, B), 200, "binding")
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 51200, 512), (2560, 2560, 512), (2560, 2560, 1024),
-                                   (512, 768, 3000), (100, 1000, 2000)])
-def test_stream_k_wait_timeout_is_reported_and_recovers(M, N, K):
+@pytest.mark.parametrize("M,N,K,drop", [(128, 51200, 512, 0), (2560, 2560, 512, 0),
+                                        (2560, 2560, 1024, 2), (512, 768, 3000, 1),
+                                        (100, 1000, 2000, 1)])
+def test_stream_k_wait_timeout_is_reported_and_recovers(M, N, K, drop):
     # The first three shapes leave a partial last wave, so the tail tiles are
     # split along K: 128 rows run on the one-block kernel (200 tiles of
     # 128 x 256, 152 per wave); 2560 x 2560 on the block-pair kernel (100 tiles
     # of 256 x 256, 76 pairs per wave).  The last two have few tiles, each cut
-    # into four K-parts (pairs; one-block kernel), so unit 1 is a middle part.
-    # Split unit 1 never raises its flags.
+    # into four K-parts (pairs; one-block kernel).  Split unit `drop` never
+    # raises its flags: the first part of a tile (0, 2) or a middle part (1 of
+    # four), so the next part waits in vain.
     lib = _abi.load()
     stream = torch.cuda.current_stream().cuda_stream
     rng = np.random.default_rng(58)
@@ -217,7 +219,7 @@ def test_stream_k_wait_timeout_is_reported_and_recovers(M, N, K):
     B = rng.integers(-4, 5, (K, N)).astype(np.float32)
     assert lib.tmm_check_device(stream) == _abi.TMM_OK
     try:
-        assert lib.tmm_testing_set_wait_hooks(1, 2_000_000) == _abi.TMM_OK
+        assert lib.tmm_testing_set_wait_hooks(drop, 2_000_000) == _abi.TMM_OK
         _run(A, B, check_canaries=False, check_status=False)
         rc = lib.tmm_check_device(stream)
         assert rc == _abi.TMM_ERR_DEVICE_TIMEOUT, rc

@@ -36,14 +36,16 @@
 // Scheduling: tiles in row-major order, so the tiles in flight move through K
 // together and share the A and B panels in L2.  When the tile count leaves the
 // last wave at most half full, each of its tiles is split into two halves of
-// the K range, run side by side: the unit holding the upper half stores its
+// the K range, run side by side: the unit holding the lower half stores its
 // partial sums into C and raises a flag (one per accumulate warp), the unit
-// holding the lower half waits for it (bounded), adds, and stores the total --
+// holding the upper half waits for it (bounded), adds, and stores the total --
 // in that fixed order, so results are deterministic.  The last wave then takes
 // half the time.  With at most half as many tiles as slots, every tile is cut
-// into up to four K-parts on chunk boundaries in the same way: the last part
-// stores, and each earlier part waits for the next one's flag, adds C, stores
-// and (unless it is the first) raises its own flag.
+// into up to four K-parts on chunk boundaries in the same way: the first part
+// stores and raises its flag, and each later part waits for the previous one's
+// flag, adds C, stores and (unless it is the last) raises its own.  A part's
+// units come in item order, so a waiting block or pair always waits for one
+// launched before it: no wait depends on a block that has not started.
 // Epilogue: each accumulate warp holds 32 rows (one per lane) of 128 columns;
 // it stores them through a 4 KiB staging buffer in shared memory, transposed
 // so that every store instruction writes whole 128-byte lines of C.
@@ -282,8 +284,8 @@ __device__ __forceinline__ void tc3_tile_coords(int tile, int tiles_n, int &tm, 
 
 // This block's work items (tile, K-slice range): items b, b + stride, ...
 // of the list [whole tiles, split units]; `unit` >= 0 numbers the items that
-// share a split tile, `parts` consecutive units per tile (part 0, the owner,
-// holds the lowest K-range).  The one-block kernel launches one block per item;
+// share a split tile, `parts` consecutive units per tile (part 0 holds the
+// lowest K-range; the last part, which stores the total, the highest).  The one-block kernel launches one block per item;
 // the pair kernel one pair per resident slot, each pair walking its items in
 // order.  Whole tiles are a multiple of the stride whenever units exist, so
 // all units fall in the last round, each on its own pair and alongside its
@@ -355,11 +357,12 @@ __device__ __forceinline__ float f4_get(const float4 &v, int j) {
 // the row-per-lane layout touches 32 lines with 16 bytes each).  16-byte
 // chunk q of staged row r sits at position q ^ (r % 8), which keeps both the
 // row-wise writes and the transposed reads free of bank conflicts.
-// adds_next: add the partial sums that C already holds (from the next K-part),
-// loaded kStoreBatch vectors at a time before the first of their stores.
+// adds_prev: add the partial sums that C already holds (the running sum of the
+// earlier K-parts), loaded kStoreBatch vectors at a time before the first of
+// their stores.
 __device__ __forceinline__ void store_c_block(const Tc3Params &p, const float (&acc)[kTcBN / 2],
                                               int row_base, int col0, uint32_t stg, int lane,
-                                              bool adds_next) {
+                                              bool adds_prev) {
   const int rsub = lane >> 3;   // row within each group of four
   const int cq = lane & 7;      // 16-byte chunk within the 32 columns
   constexpr int kStoreBatch = 2;   // groups of four rows loaded and stored together
@@ -382,7 +385,7 @@ __device__ __forceinline__ void store_c_block(const Tc3Params &p, const float (&
         v[u] = ld_shared_v4(stg + uint32_t(r * 128 + ((cq ^ (r & 7)) << 4)));
         w[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      if (adds_next && vec) {
+      if (adds_prev && vec) {
 #pragma unroll
         for (int u = 0; u < kStoreBatch; ++u) {
           const int row = row_base + 4 * (kStoreBatch * h + u) + rsub;
@@ -397,7 +400,7 @@ __device__ __forceinline__ void store_c_block(const Tc3Params &p, const float (&
         float *c_row = p.C + int64_t(row) * p.ldc;
         if (vec) {
           float4 o = v[u];
-          if (adds_next) {
+          if (adds_prev) {
             o.x = w[u].x + o.x; o.y = w[u].y + o.y; o.z = w[u].z + o.z; o.w = w[u].w + o.w;
           }
           *reinterpret_cast<float4 *>(c_row + col) = o;
@@ -406,7 +409,7 @@ __device__ __forceinline__ void store_c_block(const Tc3Params &p, const float (&
           for (int j = 0; j < 4; ++j)
             if (col + j < p.N) {
               float o = f4_get(v[u], j);
-              if (adds_next) o = __ldcg(c_row + col + j) + o;
+              if (adds_prev) o = __ldcg(c_row + col + j) + o;
               c_row[col + j] = o;
             }
         }
@@ -583,10 +586,13 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
       int tm, tn;
       tc3_tile_coords(tile, p.tiles_n, tm, tn);
       const int col0 = tn * kTcBN + half * (kTcBN / 2);
-      const bool adds_next = ke < p.slices;   // slices [ke, S) are unit + 1's, summed in C
-      if (adds_next) {
+      // A split tile's parts run in item order: part q adds the running sum of
+      // parts 0 .. q-1 (unit - 1's, in C) to its own, so every wait is for an
+      // item dispatched earlier.
+      const bool adds_prev = kb > 0;
+      if (adds_prev) {
         if (lane == 0) {
-          const unsigned int *f = &flags[(unit + 1) * kTc3FlagsPerBlock + acc_warp];
+          const unsigned int *f = &flags[(unit - 1) * kTc3FlagsPerBlock + acc_warp];
           const uint64_t t0 = timer_ns();
           while (ld_acquire_u32(f) != p.epoch) {
             if (int64_t(timer_ns() - t0) > p.wait_limit_ns) {
@@ -599,9 +605,9 @@ gemm_tc3_kernel(const __grid_constant__ CUtensorMap map_ahi,
         __syncwarp();
       }
       store_c_block(p, acc, tm * kTcBM + 32 * quarter, col0,
-                    staging + uint32_t(acc_warp) * 4096u, lane, adds_next);
-      if (kb > 0) {
-        // Slices [kb, S) of a split tile: this warp's partial sums are in C.
+                    staging + uint32_t(acc_warp) * 4096u, lane, adds_prev);
+      if (ke < p.slices) {
+        // Slices [0, ke) of a split tile: this warp's running sum is in C.
         __syncwarp();
         if (lane == 0 && unit != p.drop_signal_block) {
           __threadfence();
@@ -916,10 +922,10 @@ gemm_tc3_pair_kernel(const __grid_constant__ CUtensorMap map_ahi,
       tc3_tile_coords(tile, p.tiles_n, tm, tn);
       const int col0 = tn * kT2BN + half * (kT2BN / 2);
       const int flag = int(rank) * kTcAccWarps + acc_warp;   // per block of the pair and warp
-      const bool adds_next = ke < p.slices;   // slices [ke, S) are unit + 1's, summed in C
-      if (adds_next) {
+      const bool adds_prev = kb > 0;   // slices [0, kb): unit - 1's running sum, in C
+      if (adds_prev) {
         if (lane == 0) {
-          const unsigned int *f = &flags[(unit + 1) * 2 * kTcAccWarps + flag];
+          const unsigned int *f = &flags[(unit - 1) * 2 * kTcAccWarps + flag];
           const uint64_t t0 = timer_ns();
           while (ld_acquire_u32(f) != p.epoch) {
             if (int64_t(timer_ns() - t0) > p.wait_limit_ns) {
@@ -932,8 +938,8 @@ gemm_tc3_pair_kernel(const __grid_constant__ CUtensorMap map_ahi,
         __syncwarp();
       }
       store_c_block(p, acc, tm * kT2BM + int(rank) * kT2Rows + 32 * quarter, col0,
-                    staging + uint32_t(acc_warp) * 4096u, lane, adds_next);
-      if (kb > 0) {
+                    staging + uint32_t(acc_warp) * 4096u, lane, adds_prev);
+      if (ke < p.slices) {
         __syncwarp();
         if (lane == 0 && unit != p.drop_signal_block) {
           __threadfence();
