@@ -388,10 +388,11 @@ constexpr int kRegVecs = 8;   // a thread's staged vectors held in registers, at
 template <int kThreads, bool kVec, bool kDouble, bool kCluster>
 __global__ void __launch_bounds__(kThreads)
 softmax_staged_kernel(int64_t rows, int cols, int chunk, const float *x, int64_t ldx, float *y,
-                      int64_t ldy) {
+                      int64_t ldy, unsigned long long *rowctr) {
   extern __shared__ __align__(16) float stage[];
   __shared__ float scratch[32];
   __shared__ float2 slots[2][kMaxCluster];
+  __shared__ long long s_next;
   const int t = threadIdx.x;
   int C = 1, c = 0;
   int64_t unit = blockIdx.x, units = gridDim.x;
@@ -411,15 +412,34 @@ softmax_staged_kernel(int64_t rows, int cols, int chunk, const float *x, int64_t
     for (int q = t; q < nv; q += kThreads) cp_async_16(buf + 4 * q, xr + 4 * q);
     for (int j = 4 * nv + t; j < len; j += kThreads) cp_async_4(buf + j, xr + j);
   };
+  // Rows: a block's first is its index; with a row counter (one block per
+  // row, double-buffered) each later one is taken from the counter while the
+  // block works on the one before, so blocks the warp schedulers favour take
+  // more rows and all finish together (measured: with fixed strides the last
+  // blocks ended 40 % after the first).  A row's result does not depend on the
+  // block that computes it.
+  // Blocks of up to 256 threads only (measured: 3-13 % faster for rows of
+  // 2560-4096 columns; with 512-thread blocks 10-17 % slower).
+  constexpr bool kDyn = !kCluster && kDouble && kThreads <= 256;
+  const bool dyn = kDyn && rowctr != nullptr;
   int64_t r = unit;
+  int64_t rn = r + units;   // the row after r
+  if (dyn) {
+    if (t == 0) s_next = (long long)(units + int64_t(atomicAdd(&rowctr[0], 1ull)));
+    __syncthreads();
+    rn = s_next;
+  }
   if (kDouble) {
     if (r < rows) copy_row(stage, r);
     cp_async_commit();
   }
-  for (int it = 0; r < rows; r += units, ++it) {
+  for (int it = 0; r < rows; ++it) {
+    // The row after rn: taken now, its number needed only after pass 1, so
+    // the counter's latency is hidden behind the pass.
+    unsigned long long tok = 0;
+    if (dyn && t == 0) tok = atomicAdd(&rowctr[0], 1ull);
     float *row = stage + (kDouble ? (it & 1) * chunk_pad : 0);
     if (kDouble) {
-      const int64_t rn = r + units;
       if (rn < rows) copy_row(stage + ((it + 1) & 1) * chunk_pad, rn);
       cp_async_commit();
       cp_async_wait<1>();        // this thread's copies of row r have landed
@@ -446,6 +466,7 @@ softmax_staged_kernel(int64_t rows, int cols, int chunk, const float *x, int64_t
         }
       }
       m = block_reduce<true>(m, scratch);
+      if (dyn && t == 0) s_next = (long long)(units + int64_t(tok));   // read after the next barrier
       // In a cluster, an all -inf chunk takes 0 as its reference: its terms are 0 either way.
       const float ref = (kCluster && m == -INFINITY) ? 0.0f : m;
       // Pass 2: the exponentials, and their sum (same order as below).
@@ -465,6 +486,7 @@ softmax_staged_kernel(int64_t rows, int cols, int chunk, const float *x, int64_t
       }
       for (int j = 4 * nv + t; j < len; j += kThreads) m = fmaxf(m, row[j]);
       m = block_reduce<true>(m, scratch);
+      if (dyn && t == 0) s_next = (long long)(units + int64_t(tok));   // read after the next barrier
       const float ref = (kCluster && m == -INFINITY) ? 0.0f : m;
       // Pass 2: exponentials in place, and their sum.
       for (int q = t; q < nv; q += kThreads) {
@@ -482,6 +504,7 @@ softmax_staged_kernel(int64_t rows, int cols, int chunk, const float *x, int64_t
       }
     }
     s = block_reduce<false>(s, scratch);
+    const int64_t rnn = dyn ? int64_t(s_next) : rn + units;
     float scale;
     if (kCluster) {
       cg::cluster_group cl = cg::this_cluster();
@@ -515,9 +538,17 @@ softmax_staged_kernel(int64_t rows, int cols, int chunk, const float *x, int64_t
       }
       for (int j = 4 * nv + t; j < len; j += kThreads) __stcs(yr + j, row[j] * scale);
     }
+    r = rn;
+    rn = rnn;
   }
   cp_async_wait<0>();
   if (kCluster) cg::this_cluster().sync();
+  if (dyn && t == 0 && atomicAdd(&rowctr[1], 1ull) == gridDim.x - 1ull) {
+    // The last block done: every fetch has happened, so reset for the next call.
+    rowctr[0] = 0;
+    rowctr[1] = 0;
+    __threadfence();
+  }
 }
 
 // Running (maximum, sum) of one thread's terms: s = sum e^{x - m}.  When the
@@ -659,6 +690,19 @@ softmax_grid_kernel(const GridRowsParams p) {
 }
 
 std::atomic<unsigned int> g_grid_epoch{0};
+std::atomic<unsigned int> g_rows_epoch{0};
+
+// Row counters of softmax_staged_kernel, kGridRegions pairs (next row, blocks
+// done); each call takes the next pair, and its last block resets it.
+__device__ unsigned long long g_sm_rows[kGridRegions][2];
+
+cudaError_t row_counter(unsigned long long **ctr) {
+  unsigned long long *base = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&base), g_sm_rows);
+  if (e != cudaSuccess) return e;
+  *ctr = base + 2 * (g_rows_epoch.fetch_add(1, std::memory_order_relaxed) % kGridRegions);
+  return cudaSuccess;
+}
 std::atomic<int64_t> g_sm_wait_limit_ns{int64_t(10) * 1000 * 1000 * 1000};
 std::atomic<int> g_sm_drop_block{-1};
 
@@ -774,7 +818,14 @@ cudaError_t launch_staged(int64_t rows, int cols, const StagePlan &plan, const f
     units = std::min<int64_t>(rows, int64_t(dev.sm_count) * (nb > 0 ? nb : 1));
     cfg.gridDim = dim3(unsigned(units), 1, 1);
   }
-  return cudaLaunchKernelEx(&cfg, kernel, rows, cols, plan.chunk, x, ldx, y, ldy);
+  unsigned long long *rowctr = nullptr;
+  // A row counter only where several blocks share an SM (with one block per
+  // SM there is no imbalance to remove).
+  if (!kCluster && kDouble && kThreads <= 256 && units >= 2 * int64_t(dev.sm_count)) {
+    cudaError_t e = row_counter(&rowctr);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, rows, cols, plan.chunk, x, ldx, y, ldy, rowctr);
 }
 
 template <int kThreads>
