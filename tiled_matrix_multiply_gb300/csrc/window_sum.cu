@@ -101,9 +101,11 @@ __device__ __forceinline__ void win_wait() {
 template <int kW>   // kW > 0: compile-time width; 0: runtime width
 __global__ void __launch_bounds__(kWinThreads)
 window_sum_kernel(int64_t n, int W_rt, const float *__restrict__ x, float *__restrict__ y,
-                  int vec, int yvec, int64_t wait_limit_ns, int drop_block) {
+                  int vec, int yvec, int64_t wait_limit_ns, int drop_block,
+                  unsigned long long *tilectr) {
   extern __shared__ __align__(16) float stage[];   // two buffers of kWinBuf floats
   __shared__ __align__(8) uint64_t bars[2];         // bulk copies into buffer b (vec)
+  __shared__ long long s_next;
   const int W = kW > 0 ? kW : W_rt;
   const int64_t len = n + W - 1;                  // valid input elements
   const int64_t tiles = (n + kWinTile - 1) / kWinTile;
@@ -146,12 +148,24 @@ window_sum_kernel(int64_t n, int W_rt, const float *__restrict__ x, float *__res
   bool timed_out = false;
   int stop_it = -1;            // the iteration a timeout ended (vec)
   bool next_issued = false;
+  // Tiles: a block's first is its index; with a tile counter each later one is
+  // taken from it while the block works on the one before, so blocks the warp
+  // schedulers favour take more tiles and all finish together.
+  const bool dyn = tilectr != nullptr;
   int64_t tl = blockIdx.x;
+  int64_t next = tl + gridDim.x;   // the tile after tl
+  if (dyn) {
+    if (t == 0) s_next = (long long)(gridDim.x + atomicAdd(&tilectr[0], 1ull));
+    __syncthreads();
+    next = s_next;
+  }
   if (tl < tiles) copy_tile(0, tl);
   win_commit();
-  for (int it = 0; tl < tiles; tl += gridDim.x, ++it) {
+  for (int it = 0; tl < tiles; ++it) {
     const float *tile = stage + (it & 1) * kWinBuf;
-    const int64_t next = tl + gridDim.x;
+    // The tile after next: taken now, its number needed only after this tile.
+    unsigned long long tok = 0;
+    if (dyn && t == 0) tok = atomicAdd(&tilectr[0], 1ull);
     // The other buffer was last read before the barrier that ended the previous tile.
     next_issued = next < tiles;
     if (next_issued) copy_tile((it + 1) & 1, next);
@@ -166,6 +180,7 @@ window_sum_kernel(int64_t n, int W_rt, const float *__restrict__ x, float *__res
       stop_it = it;
       break;
     }
+    if (dyn && t == 0) s_next = (long long)(gridDim.x + tok);   // read after the last barrier
     const int64_t base = tl * kWinTile;
     if (kW > 0 && yvec) {
       // Thread t owns the groups of four outputs 4 g .. 4 g + 3, g = t, t + 256,
@@ -214,6 +229,9 @@ window_sum_kernel(int64_t n, int W_rt, const float *__restrict__ x, float *__res
       }
     }
     __syncthreads();     // every thread is done with this buffer before it is refilled
+    const int64_t nn = dyn ? int64_t(s_next) : next + gridDim.x;
+    tl = next;
+    next = nn;
   }
   win_wait<0>();
   if (stop_it >= 0 && t == 0) {
@@ -226,10 +244,22 @@ window_sum_kernel(int64_t n, int W_rt, const float *__restrict__ x, float *__res
       win_bar_wait(bar0 + 8u * uint32_t((stop_it + 1) & 1), uint32_t((stop_it + 1) >> 1) & 1u,
                    wait_limit_ns);
   }
+  if (dyn && t == 0 && atomicAdd(&tilectr[1], 1ull) == gridDim.x - 1ull) {
+    // The last block done: every fetch has happened, so reset for the next call.
+    tilectr[0] = 0;
+    tilectr[1] = 0;
+    __threadfence();
+  }
 }
 
 std::atomic<int64_t> g_win_wait_limit_ns{int64_t(10) * 1000 * 1000 * 1000};
 std::atomic<int> g_win_drop_block{-1};
+
+// Tile counters, kWinRegions pairs (next tile, blocks done); each call takes
+// the next pair, and its last block resets it (up to kWinRegions calls in flight).
+constexpr int kWinRegions = 16;
+__device__ unsigned long long g_win_tiles[kWinRegions][2];
+std::atomic<unsigned int> g_win_epoch{0};
 
 template <int kW>
 cudaError_t launch_width(int64_t n, int W, const float *x, float *y, int vec,
@@ -250,9 +280,16 @@ cudaError_t launch_width(int64_t n, int W, const float *x, float *y, int vec,
   const int64_t tiles = (n + kWinTile - 1) / kWinTile;
   const int64_t grid = std::min<int64_t>(tiles, int64_t(dev.sm_count) * (nb > 0 ? nb : 1));
   const int yvec = (reinterpret_cast<uintptr_t>(y) & 15u) == 0 ? 1 : 0;
+  // A tile counter where several blocks share an SM.
+  unsigned long long *tilectr = nullptr;
+  if (grid >= 2 * int64_t(dev.sm_count)) {
+    e = cudaGetSymbolAddress(reinterpret_cast<void **>(&tilectr), g_win_tiles);
+    if (e != cudaSuccess) return e;
+    tilectr += 2 * (g_win_epoch.fetch_add(1, std::memory_order_relaxed) % kWinRegions);
+  }
   kernel<<<unsigned(grid), kWinThreads, kWinSmemBytes, stream>>>(
       n, W, x, y, vec, yvec, g_win_wait_limit_ns.load(std::memory_order_relaxed),
-      g_win_drop_block.load(std::memory_order_relaxed));
+      g_win_drop_block.load(std::memory_order_relaxed), tilectr);
   return cudaGetLastError();
 }
 
