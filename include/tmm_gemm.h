@@ -261,17 +261,20 @@ int window_sum_f32(int64_t n, int W, const float *x, float *y, tmm_stream_t stre
  *     *out = sum_{i=0}^{n-1} x[i].
  * x: DEVICE pointer to n floats, 4-byte aligned; out: DEVICE pointer to one
  * float; workspace: DEVICE buffer of at least sum_f32_workspace_size(n) bytes,
- * 16-byte aligned, which holds one partial sum per block and must not overlap
- * x (TMM_ERR_ALIAS).  All caller-owned; n == 0 writes 0.  0 <= n <= 2^40.
- * Accumulates in FP32 in a fixed order (no atomics), so repeated calls give
- * the same bits; every term passes through at most ceil(n / 2^20) + 28
- * additions, so |*out - sum| <= (ceil(n / 2^20) + 28) 2^-24 sum |x[i]| (to
- * first order).  Two kernel launches on `stream`; no allocation.
+ * 16-byte aligned, which holds one partial sum per chunk of the input and must
+ * not overlap x (TMM_ERR_ALIAS).  All caller-owned; n == 0 writes 0.
+ * 0 <= n <= 2^40.  Accumulates in FP32 in a fixed order (the chunks are fixed
+ * pieces of x, taken by whichever block is free, and their partial sums are
+ * added in chunk order), so repeated calls give the same bits; every term
+ * passes through at most ceil(n / 2^25) + 54 additions, so
+ * |*out - sum| <= (ceil(n / 2^25) + 54) 2^-24 sum |x[i]| (to first order).
+ * Two kernel launches on `stream`, sharing a library-owned counter region
+ * with at most 15 other calls in flight; no allocation.
  */
 int sum_f32(int64_t n, const float *x, float *out, void *workspace, size_t workspace_bytes,
             tmm_stream_t stream);
 
-/* Bytes of workspace sum_f32 needs for n elements (at most 4 KiB). */
+/* Bytes of workspace sum_f32 needs for n elements (at most 64 KiB). */
 size_t sum_f32_workspace_size(int64_t n);
 
 /*

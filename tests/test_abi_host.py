@@ -109,22 +109,22 @@ def test_ex_entry_points_reject_bad_layouts(lib, entry, trans, args):
 
 
 def test_sum_workspace_size(lib):
-    assert lib.sum_f32_workspace_size(0) == lib.sum_f32_workspace_size(1 << 30) == 4096
+    assert lib.sum_f32_workspace_size(0) == lib.sum_f32_workspace_size(1 << 30) == 65536
 
 
 @pytest.mark.parametrize("args,status", [
-    ((-1, FAKE, FAKE + (1 << 30), FAKE + (1 << 31), 4096), _abi.TMM_ERR_INVALID_ARG),  # n < 0
-    (((1 << 40) + 1, FAKE, FAKE + (1 << 30), FAKE + (1 << 31), 4096),
+    ((-1, FAKE, FAKE + (1 << 30), FAKE + (1 << 31), 65536), _abi.TMM_ERR_INVALID_ARG),  # n < 0
+    (((1 << 40) + 1, FAKE, FAKE + (1 << 30), FAKE + (1 << 31), 65536),
      _abi.TMM_ERR_INVALID_ARG),                                                    # n > 2^40
-    ((8, FAKE, 0, FAKE + (1 << 31), 4096), _abi.TMM_ERR_INVALID_ARG),              # out NULL
-    ((8, 0, FAKE + (1 << 30), FAKE + (1 << 31), 4096), _abi.TMM_ERR_INVALID_ARG),  # x NULL
-    ((8, FAKE, FAKE + (1 << 30), 0, 4096), _abi.TMM_ERR_INVALID_ARG),              # no workspace
-    ((8, FAKE, FAKE + (1 << 30), FAKE + (1 << 31), 4095), _abi.TMM_ERR_INVALID_ARG),  # too small
-    ((8, FAKE, FAKE + (1 << 30), FAKE + (1 << 31) + 4, 4096),
+    ((8, FAKE, 0, FAKE + (1 << 31), 65536), _abi.TMM_ERR_INVALID_ARG),              # out NULL
+    ((8, 0, FAKE + (1 << 30), FAKE + (1 << 31), 65536), _abi.TMM_ERR_INVALID_ARG),  # x NULL
+    ((8, FAKE, FAKE + (1 << 30), 0, 65536), _abi.TMM_ERR_INVALID_ARG),              # no workspace
+    ((8, FAKE, FAKE + (1 << 30), FAKE + (1 << 31), 65535), _abi.TMM_ERR_INVALID_ARG),  # too small
+    ((8, FAKE, FAKE + (1 << 30), FAKE + (1 << 31) + 4, 65536),
      _abi.TMM_ERR_INVALID_ARG),                                                    # ws misaligned
-    ((8, FAKE + 2, FAKE + (1 << 30), FAKE + (1 << 31), 4096),
+    ((8, FAKE + 2, FAKE + (1 << 30), FAKE + (1 << 31), 65536),
      _abi.TMM_ERR_INVALID_ARG),                                                    # x misaligned
-    ((4096, FAKE, FAKE + (1 << 30), FAKE + 64, 4096), _abi.TMM_ERR_ALIAS),         # ws inside x
+    ((65536, FAKE, FAKE + (1 << 30), FAKE + 64, 65536), _abi.TMM_ERR_ALIAS),         # ws inside x
 ])
 def test_sum_rejects_bad_arguments_without_a_launch(lib, args, status):
     assert lib.sum_f32(*args, None) == status

@@ -2,7 +2,7 @@
 against the FP64 oracle, through the C ABI.
 
 Tolerances follow from the arithmetic the header states:
-  * sum: every term passes through at most D = ceil(n / 2^20) + 28 FP32
+  * sum: every term passes through at most D = ceil(n / 2^25) + 54 FP32
     additions, so |s - S| <= D 2^-24 sum|x| (times 1.01 for higher-order
     terms); integer inputs whose partial sums stay below 2^24 are exact, so
     they must match bit for bit.
@@ -67,7 +67,7 @@ def gpu_sum(x_host, offset=0):
 
 def sum_bound(x):
     n = x.shape[0]
-    depth = math.ceil(n / 2 ** 20) + 28
+    depth = math.ceil(n / 2 ** 25) + 54
     return 1.01 * depth * 2.0 ** -24 * float(np.abs(x.astype(np.float64)).sum())
 
 

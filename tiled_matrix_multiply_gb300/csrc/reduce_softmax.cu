@@ -8,18 +8,20 @@
 // reduction one tile per block of 256-1024 threads.  Both are bound by HBM
 // bandwidth on GB300: each input value is read from HBM once.
 //
-// Array sum (sum_f32): two launches, no atomics, so the result is the same bits
-// on every call.
-//   1. sum_partials_kernel: a grid of G <= min(max(8 x SMs, 512), 1024) blocks of 512
-//      threads.  Thread g of the P = 512 G threads adds, in its four lanes, the
-//      16-byte vectors g, g + P, g + 2P, ... of the 16-byte-aligned body (four
-//      streaming loads in flight per step).  Of the at most six leading and
-//      trailing scalars outside the body, thread g < 6 takes one first.  The
-//      lanes combine pairwise, the block reduces (warp shuffles, then one
-//      value per warp through shared memory), and block b writes partials[b].
-//   2. sum_final_kernel: one block of 1024 threads reduces the G partials.
-//   Every value passes through at most ceil(n / 2^20) + 28 additions on its way
-//   to the result (P >= 2^18 whenever the grid is capped).
+// Array sum (sum_f32): two launches, and a fixed order of additions, so the
+// result is the same bits on every call.
+//   1. sum_partials_kernel: the 16-byte-aligned body is cut into G <= 16384
+//      chunks of V >= 8192 vectors (V a multiple of 2048); resident blocks of
+//      512 threads take chunks from a counter, and partials[c] receives chunk
+//      c's sum: thread t adds, in its four lanes, the chunk's vectors t,
+//      t + 512, ... (four streaming loads in flight per step), the lanes
+//      combine pairwise and the block reduces (warp shuffles, then one value
+//      per warp through shared memory).
+//   2. sum_final_kernel: one block of 1024 threads; thread t takes one of the
+//      at most six scalars outside the body (t < 6), adds partials t,
+//      t + 1024, ... in order, and the block reduces.
+//   Every value passes through at most V / 512 + ceil(G / 1024) + 22 <=
+//   ceil(n / 2^25) + 54 additions on its way to the result.
 //
 // Row softmax (softmax_rows_f32): y_{r,j} = e^{x_{r,j} - m_r} / sum_k e^{x_{r,k} - m_r}
 // with m_r the row maximum.  Rows of up to 98303 columns are read from HBM once
@@ -94,42 +96,82 @@ __device__ __forceinline__ float block_reduce(float v, float *scratch) {
 // ------------------------------------------------------------------ array sum
 
 constexpr int kSumThreads = 512;
-constexpr int kSumFinalThreads = kSumMaxPartials;   // one partial per thread
+constexpr int kSumFinalThreads = 1024;
+constexpr int kSumChunkVecsMin = 8192;     // 16-byte vectors per chunk, at least (128 KiB)
+static_assert(kSumChunkVecsMin % (4 * kSumThreads) == 0, "whole groups of four per thread");
+constexpr int kSumRegions = 16;            // calls in flight at once, at most
+__device__ unsigned long long g_sum_chunks[kSumRegions][2];   // (next chunk, blocks done)
 
+// Chunk c of the body is vectors [c V, min((c + 1) V, nvec)).  A block takes
+// its first chunk by its index and each later one from the counter (taken
+// while it sums the one before, so the counter's latency is hidden): blocks
+// that the warp schedulers favour take more chunks.  Thread t of the block
+// adds, in its four lanes, the chunk's vectors t, t + 512, ... (four loads in
+// flight per step); the lanes combine pairwise, the block reduces, and
+// partials[c] holds the chunk's sum -- the same bits whichever block took it.
 __global__ void __launch_bounds__(kSumThreads)
-sum_partials_kernel(int64_t nvec, const float4 *__restrict__ body, const float *__restrict__ x,
-                    int head, int64_t tail_at, int tail, float *__restrict__ partials) {
+sum_partials_kernel(int64_t nvec, int64_t V, int64_t G, const float4 *__restrict__ body,
+                    float *__restrict__ partials, unsigned long long *ctr) {
   __shared__ float scratch[32];
-  const int64_t P = int64_t(gridDim.x) * kSumThreads;
-  const int64_t g = int64_t(blockIdx.x) * kSumThreads + threadIdx.x;
-  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  if (g < head) acc.x = x[g];
-  else if (g < head + tail) acc.x = x[tail_at + (g - head)];
-  int64_t v = g;
-  for (; v + 3 * P < nvec; v += 4 * P) {
-    const float4 a = __ldcs(body + v);
-    const float4 b = __ldcs(body + v + P);
-    const float4 c = __ldcs(body + v + 2 * P);
-    const float4 d = __ldcs(body + v + 3 * P);
-    acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
-    acc.x += b.x; acc.y += b.y; acc.z += b.z; acc.w += b.w;
-    acc.x += c.x; acc.y += c.y; acc.z += c.z; acc.w += c.w;
-    acc.x += d.x; acc.y += d.y; acc.z += d.z; acc.w += d.w;
+  __shared__ long long s_next;
+  const int t = threadIdx.x;
+  int64_t c = blockIdx.x;
+  if (t == 0) s_next = (long long)(gridDim.x + atomicAdd(&ctr[0], 1ull));
+  __syncthreads();
+  int64_t cn = s_next;   // the chunk after c
+  while (c < G) {
+    unsigned long long tok = 0;
+    if (t == 0) tok = atomicAdd(&ctr[0], 1ull);   // the chunk after cn
+    const int64_t v0 = c * V;
+    const int64_t v1 = v0 + V < nvec ? v0 + V : nvec;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    int64_t v = v0 + t;
+    for (; v + 3 * kSumThreads < v1; v += 4 * kSumThreads) {
+      const float4 a = __ldcs(body + v);
+      const float4 b = __ldcs(body + v + kSumThreads);
+      const float4 cc = __ldcs(body + v + 2 * kSumThreads);
+      const float4 d = __ldcs(body + v + 3 * kSumThreads);
+      acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+      acc.x += b.x; acc.y += b.y; acc.z += b.z; acc.w += b.w;
+      acc.x += cc.x; acc.y += cc.y; acc.z += cc.z; acc.w += cc.w;
+      acc.x += d.x; acc.y += d.y; acc.z += d.z; acc.w += d.w;
+    }
+    for (; v < v1; v += kSumThreads) {
+      const float4 a = __ldcs(body + v);
+      acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+    }
+    const float sum = block_reduce<false>((acc.x + acc.y) + (acc.z + acc.w), scratch);
+    if (t == 0) {
+      partials[c] = sum;
+      s_next = (long long)(gridDim.x + tok);
+    }
+    __syncthreads();
+    c = cn;
+    cn = s_next;
+    __syncthreads();   // every thread has read s_next before it is rewritten
   }
-  for (; v < nvec; v += P) {
-    const float4 a = __ldcs(body + v);
-    acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+  if (t == 0 && atomicAdd(&ctr[1], 1ull) == gridDim.x - 1ull) {
+    // The last block done: every fetch has happened, so reset for the next call.
+    ctr[0] = 0;
+    ctr[1] = 0;
+    __threadfence();
   }
-  const float s = block_reduce<false>((acc.x + acc.y) + (acc.z + acc.w), scratch);
-  if (threadIdx.x == 0) partials[blockIdx.x] = s;
 }
 
+// Thread t adds the at most six scalars outside the body (thread t < head +
+// tail takes one) and then partials t, t + 1024, ... in order; the block
+// reduces (warp shuffles, then one value per warp through shared memory).
 __global__ void __launch_bounds__(kSumFinalThreads)
-sum_final_kernel(int G, const float *__restrict__ partials, float *__restrict__ out) {
+sum_final_kernel(int64_t G, const float *__restrict__ partials, const float *__restrict__ x,
+                 int head, int64_t tail_at, int tail, float *__restrict__ out) {
   __shared__ float scratch[32];
-  const float v = int(threadIdx.x) < G ? partials[threadIdx.x] : 0.0f;
+  const int t = threadIdx.x;
+  float v = 0.0f;
+  if (t < head) v = x[t];
+  else if (t < head + tail) v = x[tail_at + (t - head)];
+  for (int64_t k = t; k < G; k += kSumFinalThreads) v += partials[k];
   const float s = block_reduce<false>(v, scratch);
-  if (threadIdx.x == 0) *out = s;
+  if (t == 0) *out = s;
 }
 
 // ------------------------------------------------------------------ softmax
@@ -934,13 +976,17 @@ void softmax_set_test_hooks(int drop_block, int64_t wait_limit_ns) {
                            std::memory_order_relaxed);
 }
 
-int64_t sum_grid_blocks(int64_t n, const DeviceInfo &dev) {
-  const int64_t per_block = int64_t(kSumThreads) * 4 * 4;   // four vectors per thread
-  // 8 blocks per SM (at most kSumFinalThreads partials): measured 1 % over 4.
-  const int64_t cap = std::max<int64_t>(int64_t(dev.sm_count) * 8, 512);
-  return std::max<int64_t>(1, std::min<int64_t>((n + per_block - 1) / per_block,
-                                                std::min<int64_t>(cap, kSumFinalThreads)));
+// Chunk length (a multiple of 4 x kSumThreads vectors) and count for nvec vectors.
+void sum_chunks(int64_t nvec, int64_t *V, int64_t *G) {
+  constexpr int64_t kGroup = 4 * kSumThreads;
+  int64_t v = (nvec + kSumMaxPartials - 1) / kSumMaxPartials;
+  v = v > kSumChunkVecsMin ? v : kSumChunkVecsMin;
+  v = (v + kGroup - 1) / kGroup * kGroup;
+  *V = v;
+  *G = (nvec + v - 1) / v;
 }
+
+std::atomic<unsigned int> g_sum_epoch{0};
 
 cudaError_t launch_sum(int64_t n, const float *x, float *out, float *partials,
                        const DeviceInfo &dev, cudaStream_t stream) {
@@ -950,12 +996,33 @@ cudaError_t launch_sum(int64_t n, const float *x, float *out, float *partials,
   const int64_t nvec = (n - head) >> 2;
   const int64_t tail_at = head + 4 * nvec;
   const int tail = int(n - tail_at);
-  const int G = int(sum_grid_blocks(n, dev));
-  sum_partials_kernel<<<G, kSumThreads, 0, stream>>>(
-      nvec, reinterpret_cast<const float4 *>(x + head), x, int(head), tail_at, tail, partials);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  sum_final_kernel<<<1, kSumFinalThreads, 0, stream>>>(G, partials, out);
+  int64_t V = 0, G = 0;
+  sum_chunks(nvec, &V, &G);
+  if (G > 0) {
+    static KernelSetup st;
+    static std::atomic<int> blocks_per_sm[64];
+    const uint64_t bit = uint64_t(1) << (dev.id & 63);
+    if (!(st.configured.load(std::memory_order_acquire) & bit)) {
+      int nb = 0;
+      cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, sum_partials_kernel,
+                                                                    kSumThreads, 0);
+      if (e != cudaSuccess) return e;
+      blocks_per_sm[dev.id & 63].store(nb > 0 ? nb : 1, std::memory_order_relaxed);
+      st.configured.fetch_or(bit, std::memory_order_release);
+    }
+    const int64_t grid = std::min<int64_t>(
+        G, int64_t(blocks_per_sm[dev.id & 63].load(std::memory_order_relaxed)) * dev.sm_count);
+    unsigned long long *ctr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&ctr), g_sum_chunks);
+    if (e != cudaSuccess) return e;
+    ctr += 2 * (g_sum_epoch.fetch_add(1, std::memory_order_relaxed) % kSumRegions);
+    sum_partials_kernel<<<unsigned(grid), kSumThreads, 0, stream>>>(
+        nvec, V, G, reinterpret_cast<const float4 *>(x + head), partials, ctr);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  sum_final_kernel<<<1, kSumFinalThreads, 0, stream>>>(G, partials, x, int(head), tail_at, tail,
+                                                       out);
   return cudaGetLastError();
 }
 

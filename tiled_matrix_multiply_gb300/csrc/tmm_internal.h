@@ -62,10 +62,9 @@ cudaError_t simt_device_status(unsigned int *status, bool clear);
 // Testing hooks of the tiled kernel's stream-K waits (see tmm_gemm.h).
 void simt_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns);
 
-// Array sum: a first launch writes one partial per block (at most
+// Array sum: a first launch writes one partial per chunk of the input (at most
 // kSumMaxPartials, in a caller-supplied workspace), a second adds them.
-constexpr int kSumMaxPartials = 1024;
-int64_t sum_grid_blocks(int64_t n, const DeviceInfo &dev);
+constexpr int kSumMaxPartials = 16384;
 cudaError_t launch_sum(int64_t n, const float *x, float *out, float *partials,
                        const DeviceInfo &dev, cudaStream_t stream);
 
