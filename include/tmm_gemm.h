@@ -249,8 +249,9 @@ int tmm_testing_set_wait_hooks(int drop_signal_block, int64_t wait_limit_ns);
  * must not overlap (TMM_ERR_ALIAS).  1 <= W <= 129, 0 <= n <= 2^40 (n == 0
  * is a no-op).  Each block stages its tile of inputs plus the W - 1 halo in
  * shared memory once (the page's cooperative loading); each sum starts from
- * 0 and adds the window in ascending d in FP32, the page's order.
- * Asynchronous on `stream`; no allocation.
+ * 0 and adds the window in ascending d in FP32, the page's order.  Blocks
+ * take tiles from a library-owned counter, so at most 16 calls may be in
+ * flight at once.  Asynchronous on `stream`; no allocation.
  */
 int window_sum_f32(int64_t n, int W, const float *x, float *y, tmm_stream_t stream);
 
@@ -294,7 +295,8 @@ size_t sum_f32_workspace_size(int64_t n);
  * rows are shared by several blocks that meet through library-owned global
  * memory with a bounded wait (see tmm_check_device), and are read twice, a
  * running (maximum, sum) pass and the normalise pass, the second read from L2.
- * Up to 16 calls with such rows may be in flight at once.
+ * Blocks take rows from library-owned counters (and share long rows through
+ * library-owned memory), so at most 16 calls may be in flight at once.
  * FP32 throughout: exp by CUDA's expf, the sum in a fixed order, the
  * normalisation as a product with fl(1 / s) (in a cluster, with
  * fl(e^{m_c - m} / s) for the chunk maximum m_c).  A row whose maximum is +inf, or
