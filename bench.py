@@ -592,7 +592,7 @@ def window_leg(args, flush, stream, peaks) -> dict:
 
 
 SOFTMAX_COLS = 4096
-GRID_ROW_COLS = 98304   # rows this long or longer run softmax_grid_kernel
+GRID_ROW_COLS = 65537   # rows this long or longer run softmax_grid_kernel
 
 
 def _hbm_roofline(gbs, peaks, nbytes, what, traffic=None):

@@ -218,7 +218,7 @@ int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K,
  * bounded wait inside gemm_f32 (between the blocks sharing a split tile),
  * gemm_f32_tc3 (between the copy, tensor-core and epilogue roles of a block
  * or block pair), window_sum_f32 (for a tile's bulk copy) or softmax_rows_f32
- * (between the blocks sharing a row of 98304 or more columns) ran out of time
+ * (between the blocks sharing a row of more than 65536 columns) ran out of time
  * since the last check; results written since then are not valid.  The pages have no counterpart: this is the library's failure
  * detection ("CMU DLSys Lecture 12" section 2 only asks that API and launch
  * errors be checked).  TMM_ERR_CUDA if the synchronisation itself failed.
@@ -233,7 +233,7 @@ int tmm_check_device(tmm_stream_t stream);
  * waiting on it runs into the time limit, and makes that block of later window_sum_f32
  * launches (16-byte-aligned x) wait for 16 bytes more than its first tile
  * copy brings, and that block of later softmax_rows_f32 launches on rows of
- * 98304 or more columns skip counting itself in;
+ * more than 65536 columns skip counting itself in;
  * wait_limit_ns > 0 sets the limit of every bounded wait of these kernels
  * (default, and for values <= 0, 10 s).
  * Process-wide; pass (-1, 0) to restore the defaults.  Always TMM_OK.
@@ -289,7 +289,7 @@ size_t sum_f32_workspace_size(int64_t n);
  * 4 select vector loads).  y may be x with ldy == ldx (in place); any other
  * overlap is TMM_ERR_ALIAS.  0 <= cols < 2^31; rows == 0 or cols == 0 is a
  * no-op.  Rows of up to 2048 columns are held in registers, up to 16384
- * columns staged in one block's shared memory, up to 98303 columns split over
+ * columns staged in one block's shared memory, up to 65536 columns split over
  * a thread-block cluster whose blocks combine their partial maxima and sums
  * through distributed shared memory (each row read from HBM once); longer
  * rows are shared by several blocks that meet through library-owned global

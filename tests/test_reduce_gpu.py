@@ -12,8 +12,8 @@ Tolerances follow from the arithmetic the header states:
     by their shares Y_k), 1/s and the product one each, so to first order
     |y_j - Y_j| <= (|t_j| + 4 + sum_k Y_k (|t_k| + 4) + ceil(cols/32) + 18) 2^-24 Y_j
                    + 2^-146
-    (the last term for results in the subnormal range).  Rows of 98304 columns
-    or more keep running sums: each rise of a thread's maximum costs one expf
+    (the last term for results in the subnormal range).  Rows of more than
+    65536 columns keep running sums: each rise of a thread's maximum costs one expf
     and one product (at most cols / (4 * 512 * G) of them per thread, G >= 3
     blocks per row), well inside the ceil(cols/32) additions allowed.
 """
@@ -161,8 +161,8 @@ def logits(rows, cols, seed, scale=4.0):
 
 
 COLS = [1, 2, 31, 32, 33, 64, 100, 128, 255, 256, 511, 512, 1000, 1024, 1025, 2047, 2048, 2049,
-        4096, 8191, 8192, 8193, 16384, 16385, 24577, 32768, 49152, 49153, 65536, 100003,
-        131072, 131073, 262144, 786432, 800000]
+        4096, 8191, 8192, 8193, 16384, 16385, 24577, 32768, 49152, 49153, 65536, 65537, 65540,
+        81920, 100003, 131072, 131073, 262144, 786432, 800000]
 
 
 def rows_for(cols):
@@ -262,7 +262,7 @@ def test_python_wrappers():
 
 @pytest.mark.parametrize("rows,cols", [(64, 98304), (64, 300000), (4, 4194304)])
 def test_softmax_grid_wait_timeout_is_reported_and_recovers(rows, cols):
-    # Rows of 98304 columns or more are shared by several blocks that meet
+    # Rows of more than 65536 columns are shared by several blocks that meet
     # through a counter in global memory (3 blocks per row; 10; 128).  Block 1
     # never counts itself in, so the other blocks of its row run into the
     # (2 ms) limit.

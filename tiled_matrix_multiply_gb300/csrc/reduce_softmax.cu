@@ -24,7 +24,7 @@
 //   ceil(n / 2^25) + 54 additions on its way to the result.
 //
 // Row softmax (softmax_rows_f32): y_{r,j} = e^{x_{r,j} - m_r} / sum_k e^{x_{r,k} - m_r}
-// with m_r the row maximum.  Rows of up to 98303 columns are read from HBM once
+// with m_r the row maximum.  Rows of up to 65536 columns are read from HBM once
 // and written once; what holds them on chip between the two passes depends on
 // their length:
 //   * up to 2048 columns (rows on 16-byte boundaries, cols % 4 == 0; 1024
@@ -36,7 +36,7 @@
 //     flight while this one is reduced; pass 1 takes the maximum, pass 2
 //     replaces each staged value by e^{x - m} and sums them, and the stores
 //     scale by 1 / s.
-//   * up to 98303 columns: a cluster of 2-8 blocks per row, each staging one
+//   * up to 65536 columns: a cluster of 2-8 blocks per row, each staging one
 //     chunk, the partial maxima and sums combined through distributed shared
 //     memory (softmax_staged_kernel describes the exchange).
 //   * longer rows: G blocks per row of a cooperative grid, meeting through
@@ -46,7 +46,7 @@
 // Arithmetic: t = fl(x - m), e = expf(t) (CUDA's, within 2 ulp), s summed in
 // FP32 in a fixed order (each thread in ascending column order, then a shuffle
 // tree, then the cluster's chunks in rank order), y = e * fl(1 / s) (in a
-// cluster, e^{x - m_c} * fl(e^{m_c - m} / s)).  Past 98303 columns the sum is
+// cluster, e^{x - m_c} * fl(e^{m_c - m} / s)).  Past 65536 columns the sum is
 // a running one (each rise of a thread's maximum rescales its sum, one more
 // product and one more expf), and the G parts merge in a fixed order.
 // y may be x itself (in place): every row (chunk) is read completely before
@@ -887,7 +887,7 @@ cudaError_t launch_staged_any(int64_t rows, int cols, const StagePlan &plan, con
 
 // Rows from this length on take softmax_grid_kernel (measured on GB300: from
 // here on it beats a cluster staging the row; below, staging wins).
-constexpr int kGridRowCols = 98304;
+constexpr int kGridRowCols = 65537;
 
 template <bool kVec>
 cudaError_t launch_grid_rows(int64_t rows, int cols, const float *x, int64_t ldx, float *y,
