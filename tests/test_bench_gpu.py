@@ -67,8 +67,10 @@ def test_extra_legs(line):
     t = line["tc3"]
     assert t["unit"] == "TFLOP/s" and t["roofline"]["bound"] == "tensor" and t["value"] > 0
     for leg in ("window5", "sum", "softmax"):
+        # 2^22 floats here: written lines may still sit in L2 when a step ends, so the
+        # fraction of the copy bandwidth can read above 1; far above means no work.
         r = line[leg]["roofline"]
-        assert r["bound"] == "hbm" and r["unit"] == "GB/s" and 0.05 < r["frac"] < 1.2, leg
+        assert r["bound"] == "hbm" and r["unit"] == "GB/s" and 0.05 < r["frac"] < 1.6, leg
     for lay in ("tn", "nt", "tt"):
         assert line["layouts"][lay]["gemm_f32_ex"]["value"] > 0
         assert line["layouts"][lay]["gemm_f32_tc3_ex"]["value"] > 0
