@@ -96,6 +96,27 @@ def test_layouts_padded_and_unaligned(entry, ta, tb, pad, off):
     parity.assert_close(C, oracle.gemm(A, B), K, f"{entry} ta={ta} tb={tb} pad={pad} off={off}")
 
 
+@pytest.mark.parametrize("ta,tb", TRANS)
+@pytest.mark.parametrize("shape", [(130, 515, 45), (700, 1030, 333)])
+def test_simt_rows_at_every_alignment(ta, tb, shape):
+    # Rows of A (stored K x M) and B (stored K x N) that start at each 4-byte
+    # position inside a 16-byte line: every base offset mod 4 against every
+    # leading dimension mod 4, over several tiles in each direction and a
+    # ragged K.  Integer inputs, so the products are exact; the canary NaNs
+    # around each matrix reach C if any element outside the matrix is read
+    # into a sum.
+    M, N, K = shape
+    rng = np.random.default_rng(73)
+    A = rng.integers(-8, 9, (M, K)).astype(np.float32)
+    B = rng.integers(-8, 9, (K, N)).astype(np.float32)
+    want = oracle.gemm(A, B)
+    for off, pad in itertools.product(range(4), range(4)):
+        o = (off, (off + 2) % 4, 0)
+        d = (pad, (pad + 1) % 4, 0)
+        C = run_layout("gemm_f32_ex", ta, tb, A, B, d, o)
+        parity.assert_bit_exact(C, want, f"ta={ta} tb={tb} {shape} off={o} pad={d}")
+
+
 @pytest.mark.parametrize("entry", ENTRIES)
 @pytest.mark.parametrize("ta,tb", [(1, 0), (0, 1), (1, 1)])
 def test_headline_size_transposed(entry, ta, tb):
