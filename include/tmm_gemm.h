@@ -24,8 +24,14 @@
  *   A, B         DEVICE pointers (cudaMalloc'd or any device-accessible
  *                memory of the current device) to FP32 row-major operands.
  *                Caller-owned; read only.  Pointers must be 4-byte aligned
- *                (natural float alignment); 16-byte aligned bases with lda,
- *                ldb, K and N multiples of 4 take the vectorised load path.
+ *                (natural float alignment).  Rows that all start on 16-byte
+ *                boundaries (16-byte aligned base, leading dimension a
+ *                multiple of 4) are faster: on the FFMA path B stored K x N
+ *                (and A stored K x M) is then read in 16-byte vectors, else
+ *                element by element, which costs about a fifth of
+ *                gemm_f32's throughput when B's rows are unaligned; on the
+ *                tensor-core path an operand stored K-major is then read in
+ *                place as its own TF32 high part.
  *   lda, ldb     leading dimensions in elements: lda >= max(1, K),
  *                ldb >= max(1, N).
  *   C            DEVICE pointer to the FP32 row-major result, caller-owned,

@@ -1,7 +1,7 @@
 // gemm_simt.cu -- two-level tiled FP32 product on the CUDA cores (FFMA).
 //
 // Tiling ("Tiling Strategies" sections 2-4, "CMU DLSys Lecture 12" section 5):
-//   * block tile: each block owns a BM x BN tile of C (128 x 128 with four
+//   * block tile: each block owns a BM x BN tile of C (64 x 256 with 1 x 4
 //     warps in the default configuration; two blocks resident per SM);
 //   * K-slices of BK flow through a ring of kStages shared-memory stages
 //     filled by asynchronous copies (cp.async).  This generalises the double
@@ -15,11 +15,14 @@
 //     prefetching", "Reducing Overhead Slots").
 //
 // Shared-memory layout.  The A slab is stored transposed, a[k][m], so a
-// thread's rows of A at one k are 16-byte vectors; it is filled by 4-byte
-// copies, each warp copying 4 rows x 8 consecutive k (four 32-byte global
-// sectors) into 32 distinct banks (row length BM + 4 floats).  The B slab
-// keeps its global layout b[k][n] and is filled by 16-byte copies of whole
-// row segments when B is 16-byte aligned (4-byte copies otherwise).
+// thread's rows of A at one k are 16-byte vectors; from A stored M x K it is
+// filled by 4-byte copies, each warp copying 4 rows x 8 consecutive k (four
+// 32-byte global sectors) into 32 distinct banks (row length BM + 4 floats).
+// The B slab keeps B's layout b[k][n] and is filled by 16-byte copies of
+// whole row segments when every row of B starts on a 16-byte boundary
+// (4-byte copies otherwise).  The layouts that read A stored K x M or B
+// stored N x K use the same copies with the roles exchanged (see the copy
+// kinds below).
 //
 // Warp tiling ("Tiling Hierarchy on GPUs", "Warp Tiling"): the 32 lanes of a
 // warp form an LM x LN grid (4 x 8 or 8 x 4); lane (lm, ln) owns rows
