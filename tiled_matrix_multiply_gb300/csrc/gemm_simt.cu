@@ -439,7 +439,8 @@ struct SimtBlock {
     float *c_base = p.C + int64_t(row0) * p.ldc + col0;
     // kAdd: the partial sums of kAddRows rows are all loaded before the first
     // store, so the loads are in flight together (a store before a load of the
-    // same array would order them one after another).
+    // same array would order them one after another) -- element by element
+    // when C takes no 16-byte stores.
     constexpr int kAddRows = 4;
     static_assert(Cf::TM % kAddRows == 0, "whole row groups");
 #pragma unroll
@@ -460,6 +461,23 @@ struct SimtBlock {
           for (int c = 0; c < Cf::TN / 4; ++c)
             if (col0 + 4 * Cf::LN * c < p.N)
               w[i][c] = __ldcg(reinterpret_cast<const float4 *>(c_row + 4 * Cf::LN * c));
+        }
+      } else if (kAdd) {
+#pragma unroll
+        for (int i = 0; i < kAddRows; ++i) {
+          const int r = r0 + i;
+          const int dr = 4 * Cf::LM * (r / 4) + r % 4;
+          if (row0 + dr >= p.M) continue;
+          const float *c_row = c_base + int64_t(dr) * p.ldc;
+#pragma unroll
+          for (int c = 0; c < Cf::TN / 4; ++c) {
+            const int dc = 4 * Cf::LN * c;
+            const int left = p.N - (col0 + dc);
+            w[i][c].x = left > 0 ? __ldcg(c_row + dc + 0) : 0.f;
+            w[i][c].y = left > 1 ? __ldcg(c_row + dc + 1) : 0.f;
+            w[i][c].z = left > 2 ? __ldcg(c_row + dc + 2) : 0.f;
+            w[i][c].w = left > 3 ? __ldcg(c_row + dc + 3) : 0.f;
+          }
         }
       }
 #pragma unroll
@@ -484,11 +502,12 @@ struct SimtBlock {
               *reinterpret_cast<float4 *>(c_row + dc) = v;
             }
           } else {
+            const float wv[4] = {w[i][c].x, w[i][c].y, w[i][c].z, w[i][c].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               if (col0 + dc + j < p.N) {
                 float v = a[4 * c + j];
-                if (kAdd) v = __ldcg(c_row + dc + j) + v;
+                if (kAdd) v = wv[j] + v;
                 c_row[dc + j] = v;
               }
           }
@@ -574,6 +593,13 @@ using DefaultConfig = SimtConfig<8, 16, 1, 4, 16, 4, 2>;
 // directly (A stored K x M), 128 x 128 when both operands are transposed.
 using WideMConfig = SimtConfig<8, 16, 4, 1, 16, 4, 2>;
 using SquareConfig = SimtConfig<8, 16, 2, 2, 16, 4, 2>;
+// B rows that do not start on 16-byte boundaries are copied element by
+// element, and those copies limit the default tile (32 of a thread's 40 copies
+// per K-slice).  A 128 x 256 tile with 2 x 4 warps gives each thread the same
+// products for 8 copies of A and 16 of B; at 232 registers one block fits per
+// SM, and 3 stages measured best (4000 x 3001 x 2047: 48.4 TFLOP/s against
+// 45.6; 4096 x 4095 x 4096: 54.5 against 50.0).
+using UnalignedBConfig = SimtConfig<8, 16, 2, 4, 16, 3, 1>;
 
 struct LaunchState {
   std::atomic<uint64_t> configured{0};   // bit per device: smem opt-in done
@@ -679,16 +705,16 @@ cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_
     if (p.transb)
       return launch_variant<SquareConfig, kCopyTransposing, kCopyTransposing>(p, dev, stream);
     return vec_b ? launch_variant<Cf, kCopyTransposing, kCopyVec>(p, dev, stream)
-                 : launch_variant<Cf, kCopyTransposing, kCopyScalar>(p, dev, stream);
+                 : launch_variant<UnalignedBConfig, kCopyTransposing, kCopyScalar>(p, dev, stream);
   }
   if (p.transb)
     return vec_a ? launch_variant<WideMConfig, kCopyVec, kCopyTransposing>(p, dev, stream)
                  : launch_variant<WideMConfig, kCopyScalar, kCopyTransposing>(p, dev, stream);
   if (vec_a)
     return vec_b ? launch_variant<Cf, kCopyVec, kCopyVec>(p, dev, stream)
-                 : launch_variant<Cf, kCopyVec, kCopyScalar>(p, dev, stream);
+                 : launch_variant<UnalignedBConfig, kCopyVec, kCopyScalar>(p, dev, stream);
   return vec_b ? launch_variant<Cf, kCopyScalar, kCopyVec>(p, dev, stream)
-               : launch_variant<Cf, kCopyScalar, kCopyScalar>(p, dev, stream);
+               : launch_variant<UnalignedBConfig, kCopyScalar, kCopyScalar>(p, dev, stream);
 }
 
 cudaError_t simt_device_status(unsigned int *status, bool clear) {
