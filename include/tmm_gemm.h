@@ -28,8 +28,9 @@
  *                boundaries (16-byte aligned base, leading dimension a
  *                multiple of 4) are faster: on the FFMA path B stored K x N
  *                (and A stored K x M) is then read in 16-byte vectors, else
- *                element by element, which costs about a fifth of
- *                gemm_f32's throughput when B's rows are unaligned; on the
+ *                element by element, which costs about an eighth of
+ *                gemm_f32's throughput when B's rows are unaligned
+ *                (4096 x 4095 x 4096: 55 against 63.7 TFLOP/s); on the
  *                tensor-core path an operand stored K-major is then read in
  *                place as its own TF32 high part.
  *   lda, ldb     leading dimensions in elements: lda >= max(1, K),
