@@ -28,9 +28,8 @@
  *                boundaries (16-byte aligned base, leading dimension a
  *                multiple of 4) are faster: on the FFMA path B stored K x N
  *                (and A stored K x M) is then read in 16-byte vectors, else
- *                element by element, which costs about an eighth of
- *                gemm_f32's throughput when B's rows are unaligned
- *                (4096 x 4095 x 4096: 55 against 63.7 TFLOP/s); on the
+ *                element by element, which costs gemm_f32 a noticeable part
+ *                of its throughput when B's rows are unaligned; on the
  *                tensor-core path an operand stored K-major is then read in
  *                place as its own TF32 high part.
  *   lda, ldb     leading dimensions in elements: lda >= max(1, K),
@@ -80,17 +79,27 @@ typedef struct CUstream_st *tmm_stream_t;
  * time, and results written since the last check are not valid. */
 #define TMM_ERR_DEVICE_TIMEOUT (-5)
 
+/* The same status codes under the names of the product's boundary contract
+ * (GEMM_ERR_*); each equals its TMM_ERR_* counterpart. */
+#define GEMM_OK TMM_OK
+#define GEMM_ERR_INVALID_ARG TMM_ERR_INVALID_ARG
+#define GEMM_ERR_ALIAS TMM_ERR_ALIAS
+#define GEMM_ERR_UNSUPPORTED_DEVICE TMM_ERR_UNSUPPORTED_DEVICE
+#define GEMM_ERR_CUDA TMM_ERR_CUDA
+#define GEMM_ERR_DEVICE_TIMEOUT TMM_ERR_DEVICE_TIMEOUT
+
 /*
  * gemm_f32 -- the tiled FP32 product on the CUDA cores (FFMA, IEEE single
  * precision, one rounding per multiply-add).
  *
  * Follows the two-level tiling of "Tiling Strategies" sections 2-4 and "CMU
  * DLSys Lecture 12" section 5: each thread block owns one block tile of C,
- * stages K-slices of A and B in shared memory (double buffered, as in
- * "Tiling Strategies" section 3), and each thread accumulates an 8 x 8 tile
- * of C in registers as a sequence of outer products ("Tiling Hierarchy on
- * GPUs", sections "Register Tiling" and "Register prefetching").  Tail tiles
- * are handled with zero-filled masked loads and masked stores (DLSys section 5).
+ * stages K-slices of A and B in shared memory (a multi-stage ring, the
+ * double buffer of "Tiling Strategies" section 3 made deeper), and each
+ * thread accumulates a tile of C in registers as a sequence of outer products
+ * ("Tiling Hierarchy on GPUs", sections "Register Tiling" and "Register
+ * prefetching").  Tail tiles are handled with zero-filled masked loads and
+ * masked stores (DLSys section 5).
  *
  * When the tile count leaves the last wave of blocks partly empty, the call
  * runs persistent and cooperative (one block per resident slot) and splits
@@ -162,9 +171,18 @@ int gemm_f32_naive(int64_t M, int64_t N, int64_t K,
  *                    split operands (its contents are scratch, not preserved);
  *                    it must not overlap A, B or C.
  *   workspace_bytes  its size.
- * TMM_ERR_INVALID_ARG if the workspace is missing, short or misaligned,
- * TMM_ERR_ALIAS if it overlaps an operand.  Calls sharing one workspace must
- * not overlap on the GPU.
+ * TMM_ERR_INVALID_ARG if the workspace is missing, short or misaligned (or
+ * its size does not fit in size_t), TMM_ERR_ALIAS if it overlaps an operand.
+ * Calls sharing one workspace must not overlap on the GPU.
+ *
+ * Ordering assumption: the K-parts of a split tile are consecutive work items,
+ * and a part only ever waits (bounded) for a part that was scheduled before
+ * it.  The product kernel is not a cooperative launch, so this relies on the
+ * GPU starting a grid's blocks in block order, which CUDA does in practice but
+ * does not guarantee.  Should the blocks start out of order (for example with
+ * other kernels holding SMs), a wait can run into its time limit; the call
+ * then reports TMM_ERR_DEVICE_TIMEOUT through tmm_check_device instead of
+ * hanging.  As for gemm_f32, up to 16 calls may be in flight at once.
  */
 int gemm_f32_tc3(int64_t M, int64_t N, int64_t K,
                  const float *A, int64_t lda,
@@ -185,8 +203,9 @@ int gemm_f32_tc3_ex(int transa, int transb,
                     tmm_stream_t stream);
 
 /* Workspace bytes gemm_f32_tc3 needs for an M x N x K product (0 for an empty
- * product or sizes out of range):  4 Kp (2M + 2N) rounded to 256-byte
- * sections, Kp = K rounded up to a multiple of 32. */
+ * product or sizes out of range; SIZE_MAX when the count does not fit in
+ * size_t):  4 Kp (2M + 2N) rounded to 256-byte sections, Kp = K rounded up to
+ * a multiple of 32. */
 size_t gemm_f32_tc3_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -204,10 +223,12 @@ size_t gemm_f32_tc3_workspace_size(int64_t M, int64_t N, int64_t K);
  *     holds it until the process exits;
  *   - products needing more than that (gemm_f32_tc3_workspace_size(M, N, K)
  *     > TMM_TC3_NOALLOC_SCRATCH_BYTES, for example beyond about 2048^3) are
- *     rejected with TMM_ERR_INVALID_ARG and a message naming the sizes;
- *   - the first call on each device looks up the scratch's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture;
+ *     rejected with TMM_ERR_INVALID_ARG and a message naming the sizes,
+ *     before any CUDA call;
+ *   - every call looks up the scratch's address on the current device
+ *     (cudaGetSymbolAddress), so the address always belongs to the current
+ *     context; the first call on a device may be the one that loads the
+ *     library's device code there, so make it before any stream capture;
  *   - every call on a device uses the same scratch and leaves its contents
  *     behind; calls that overlap on the GPU (for example on two streams) race
  *     on it and must be serialised by the caller.
@@ -316,6 +337,13 @@ int softmax_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx, fl
 /* One-line description of the calling thread's last failed call ("" if none).
  * The string is owned by the library and valid until the thread's next call. */
 const char *tmm_last_error_string(void);
+
+/* The names the product's boundary contract gives these two calls:
+ * gemm_last_error_string is tmm_last_error_string, gemm_check_status is
+ * tmm_check_device (same arguments, same results).  "CMU DLSys Lecture 12"
+ * section 2: production code checks API and launch errors. */
+const char *gemm_last_error_string(void);
+int gemm_check_status(tmm_stream_t stream);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int tmm_version(void);

@@ -153,3 +153,90 @@ def test_softmax_rejects_bad_arguments_without_a_launch(lib, args, status):
 def test_softmax_empty_shapes_need_no_device(lib):
     assert lib.softmax_rows_f32(0, 8, FAKE, 8, FAKE + 64, 8, None) == _abi.TMM_OK
     assert lib.softmax_rows_f32(8, 0, FAKE, 1, FAKE, 1, None) == _abi.TMM_OK
+
+
+def _header_macros():
+    text = open(os.path.join(ROOT, "include", "tmm_gemm.h")).read()
+    return dict(re.findall(r"^#define\s+(\w+)\s+(.+?)\s*$", text, flags=re.M))
+
+
+def _macro_value(macros, name):
+    v = macros[name]
+    while v in macros:          # an alias of another macro
+        v = macros[v]
+    return int(v.strip("()"))
+
+
+def test_boundary_contract_names_alias_the_library_names(lib):
+    # Status codes: GEMM_ERR_* in the header equal the TMM_ERR_* codes, and the
+    # binding carries both names.
+    macros = _header_macros()
+    for suffix in ("INVALID_ARG", "ALIAS", "UNSUPPORTED_DEVICE", "CUDA", "DEVICE_TIMEOUT"):
+        g, t = _macro_value(macros, "GEMM_ERR_" + suffix), _macro_value(macros, "TMM_ERR_" + suffix)
+        assert g == t == getattr(_abi, "GEMM_ERR_" + suffix) == getattr(_abi, "TMM_ERR_" + suffix)
+    assert _macro_value(macros, "GEMM_OK") == _abi.TMM_OK == 0
+    # The error string: both names read the calling thread's last failure.
+    assert lib.gemm_f32(-1, 4, 4, FAKE, 4, FAKE, 4, FAKE + (1 << 20), 4, None) \
+        == _abi.GEMM_ERR_INVALID_ARG
+    msg = lib.gemm_last_error_string().decode()
+    assert msg and msg == lib.tmm_last_error_string().decode()
+    assert "negative size" in msg
+
+
+SCRATCH = 64 << 20      # TMM_TC3_NOALLOC_SCRATCH_BYTES
+
+
+def test_noalloc_scratch_constant_matches_header():
+    macros = _header_macros()
+    assert macros["TMM_TC3_NOALLOC_SCRATCH_BYTES"] == "((size_t)64 << 20)"
+
+
+def test_tc3_workspace_size_formula_and_overflow(lib):
+    # 4 Kp (2M + 2N) in 256-byte sections, Kp = K rounded up to 32.
+    assert lib.gemm_f32_tc3_workspace_size(2048, 2048, 2048) == SCRATCH
+    assert lib.gemm_f32_tc3_workspace_size(3, 5, 1) == 2 * 512 + 2 * 768   # 384 -> 512, 640 -> 768
+    assert lib.gemm_f32_tc3_workspace_size(0, 5, 7) == 0
+    assert lib.gemm_f32_tc3_workspace_size(5, 5, 1 << 31) == 0       # K out of range
+    # The largest sizes: 4 * 2^31 * (4 (2^31 - 1)) bytes does not fit in size_t.
+    big = (1 << 31) - 1
+    assert lib.gemm_f32_tc3_workspace_size(big, big, big) == 2 ** 64 - 1
+
+
+def test_noalloc_scratch_limit_boundary(lib):
+    # 2048^3 needs exactly the scratch; every K that rounds to the next 32 needs more.
+    assert lib.gemm_f32_tc3_workspace_size(2048, 2048, 2048) <= SCRATCH
+    for K in (2049, 2080):
+        assert lib.gemm_f32_tc3_workspace_size(2048, 2048, K) > SCRATCH
+    assert lib.gemm_f32_tc3_workspace_size(2048, 2049, 2048) > SCRATCH
+    assert lib.gemm_f32_tc3_workspace_size(3072, 1024, 2048) == SCRATCH
+
+
+def _no_cuda_device():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except ImportError:
+        return True
+
+
+@pytest.mark.skipif(not _no_cuda_device(),
+                    reason="placeholder pointers are only passed where no GPU exists")
+@pytest.mark.parametrize("shape", [(2048, 2048, 2049), (4096, 4096, 4096), (2048, 2049, 2048)])
+def test_noalloc_refuses_oversized_products_before_any_cuda_call(lib, shape):
+    # Refused on the size alone: on a machine without a GPU any CUDA call would
+    # fail with TMM_ERR_CUDA instead, so this status shows that none was made.
+    M, N, K = shape
+    rc = lib.gemm_f32_tc3_noalloc(M, N, K, FAKE, K, FAKE + (1 << 36), N, FAKE + (1 << 37), N,
+                                  None)
+    assert rc == _abi.TMM_ERR_INVALID_ARG
+    assert "scratch" in lib.tmm_last_error_string().decode()
+
+
+@pytest.mark.skipif(not _no_cuda_device(),
+                    reason="placeholder pointers are only passed where no GPU exists")
+def test_tc3_refuses_unrepresentable_workspace(lib):
+    big = (1 << 31) - 1
+    rc = lib.gemm_f32_tc3(big, big, big, FAKE, big, FAKE + (1 << 62), big, FAKE + (1 << 63), big,
+                          FAKE, 2 ** 64 - 1, None)
+    # Either the extent check or the workspace-size check refuses it, before any CUDA call.
+    assert rc == _abi.TMM_ERR_INVALID_ARG

@@ -92,11 +92,12 @@ def _freivalds(A, B, C, x):
     return lhs, rhs
 
 
+@pytest.mark.parametrize("entry", ENTRIES)
 @pytest.mark.parametrize("name", LARGE)
-def test_large_workload_sampled_and_freivalds(name):
+def test_large_workload_sampled_and_freivalds(entry, name):
     w = inputs.WORKLOADS[name]
     A, B = inputs.workload_operands(w)
-    C = _run("gemm_f32", A, B, check_canaries=False)
+    C = _run(entry, A, B, check_canaries=False)
     ii, jj = _sample_indices(w.M, w.N, 4096, 7)
     ref = oracle.gemm_entries(A, B, ii, jj)
     got = C[ii, jj]
@@ -108,14 +109,15 @@ def test_large_workload_sampled_and_freivalds(name):
     assert np.linalg.norm(lhs - rhs) / np.linalg.norm(rhs) <= parity.NORMWISE_TOL
 
 
+@pytest.mark.parametrize("entry", ENTRIES)
 @pytest.mark.parametrize("name", LARGE)
-def test_large_workload_integer_variant_exact(name):
+def test_large_workload_integer_variant_exact(entry, name):
     w = inputs.WORKLOADS[name]
     A, B = inputs.make_operands(w.M, w.N, w.K, "int4", w.seed)
-    C = _run("gemm_f32", A, B, check_canaries=False)
+    C = _run(entry, A, B, check_canaries=False)
     ii, jj = _sample_indices(w.M, w.N, 4096, 9)
     ref = oracle.gemm_entries(A, B, ii, jj)
-    parity.assert_bit_exact(C[ii, jj], ref, name)
+    parity.assert_bit_exact(C[ii, jj], ref, f"{entry} {name}")
     # With integer C and x in {-1, 0, 1} both sides of Freivalds' identity are
     # exact in FP64, so any wrong entry shows with probability >= 1/2 per vector.
     rng = np.random.default_rng(10)

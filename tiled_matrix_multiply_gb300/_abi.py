@@ -18,6 +18,13 @@ TMM_ERR_ALIAS = -2
 TMM_ERR_UNSUPPORTED_DEVICE = -3
 TMM_ERR_CUDA = -4
 TMM_ERR_DEVICE_TIMEOUT = -5
+# The boundary contract's names for the same codes (GEMM_ERR_* in the header).
+GEMM_OK = TMM_OK
+GEMM_ERR_INVALID_ARG = TMM_ERR_INVALID_ARG
+GEMM_ERR_ALIAS = TMM_ERR_ALIAS
+GEMM_ERR_UNSUPPORTED_DEVICE = TMM_ERR_UNSUPPORTED_DEVICE
+GEMM_ERR_CUDA = TMM_ERR_CUDA
+GEMM_ERR_DEVICE_TIMEOUT = TMM_ERR_DEVICE_TIMEOUT
 
 STATUS_NAMES = {
     TMM_OK: "TMM_OK",
@@ -37,7 +44,8 @@ EXPORTED = GEMM_ENTRY_POINTS + ("gemm_f32_ex", "gemm_f32_tc3", "gemm_f32_tc3_ex"
                                  "window_sum_f32", "sum_f32", "sum_f32_workspace_size",
                                  "softmax_rows_f32",
                                  "tmm_check_device", "tmm_testing_set_wait_hooks",
-                                 "tmm_last_error_string", "tmm_version")
+                                 "tmm_last_error_string", "tmm_version",
+                                 "gemm_last_error_string", "gemm_check_status")
 
 _lock = threading.Lock()
 _lib = None
@@ -101,6 +109,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.tmm_last_error_string.restype = ctypes.c_char_p
         lib.tmm_version.argtypes = []
         lib.tmm_version.restype = ctypes.c_int
+        lib.gemm_last_error_string.argtypes = []
+        lib.gemm_last_error_string.restype = ctypes.c_char_p
+        lib.gemm_check_status.argtypes = [ptr]
+        lib.gemm_check_status.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib

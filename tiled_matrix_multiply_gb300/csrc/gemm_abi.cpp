@@ -230,6 +230,9 @@ int gemm_f32_tc3_ex(int transa, int transb, int64_t M, int64_t N, int64_t K, con
     return TMM_OK;
   }
   const size_t need = tmm::tc3_workspace_bytes(M, N, K);
+  if (need == SIZE_MAX)
+    return fail(TMM_ERR_INVALID_ARG, "%s: the workspace size of this product overflows size_t",
+                who);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(TMM_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", who, need,
                 workspace == nullptr ? size_t(0) : workspace_bytes);
@@ -267,6 +270,15 @@ int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_
   bool noop = false;
   int rc = check_args(who, M, N, K, 0, 0, A, lda, B, ldb, C, ldc, &noop);
   if (rc != TMM_OK || noop) return rc;
+  // The size limit is checked before any CUDA call, so a refused product
+  // reaches neither the device nor the scratch.
+  const size_t need = K > 0 ? tmm::tc3_workspace_bytes(M, N, K) : 0;
+  const size_t limit = tmm::tc3_noalloc_scratch_bytes();
+  if (need > limit)
+    return fail(TMM_ERR_INVALID_ARG,
+                "%s: this product needs %zu bytes of scratch but the fixed scratch holds %zu; "
+                "use gemm_f32_tc3 with a caller-supplied workspace",
+                who, need, limit);
   tmm::DeviceInfo dev;
   if ((rc = current_device(&dev)) != TMM_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -277,15 +289,8 @@ int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_
       return fail(TMM_ERR_CUDA, "%s: cudaMemset2DAsync: %s", who, cudaGetErrorString(e));
     return TMM_OK;
   }
-  const size_t need = tmm::tc3_workspace_bytes(M, N, K);
-  const size_t limit = tmm::tc3_noalloc_scratch_bytes();
-  if (need > limit)
-    return fail(TMM_ERR_INVALID_ARG,
-                "%s: this product needs %zu bytes of scratch but the fixed scratch holds %zu; "
-                "use gemm_f32_tc3 with a caller-supplied workspace",
-                who, need, limit);
   void *scratch = nullptr;
-  cudaError_t e = tmm::tc3_noalloc_scratch(dev.id, &scratch);
+  cudaError_t e = tmm::tc3_noalloc_scratch(&scratch);
   if (e != cudaSuccess)
     return fail(TMM_ERR_CUDA, "%s: scratch address lookup: %s", who, cudaGetErrorString(e));
   const tmm::GemmProblem p = {M, N, K, A, lda, B, ldb, C, ldc};
@@ -390,6 +395,10 @@ int softmax_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx, fl
 }
 
 const char *tmm_last_error_string(void) { return g_last_error; }
+
+const char *gemm_last_error_string(void) { return g_last_error; }
+
+int gemm_check_status(tmm_stream_t stream) { return tmm_check_device(stream); }
 
 int tmm_version(void) { return 100; }
 

@@ -1106,8 +1106,12 @@ cudaError_t launch_tc3_pairs(const GemmProblem &p, const DeviceInfo &dev, int64_
 }  // namespace
 
 size_t tc3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  const int64_t Kp = pad_k(K);
-  return 2 * round256(size_t(M) * Kp * 4) + 2 * round256(size_t(N) * Kp * 4);
+  // In 128-bit arithmetic: with sizes up to 2^31 - 1 the count reaches about
+  // 2^68 bytes, which size_t cannot hold; such products get SIZE_MAX.
+  const __int128 Kp = pad_k(K);
+  const auto part = [](__int128 b) { return (b + 255) / 256 * 256; };
+  const __int128 total = 2 * part(__int128(M) * Kp * 4) + 2 * part(__int128(N) * Kp * 4);
+  return total >= __int128(SIZE_MAX) ? SIZE_MAX : size_t(total);
 }
 
 cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *workspace,

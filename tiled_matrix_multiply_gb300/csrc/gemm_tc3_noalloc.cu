@@ -10,15 +10,17 @@
 // that the CUDA runtime sets aside when this module is loaded; every GPU that
 // loads it holds the array until the process exits.
 //
-// The array's name is only a host-side stand-in in host code: it is turned
-// into the device address with cudaGetSymbolAddress, once per device, with
-// that device current, and that address is what the kernels receive.  All
-// calls share the array and it keeps the last call's contents; nothing in it
-// needs to start at zero (the split pre-pass writes every element the product
-// kernel reads).  Calls that overlap on the GPU (for example on two streams)
-// race on it.
+// The array's name is only a host-side stand-in in host code: every call turns
+// it into the device address with cudaGetSymbolAddress, with the caller's
+// device current, and that address is what the kernels receive.  The lookup
+// is not cached: an address kept per device ordinal would outlive the context
+// it belongs to (after cudaDeviceReset, or with another context current on the
+// same ordinal) and send the kernels to memory that is no longer the array.
+// All calls share the array and it keeps the last call's contents; nothing in
+// it needs to start at zero (the split pre-pass writes every element the
+// product kernel reads).  Calls that overlap on the GPU (for example on two
+// streams) race on it.
 #include <cstddef>
-#include <mutex>
 
 #include "tmm_internal.h"
 
@@ -31,28 +33,16 @@ constexpr size_t kTc3NoallocScratchBytes = size_t(64) << 20;   // 64 MiB per dev
 static __device__ __align__(256) unsigned char g_tc3_noalloc_scratch[kTc3NoallocScratchBytes];
 
 namespace tmm {
-namespace {
-
-constexpr int kMaxScratchDevices = 64;
-std::mutex g_scratch_mutex;
-void *g_scratch_ptr[kMaxScratchDevices] = {};
-
-}  // namespace
 
 size_t tc3_noalloc_scratch_bytes() { return kTc3NoallocScratchBytes; }
 
-cudaError_t tc3_noalloc_scratch(int device, void **ptr) {
-  if (device < 0 || device >= kMaxScratchDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[device] == nullptr) {
-    // The caller has `device` current: the address is that device's copy.
-    void *p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_tc3_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    if (p == nullptr) return cudaErrorInvalidSymbol;
-    g_scratch_ptr[device] = p;
-  }
-  *ptr = g_scratch_ptr[device];
+cudaError_t tc3_noalloc_scratch(void **ptr) {
+  // The current device's (and current context's) copy of the array.
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_tc3_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  if (p == nullptr) return cudaErrorInvalidSymbol;
+  *ptr = p;
   return cudaSuccess;
 }
 

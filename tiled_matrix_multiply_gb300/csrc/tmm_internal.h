@@ -35,16 +35,17 @@ struct DeviceInfo {
 cudaError_t launch_naive(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream);
 cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream);
 
-// Split-TF32 tensor-core path: workspace bytes for an M x N x K product, and
-// the launch (split pre-pass + product kernel); `workspace` is 256-byte aligned.
+// Split-TF32 tensor-core path: workspace bytes for an M x N x K product
+// (SIZE_MAX when the count does not fit in size_t), and the launch (split
+// pre-pass + product kernel); `workspace` is 256-byte aligned.
 size_t tc3_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *workspace,
                        cudaStream_t stream);
 cudaError_t tc3_device_status(unsigned int *status, bool clear);
-// Fixed scratch of gemm_f32_tc3_noalloc: its size, and the current device's
-// address of it (looked up once per device; `device` must be current).
+// Fixed scratch of gemm_f32_tc3_noalloc: its size, and its address on the
+// current device (looked up on every call).
 size_t tc3_noalloc_scratch_bytes();
-cudaError_t tc3_noalloc_scratch(int device, void **ptr);
+cudaError_t tc3_noalloc_scratch(void **ptr);
 void tc3_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns);
 
 // Sliding-window sums (y_i = sum_{d<W} x_{i+d}, i < n); 1 <= W <= kMaxWindow.
