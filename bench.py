@@ -167,6 +167,7 @@ def ffma_peak_tflops(sm_count: int, peaks: dict) -> tuple[float, str]:
 
 
 KERNEL_SOURCES = {"gemm_simt": ["gemm_simt.cu"], "gemm_tc3": ["gemm_tc3.cu"],
+                  "tc3_split_a": ["gemm_tc3.cu"], "tc3_split_b": ["gemm_tc3.cu"],
                   "window_sum": ["window_sum.cu"], "sum_partials": ["reduce_softmax.cu"],
                   "softmax_staged": ["reduce_softmax.cu"], "softmax_grid": ["reduce_softmax.cu"]}
 
@@ -442,8 +443,10 @@ def run_ours(args, world, rank, local):
                                            if clocks.get("sm_mhz") else None)}
 
     extra = {}
+    gpu_id = f"GPU-{uuid}" if uuid else None
+    sm_count = props.multi_processor_count
     if not args.no_tc3 and rank == 0:
-        extra["tc3"] = tc3_leg(args, w, A, B, C, flush, stream, peaks)
+        extra["tc3"] = tc3_leg(args, w, A, B, C, flush, stream, peaks, gpu_id, sm_count)
     if not args.no_layouts and rank == 0:
         extra["layouts"] = layouts_leg(args, w, A, B, C, flush, stream)
     if not args.no_window and rank == 0:
@@ -452,6 +455,8 @@ def run_ours(args, world, rank, local):
         extra.update(reduction_legs(args, flush, stream, peaks))
     if not args.no_contrast and rank == 0:
         extra["contrast"] = contrast_paths(args, w, A, B, C, flush, stream, props, peaks)
+    if not args.no_configs and rank == 0:
+        extra["configs"] = configs_leg(args, flush, stream, peaks, gpu_id, sm_count)
 
     if rank == 0:
         cpu = (cpu_baseline(A_h, B_h, w, args.cpu_seconds)
@@ -480,9 +485,33 @@ def run_ours(args, world, rank, local):
 
 
 TF32_PER_BF16 = 1.1 / 2.25       # nominal dense TF32 / BF16 tensor rates of the part
+TF32_FLOP_PER_CLK_PER_SM = 4096   # dense TF32 tensor FLOP per clock per SM (ncu's instruction rate)
 
 
-def tc3_leg(args, w, A, B, C, flush, stream, peaks) -> dict:
+def tf32_peak(peaks) -> tuple[float, str]:
+    bf16 = peaks.get("bf16_tflops")
+    if bf16:
+        return bf16 * TF32_PER_BF16, ("MEASURED_PEAKS.json bf16_tflops x 1.1/2.25 (nominal "
+                                      "TF32/BF16 dense ratio)")
+    return 1900.0 * TF32_PER_BF16, "fallback 1.9 PFLOP/s bf16 x 1.1/2.25"
+
+
+def tf32_instruction_rate(sm_count: int, mhz) -> float | None:
+    """TF32 tensor FLOP/s at the sampled SM clock: 4096 FLOP per clock per SM."""
+    return sm_count * TF32_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12 if mhz else None
+
+
+def tc3_traffic(workload: str):
+    """DRAM bytes of one gemm_f32_tc3 step: the product kernel and both split
+    kernels, each from its committed ncu capture (None unless all three are
+    recorded for the current sources)."""
+    parts = {k: recorded_traffic(k, workload)
+             for k in ("gemm_tc3", "tc3_split_a", "tc3_split_b")}
+    total = sum(parts.values()) if all(v is not None for v in parts.values()) else None
+    return total, parts
+
+
+def tc3_leg(args, w, A, B, C, flush, stream, peaks, gpu_id, sm_count) -> dict:
     """gemm_f32_tc3 on the same workload: three TF32 tensor-core products per
     output term; reported as effective FP32 TFLOP/s and against the TF32 pipe."""
     import torch
@@ -501,25 +530,114 @@ def tc3_leg(args, w, A, B, C, flush, stream, peaks) -> dict:
         launches["n"] += 3   # split of A, split of B, product kernel
 
     steps = max(3, min(args.steps, 200))
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    launches["n"] = 0
     times = time_device(step, flush, steps, args.warmup, stream, None)
+    clocks = sampler.stop()
     if lib.tmm_check_device(stream.cuda_stream) != _abi.TMM_OK:
         raise _abi.TmmError("tmm_check_device", _abi.TMM_ERR_DEVICE_TIMEOUT, _abi.last_error())
     ms = statistics.mean(times)
-    bf16 = peaks.get("bf16_tflops")
-    peak = bf16 * TF32_PER_BF16 if bf16 else 1900.0 * TF32_PER_BF16
+    peak, peak_src = tf32_peak(peaks)
     tensor_tflops = 3 * w.flops / (ms / 1e3) / 1e12
+    inst_rate = tf32_instruction_rate(sm_count, clocks.get("sm_mhz"))
+    traffic, traffic_parts = tc3_traffic(w.name)
     return {"path": "gemm_f32_tc3 (tcgen05, 3 x TF32 split products, FP32 accumulation)",
             "value": w.flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms,
             "steps": steps, "gpu_launches": launches["n"] - 3 * args.warmup,
-            "workspace_bytes": need,
+            "workspace_bytes": need, "clocks": clocks,
             "roofline": {"bound": "tensor", "achieved": tensor_tflops, "peak": peak, "unit": UNIT,
                          "frac": tensor_tflops / peak,
-                         "traffic": recorded_traffic("gemm_tc3", w.name),
-                         "peak_source": ("MEASURED_PEAKS.json bf16_tflops x 1.1/2.25 (nominal "
-                                         "TF32/BF16 dense ratio)" if bf16 else
-                                         "fallback 1.9 PFLOP/s bf16 x 1.1/2.25"),
+                         "frac_at_instruction_rate": (tensor_tflops / inst_rate
+                                                      if inst_rate else None),
+                         "instruction_rate": inst_rate,
+                         "instruction_rate_source": (f"{sm_count} SMs x 4096 TF32 FLOP/clk x "
+                                                     "median sampled SM clock"),
+                         "traffic": traffic, "traffic_parts": traffic_parts,
+                         "peak_source": peak_src,
                          "algorithmic": f"3 x 2MNK = {3 * w.flops:.4e} tensor FLOP per step "
-                                        "(split pre-pass included in the step time)"}}
+                                        "(split pre-pass included in the step time; traffic "
+                                        "counts the split kernels and the product kernel)"}}
+
+
+#: The workloads of the configs leg: every product configuration, at full size.
+CONFIG_WORKLOADS = ["square256", "square1024", "square4096", "ragged4000x3001x2047",
+                    "rect8192x8192x1024", "rect16384x1024x4096", "rect1024x16384x4096",
+                    "square8192"]
+
+
+def configs_leg(args, flush, stream, peaks, gpu_id, sm_count) -> dict:
+    """Every product configuration at full size, operands in HBM, L2 flushed before
+    every step: gemm_f32 (FFMA roofline) and gemm_f32_tc3 (TF32 tensor roofline), and
+    gemm_f32_naive where a few of its steps take well under a second.  Steps per
+    configuration are sized to about 0.2 s of work per path (5 to 50)."""
+    import torch
+    from tiled_matrix_multiply_gb300 import _abi
+    lib = _abi.load()
+    ffma_peak, ffma_src = ffma_peak_tflops(sm_count, peaks)
+    tf32, tf32_src = tf32_peak(peaks)
+    out = {"peaks": {"gemm_f32": ffma_peak, "gemm_f32_source": ffma_src,
+                     "gemm_f32_tc3": tf32, "gemm_f32_tc3_source": tf32_src,
+                     "unit": UNIT},
+           "l2": "flushed before every step (memset of 2x L2 bytes, outside the events)"}
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    for name in CONFIG_WORKLOADS:
+        w = inputs.WORKLOADS[name]
+        A_h, B_h = inputs.workload_operands(w)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        A = torch.from_numpy(A_h).to(dev)
+        B = torch.from_numpy(B_h).to(dev)
+        C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+        need = int(lib.gemm_f32_tc3_workspace_size(w.M, w.N, w.K))
+        ws = torch.empty(need + 256, dtype=torch.uint8, device=dev)
+        wptr = (ws.data_ptr() + 255) // 256 * 256
+        s = stream.cuda_stream
+
+        def simt():
+            _abi.check("gemm_f32", w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N,
+                       C.data_ptr(), w.N, s)
+
+        def tc3():
+            rc = lib.gemm_f32_tc3(w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N,
+                                  C.data_ptr(), w.N, wptr, need, s)
+            if rc != _abi.TMM_OK:
+                raise _abi.TmmError("gemm_f32_tc3", rc, _abi.last_error())
+
+        def naive():
+            _abi.check("gemm_f32_naive", w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N,
+                       C.data_ptr(), w.N, s)
+
+        rec = {"M": w.M, "N": w.N, "K": w.K, "workload": w.describe()}
+        for label, fn, rate, peak in (("gemm_f32", simt, 60e12, ffma_peak),
+                                      ("gemm_f32_tc3", tc3, 250e12, tf32 / 3),
+                                      ("gemm_f32_naive", naive, 6e12, ffma_peak)):
+            est_s = w.flops / rate
+            if label == "gemm_f32_naive" and est_s > 0.05:
+                continue
+            steps = int(min(50, max(5, 0.2 / est_s)))
+            ms = statistics.mean(time_device(fn, flush, steps, 3, stream, None))
+            tflops = w.flops / (ms / 1e3) / 1e12
+            rec[label] = {"value": tflops, "unit": UNIT, "ms_per_step": ms, "steps": steps,
+                          "frac": tflops / peak}
+            if label == "gemm_f32_tc3":
+                rec[label]["frac_note"] = "effective FP32 TFLOP/s over (TF32 peak / 3)"
+        if lib.tmm_check_device(s) != _abi.TMM_OK:
+            raise _abi.TmmError("tmm_check_device", _abi.TMM_ERR_DEVICE_TIMEOUT,
+                                _abi.last_error())
+        out[name] = rec
+        del A, B, C, ws
+        torch.cuda.empty_cache()
+    clocks = sampler.stop()
+    out["clocks"] = clocks
+    inst = tf32_instruction_rate(sm_count, clocks.get("sm_mhz"))
+    if inst:
+        for name in CONFIG_WORKLOADS:
+            r = out[name].get("gemm_f32_tc3")
+            if r:
+                r["frac_at_instruction_rate"] = 3 * r["value"] / inst
+    return out
 
 
 def layouts_leg(args, w, A, B, C, flush, stream) -> dict:
@@ -693,6 +811,8 @@ def main(argv=None):
                     help="row length of the softmax leg (default 4096)")
     ap.add_argument("--no-layouts", action="store_true",
                     help="skip the transposed-layout (gemm_f32_ex, gemm_f32_tc3_ex) leg")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the leg that times every product configuration")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps, always
     world, rank, local = dist_env()

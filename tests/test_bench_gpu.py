@@ -75,3 +75,28 @@ def test_extra_legs(line):
         assert line["layouts"][lay]["gemm_f32_ex"]["value"] > 0
         assert line["layouts"][lay]["gemm_f32_tc3_ex"]["value"] > 0
     assert line["contrast"]["gemm_f32_naive"]["value"] < line["value"]
+
+
+def test_configs_leg_covers_every_configuration(line):
+    import bench
+    c = line["configs"]
+    assert c["peaks"]["unit"] == "TFLOP/s" and c["clocks"]["samples"] >= 0
+    for name in bench.CONFIG_WORKLOADS:
+        rec = c[name]
+        flops = 2 * rec["M"] * rec["N"] * rec["K"]
+        for path in ("gemm_f32", "gemm_f32_tc3"):
+            r = rec[path]
+            assert r["unit"] == "TFLOP/s" and 5 <= r["steps"] <= 50
+            assert r["value"] == pytest.approx(flops / (r["ms_per_step"] / 1e3) / 1e12, rel=1e-6)
+            assert 0 < r["frac"] < 1.2, (name, path)
+    assert c["square4096"]["gemm_f32"]["value"] > c["square4096"]["gemm_f32_naive"]["value"]
+
+
+def test_tc3_leg_clocks_and_instruction_rate(line):
+    r = line["tc3"]["roofline"]
+    assert "clocks" in line["tc3"]
+    if r["instruction_rate"] is not None:
+        assert r["frac_at_instruction_rate"] == pytest.approx(
+            r["achieved"] / r["instruction_rate"], rel=1e-6)
+        assert 0.1 < r["frac_at_instruction_rate"] < 1.1
+    assert set(r["traffic_parts"]) == {"gemm_tc3", "tc3_split_a", "tc3_split_b"}
