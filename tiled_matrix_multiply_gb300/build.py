@@ -20,7 +20,7 @@ LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libtmm_gemm.so")
 
 SOURCES = ["gemm_abi.cpp", "gemm_naive.cu", "gemm_simt.cu", "gemm_tc3.cu",
-           "gemm_tc3_noalloc.cu", "window_sum.cu", "reduce_softmax.cu"]
+           "gemm_tc3_noalloc.cu", "window_sum.cu", "reduce_softmax.cu", "tensor_map.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC] + ARCH

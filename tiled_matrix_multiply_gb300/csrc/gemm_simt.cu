@@ -84,8 +84,12 @@ constexpr int kGroupM = 16;
 //                        warp instruction, into 32 distinct banks);
 //   kCopyVec          -- the stored rows run along k, contiguous in m or n, 16-byte
 //                        aligned: whole 16-byte vectors;
-//   kCopyScalar       -- as kCopyVec without the alignment: 4-byte copies.
-constexpr int kCopyTransposing = 0, kCopyVec = 1, kCopyScalar = 2;
+//   kCopyScalar       -- as kCopyVec without the alignment: 4-byte copies;
+//   kCopyTma          -- as kCopyVec, by TMA: one copy of the whole slab per
+//                        K-slice (B stored K x N, A stored K x M), issued by one
+//                        thread and counted on the stage's mbarrier; no
+//                        per-thread copy instructions.
+constexpr int kCopyTransposing = 0, kCopyVec = 1, kCopyScalar = 2, kCopyTma = 3;
 
 template <int TM_, int TN_, int kWarpsM_, int kWarpsN_, int BK_, int kStages_, int kMinBlocks_>
 struct SimtConfig {
@@ -102,18 +106,33 @@ struct SimtConfig {
   static constexpr int kMinBlocks = kMinBlocks_;
   // Row pitches of the k-major slabs; both are 4 mod 32 floats when filled by
   // transposing copies, which spreads a warp's 4 rows x 8 k over 32 banks.
-  static constexpr int kAsLd = BM + 4;
+  // A TMA copy writes its box densely.
+  template <int kACopy>
+  __host__ __device__ static constexpr int as_ld() {
+    return kACopy == kCopyTma ? BM : BM + 4;
+  }
   template <int kBCopy>
   __host__ __device__ static constexpr int bs_ld() {
     return kBCopy == kCopyTransposing ? BN + 4 : BN;
   }
-  template <int kBCopy>
-  __host__ __device__ static constexpr int stage_floats() {
-    return BK * kAsLd + BK * bs_ld<kBCopy>();
+  template <int kACopy>
+  __host__ __device__ static constexpr int a_slab_floats() {
+    return BK * as_ld<kACopy>();
   }
-  template <int kBCopy>
+  template <int kACopy, int kBCopy>
+  __host__ __device__ static constexpr int stage_floats() {
+    return a_slab_floats<kACopy>() + BK * bs_ld<kBCopy>();
+  }
+  template <int kACopy, int kBCopy>
+  __host__ __device__ static constexpr bool uses_tma() {
+    return kACopy == kCopyTma || kBCopy == kCopyTma;
+  }
+  // With TMA copies the ring starts on a 128-byte boundary (the TMA
+  // destination rule), and is followed by one mbarrier per stage.
+  template <int kACopy, int kBCopy>
   __host__ __device__ static constexpr int smem_bytes() {
-    return kStages * stage_floats<kBCopy>() * 4;
+    return kStages * stage_floats<kACopy, kBCopy>() * 4 +
+           (uses_tma<kACopy, kBCopy>() ? 128 + 8 * kStages : 0);
   }
   // A copies: groups of 4 rows x 8 k per warp instruction.
   static constexpr int kARowGroups = BM / 4;
@@ -131,10 +150,12 @@ struct SimtConfig {
   static_assert((BN / 4) % kWarps == 0, "transposing B copy groups divide among warps");
   static_assert(kThreads % (BM / 4) == 0 && (BK * BM) % (4 * kThreads) == 0 &&
                 (BK * BM) % kThreads == 0 && BM % 32 == 0, "direct A copies");
-  static_assert(kAsLd % 32 == 4 && (BN + 4) % 32 == 4, "pitches for transposing copies");
+  static_assert((BM + 4) % 32 == 4 && (BN + 4) % 32 == 4, "pitches for transposing copies");
   static_assert(kThreads % kBVecPerRow == 0, "B vector copies cover whole rows");
   static_assert((BK * BN) % (4 * kThreads) == 0 && (BK * BN) % kThreads == 0, "B copies");
   static_assert(BN % 32 == 0, "scalar B copies: a warp copies 32 consecutive columns");
+  static_assert((BK * (BM + 4) * 4) % 128 == 0 && (BK * BM * 4) % 128 == 0 &&
+                (BK * BN * 4) % 128 == 0, "TMA destinations on 128-byte boundaries");
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -195,6 +216,52 @@ __device__ __forceinline__ void store_release(unsigned int *p, unsigned int v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// mbarrier and bulk-tensor (TMA) primitives of the TMA copy kinds.
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Wait for phase `parity` of the barrier to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (int64_t(global_timer_ns() - t0) > limit_ns) return false;
+  return true;
+}
+// As mbar_wait; while waiting also gives up at once when `dead` is set (a
+// register flag of the caller, read only after the first poll has failed).
+__device__ __forceinline__ bool mbar_wait_unless(uint32_t bar, uint32_t parity, int64_t limit_ns,
+                                                 const bool &dead) {
+  if (mbar_try_wait(bar, parity)) return true;
+  if (dead) return false;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (int64_t(global_timer_ns() - t0) > limit_ns) return false;
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &tm,
                                             int &tn) {
   const int per_group = kGroupM * tiles_n;
@@ -248,10 +315,32 @@ struct SimtBlock {
     b_off = wn * (Cf::LN * Cf::TN) + ln * 4;
   }
 
+  // Row of C (relative to the block tile's a_off) of accumulator row r.
+  __device__ __forceinline__ static constexpr int row_of(int r) {
+    return 4 * Cf::LM * (r / 4) + r % 4;
+  }
+
+  // With TMA copies, `bars` holds one mbarrier per stage and bit i of
+  // `phases` the parity its next completion will have.  A wait that runs out
+  // of time is handled off the fast path (tma_wait_failed): the thread sets
+  // the status word and waits no more (its later waits give up at once), so
+  // the kernel still runs to its end in bounded time, its results not valid;
+  // thread 0, the only one issuing copies, first waits (bounded) for every
+  // copy it has in flight and then issues no more (re-arming a stage whose
+  // copy has not landed is unsafe), so no copy lands after the block is gone.
   __device__ __forceinline__ void mainloop(const SimtParams &p, float *smem, int m0, int n0,
-                                           int s_begin, int s_end) {
-    constexpr int BK = Cf::BK, kAsLd = Cf::kAsLd, kBsLd = Cf::template bs_ld<kBCopy>();
-    constexpr int kStageFloats = Cf::template stage_floats<kBCopy>(), kStages = Cf::kStages;
+                                           int s_begin, int s_end, const CUtensorMap *a_map,
+                                           const CUtensorMap *b_map, uint32_t bars,
+                                           uint32_t &phases) {
+    constexpr int BK = Cf::BK, kAsLd = Cf::template as_ld<kACopy>();
+    constexpr int kBsLd = Cf::template bs_ld<kBCopy>();
+    constexpr int kASlab = Cf::template a_slab_floats<kACopy>();
+    constexpr int kStageFloats = Cf::template stage_floats<kACopy, kBCopy>();
+    constexpr int kStages = Cf::kStages;
+    constexpr bool kTma = Cf::template uses_tma<kACopy, kBCopy>();
+    constexpr bool kTmaA = kACopy == kCopyTma;
+    constexpr uint32_t kTmaBytes =
+        (kTmaA ? kASlab * 4 : 0) + (kBCopy == kCopyTma ? BK * Cf::BN * 4 : 0);
 
     // Transposing copies (A stored M x K, B stored N x K): warp instruction
     // (r, h) copies rows 4 (warp + kWarps r) + lane/8 of the tile, k 8 h + lane % 8.
@@ -291,13 +380,13 @@ struct SimtBlock {
         b_rows_ok |= uint32_t(n0 + t_row + 4 * Cf::kWarps * r < p.N) << r;
       b_src = p.B + int64_t(min(n0 + t_row, p.N - 1)) * p.ldb + t_k;
       b_step = int64_t(4 * Cf::kWarps) * p.ldb;
-      b_dst0 = smem_addr(smem) + 4u * (BK * kAsLd + t_k * kBsLd + t_row);
+      b_dst0 = smem_addr(smem) + 4u * (kASlab + t_k * kBsLd + t_row);
     } else {
       b_k = kBCopy == kCopyVec ? tid / Cf::kBVecPerRow : warp;
       b_n = kBCopy == kCopyVec ? (tid % Cf::kBVecPerRow) * 4 : lane;
       b_src = p.B + int64_t(b_k) * p.ldb + min(n0 + b_n, p.N - 1);
       b_step = p.ldb;
-      b_dst0 = smem_addr(smem) + 4u * (BK * kAsLd + b_k * kBsLd + b_n);
+      b_dst0 = smem_addr(smem) + 4u * (kASlab + b_k * kBsLd + b_n);
     }
 
     auto issue_slice = [&](int s, int stage) {
@@ -322,7 +411,7 @@ struct SimtBlock {
           cp_async_16(a_dst0 + st_off + 4u * (kRowsPerPass * v * kAsLd),
                       a + int64_t(kRowsPerPass * v) * a_step, col_ok && (k0 + kr < p.K), p.A);
         }
-      } else {
+      } else if (kACopy == kCopyScalar) {
         constexpr int kColPasses = Cf::BM / 32;
         const float *a = a_src + int64_t(k0) * a_step;
 #pragma unroll
@@ -353,7 +442,7 @@ struct SimtBlock {
           cp_async_16(b_dst0 + st_off + 4u * (kBRowsPerPass * v * kBsLd),
                       b + int64_t(kBRowsPerPass * v) * b_step, ok, p.B);
         }
-      } else {
+      } else if (kBCopy == kCopyScalar) {
         constexpr int kColPasses = Cf::BN / 32;
         const float *b = b_src + int64_t(k0) * b_step;
 #pragma unroll
@@ -364,28 +453,15 @@ struct SimtBlock {
                      b + int64_t(kr) * b_step + 32 * c, ok, p.B);
         }
       }
-    };
-
-    auto load_frag = [&](const float *st, int k, float (&af)[Cf::TM],
-                         uint64_t (&bf)[Cf::TN / 2]) {
-      const float *as = st + k * kAsLd + a_off;
-      const float *bs = st + BK * kAsLd + k * kBsLd + b_off;
-#pragma unroll
-      for (int t = 0; t < Cf::TM / 4; ++t) {
-        const float4 v = *reinterpret_cast<const float4 *>(as + 4 * Cf::LM * t);
-        af[4 * t + 0] = v.x; af[4 * t + 1] = v.y; af[4 * t + 2] = v.z; af[4 * t + 3] = v.w;
-      }
-#pragma unroll
-      for (int c = 0; c < Cf::TN / 4; ++c) {
-        const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(bs + 4 * Cf::LN * c);
-        bf[2 * c + 0] = v.x; bf[2 * c + 1] = v.y;
+      if (kTma && tid == 0 && !tma_dead) {
+        const uint32_t bar = bars + 8u * stage, st = smem_addr(smem) + st_off;
+        mbar_arrive_expect_tx(bar, kTmaBytes);
+        if (kACopy == kCopyTma) tma_load_2d(st, a_map, m0, k0, bar);
+        if (kBCopy == kCopyTma) tma_load_2d(st + 4u * kASlab, b_map, n0, k0, bar);
       }
     };
 
-#pragma unroll
-    for (int i = 0; i < Cf::TM; ++i)
-#pragma unroll
-      for (int j = 0; j < Cf::TN / 2; ++j) acc[i][j] = 0;   // +0.0f in both halves
+    zero_acc();
 
 #pragma unroll
     for (int s = 0; s < kStages - 1; ++s) {
@@ -393,12 +469,19 @@ struct SimtBlock {
       cp_async_commit();
     }
 
-    float af[2][Cf::TM];
-    uint64_t bf[2][Cf::TN / 2];
     int stage = 0;
     for (int s = s_begin; s < s_end; ++s) {
       cp_async_wait<kStages - 2>();   // slice s has landed (this thread's copies) ...
-      __syncthreads();                // ... and everyone's; slice s-1's stage is free
+      if (kTma) {
+        // ... and its TMA copies ...
+        if (!mbar_wait_unless(bars + 8u * stage, (phases >> stage) & 1u, p.wait_limit_ns,
+                              tma_dead))
+          tma_wait_failed(p, bars, phases, stage, s, s_end);
+        phases ^= 1u << stage;
+        __syncthreads();              // ... and everyone's; slice s-1's stage is free
+      } else {
+        __syncthreads();              // ... and everyone's; slice s-1's stage is free
+      }
       {
         const int sn = s + kStages - 1;
         int stage_n = stage + kStages - 1;
@@ -407,32 +490,88 @@ struct SimtBlock {
         cp_async_commit();
       }
       const float *st = smem + stage * kStageFloats;
-      load_frag(st, 0, af[0], bf[0]);
-#pragma unroll 1
-      for (int kk = 0; kk < BK; kk += Cf::kKUnroll) {
-#pragma unroll
-        for (int u = 0; u < Cf::kKUnroll; ++u) {
-          const int k = kk + u;
-          if (u + 1 < Cf::kKUnroll || k + 1 < BK)
-            load_frag(st, k + 1, af[(u + 1) & 1], bf[(u + 1) & 1]);
-          // Outer product: acc[i][j] += a[i] * b[j], two columns per instruction.
-#pragma unroll
-          for (int i = 0; i < Cf::TM; ++i) {
-            const uint64_t ai = pack2(af[u & 1][i], af[u & 1][i]);
-#pragma unroll
-            for (int j = 0; j < Cf::TN / 2; ++j) acc[i][j] = ffma2(ai, bf[u & 1][j], acc[i][j]);
-          }
-        }
-      }
+      slice_products<kAsLd, kBsLd>(st, st + kASlab);
       if (++stage == kStages) stage = 0;
     }
     cp_async_wait<0>();
     __syncthreads();   // the next tile's copies may overwrite any stage
   }
 
-  // Accumulator (4t + i, 4c + j) is C[m0 + a_off + 4 LM t + i][n0 + b_off + 4 LN c + j].
-  // kAdd: add the partial sums already in C (loaded through L2) before storing.
-  template <bool kAdd>
+  // Set once one of this thread's TMA waits has run out of time.
+  bool tma_dead = false;
+
+  // The wait for slice s (in `stage`) ran out of time.  Thread 0 has copies in
+  // flight for slices s .. min(s_end, s + kStages - 1) - 1, one per stage from
+  // `stage` on, each at its stage's parity in `phases`.
+  __device__ __forceinline__ void tma_wait_failed(const SimtParams &p, uint32_t bars,
+                                                  uint32_t phases, int stage, int s, int s_end) {
+    if (!tma_dead) {   // this thread's first failure
+      atomicOr(&g_simt_status, 2u);
+      if (tid == 0) {
+        const int last = min(s_end, s + Cf::kStages - 1);
+        for (int q = s, st = stage; q < last; ++q, st = (st + 1) % Cf::kStages)
+          mbar_wait(bars + 8u * st, (phases >> st) & 1u, p.wait_limit_ns);
+      }
+    }
+    tma_dead = true;
+  }
+
+  __device__ __forceinline__ void zero_acc() {
+#pragma unroll
+    for (int i = 0; i < Cf::TM; ++i)
+#pragma unroll
+      for (int j = 0; j < Cf::TN / 2; ++j) acc[i][j] = 0;   // +0.0f in both halves
+  }
+
+  // This thread's fragments at k of a staged slice: TM values of the k-major A
+  // slab `as` (row pitch kAsLd) and TN values of the B slab `bs` (pitch kBsLd).
+  template <int kAsLd, int kBsLd>
+  __device__ __forceinline__ void load_frag(const float *as, const float *bs, int k,
+                                            float (&af)[Cf::TM], uint64_t (&bf)[Cf::TN / 2]) {
+    const float *a = as + k * kAsLd + a_off;
+    const float *b = bs + k * kBsLd + b_off;
+#pragma unroll
+    for (int t = 0; t < Cf::TM / 4; ++t) {
+      const float4 v = *reinterpret_cast<const float4 *>(a + 4 * Cf::LM * t);
+      af[4 * t + 0] = v.x; af[4 * t + 1] = v.y; af[4 * t + 2] = v.z; af[4 * t + 3] = v.w;
+    }
+#pragma unroll
+    for (int c = 0; c < Cf::TN / 4; ++c) {
+      const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(b + 4 * Cf::LN * c);
+      bf[2 * c + 0] = v.x; bf[2 * c + 1] = v.y;
+    }
+  }
+
+  // The BK outer products of one staged slice, the fragments of step k + 1
+  // loaded while step k's packed FMAs issue.
+  template <int kAsLd, int kBsLd>
+  __device__ __forceinline__ void slice_products(const float *as, const float *bs) {
+    constexpr int BK = Cf::BK;
+    float af[2][Cf::TM];
+    uint64_t bf[2][Cf::TN / 2];
+    load_frag<kAsLd, kBsLd>(as, bs, 0, af[0], bf[0]);
+#pragma unroll 1
+    for (int kk = 0; kk < BK; kk += Cf::kKUnroll) {
+#pragma unroll
+      for (int u = 0; u < Cf::kKUnroll; ++u) {
+        const int k = kk + u;
+        if (u + 1 < Cf::kKUnroll || k + 1 < BK)
+          load_frag<kAsLd, kBsLd>(as, bs, k + 1, af[(u + 1) & 1], bf[(u + 1) & 1]);
+        // Outer product: acc[i][j] += a[i] * b[j], two columns per instruction.
+#pragma unroll
+        for (int i = 0; i < Cf::TM; ++i) {
+          const uint64_t ai = pack2(af[u & 1][i], af[u & 1][i]);
+#pragma unroll
+          for (int j = 0; j < Cf::TN / 2; ++j) acc[i][j] = ffma2(ai, bf[u & 1][j], acc[i][j]);
+        }
+      }
+    }
+  }
+
+  // Accumulator (r, 4c + j) is C[m0 + a_off + row_of(r)][n0 + b_off + 4 LN c + j].
+  // kAdd: add the partial sums already in C (loaded through L2) before storing,
+  // kAddRows rows of them loaded together.
+  template <bool kAdd, int kAddRows = 4>
   __device__ __forceinline__ void epilogue(const SimtParams &p, int m0, int n0) {
     const int row0 = m0 + a_off;
     const int col0 = n0 + b_off;
@@ -441,7 +580,6 @@ struct SimtBlock {
     // store, so the loads are in flight together (a store before a load of the
     // same array would order them one after another) -- element by element
     // when C takes no 16-byte stores.
-    constexpr int kAddRows = 4;
     static_assert(Cf::TM % kAddRows == 0, "whole row groups");
 #pragma unroll
     for (int r0 = 0; r0 < Cf::TM; r0 += kAddRows) {
@@ -454,7 +592,7 @@ struct SimtBlock {
 #pragma unroll
         for (int i = 0; i < kAddRows; ++i) {
           const int r = r0 + i;
-          const int dr = 4 * Cf::LM * (r / 4) + r % 4;
+          const int dr = row_of(r);
           if (row0 + dr >= p.M) continue;
           const float *c_row = c_base + int64_t(dr) * p.ldc;
 #pragma unroll
@@ -466,7 +604,7 @@ struct SimtBlock {
 #pragma unroll
         for (int i = 0; i < kAddRows; ++i) {
           const int r = r0 + i;
-          const int dr = 4 * Cf::LM * (r / 4) + r % 4;
+          const int dr = row_of(r);
           if (row0 + dr >= p.M) continue;
           const float *c_row = c_base + int64_t(dr) * p.ldc;
 #pragma unroll
@@ -483,7 +621,7 @@ struct SimtBlock {
 #pragma unroll
       for (int i = 0; i < kAddRows; ++i) {
         const int r = r0 + i;
-        const int dr = 4 * Cf::LM * (r / 4) + r % 4;
+        const int dr = row_of(r);
         if (row0 + dr >= p.M) continue;
         float *c_row = c_base + int64_t(dr) * p.ldc;
         float a[Cf::TN];
@@ -517,10 +655,26 @@ struct SimtBlock {
   }
 };
 
+// a_map, b_map: the tensor maps of A and B for the TMA copy kinds, else unused.
 template <class Cf, int kACopy, int kBCopy>
 __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
-gemm_simt_kernel(const SimtParams p) {
-  extern __shared__ __align__(16) float smem[];
+gemm_simt_kernel(const __grid_constant__ CUtensorMap a_map,
+                 const __grid_constant__ CUtensorMap b_map, const SimtParams p) {
+  extern __shared__ __align__(16) float smem_raw[];
+  constexpr int kRingFloats = Cf::kStages * Cf::template stage_floats<kACopy, kBCopy>();
+  float *smem = smem_raw;
+  uint32_t bars = 0, phases = 0;
+  if (Cf::template uses_tma<kACopy, kBCopy>()) {
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 127u) & ~127u;
+    smem = smem_raw + (base - raw) / 4;
+    bars = base + uint32_t(kRingFloats * 4);
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < Cf::kStages; ++i) mbar_init(bars + 8u * i, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+  }
   SimtBlock<Cf, kACopy, kBCopy> blk;
   blk.init_lanes();
 
@@ -528,7 +682,7 @@ gemm_simt_kernel(const SimtParams p) {
   for (int tile = blockIdx.x; tile < p.dp_tiles; tile += gridDim.x) {
     int tm, tn;
     tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
-    blk.mainloop(p, smem, tm * Cf::BM, tn * Cf::BN, 0, p.slices);
+    blk.mainloop(p, smem, tm * Cf::BM, tn * Cf::BN, 0, p.slices, &a_map, &b_map, bars, phases);
     blk.template epilogue<false>(p, tm * Cf::BM, tn * Cf::BN);
   }
   if (p.sk_iters == 0) return;
@@ -545,7 +699,7 @@ gemm_simt_kernel(const SimtParams p) {
     int tm, tn;
     tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
     const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
-    blk.mainloop(p, smem, m0, n0, s_begin, s_end);
+    blk.mainloop(p, smem, m0, n0, s_begin, s_end, &a_map, &b_map, bars, phases);
     if (s_begin == 0 && s_end == p.slices) {
       blk.template epilogue<false>(p, m0, n0);
     } else if (s_end == p.slices) {
@@ -610,11 +764,62 @@ std::atomic<unsigned int> g_epoch{0};
 std::atomic<int64_t> g_wait_limit_ns{int64_t(10) * 1000 * 1000 * 1000};
 std::atomic<int> g_drop_signal_block{-1};
 
+// Tiling and work split shared by both kernels: fills prm and returns the
+// grid size.  When the tile count leaves the last wave of `slots` resident
+// blocks partly empty, one block per slot, the last full wave plus the
+// remainder split over K (stream-K); with fewer tiles than slots, every
+// tile's K-slices shared by up to about five consecutive blocks (a share is at
+// least a quarter of a tile and four slices), when that gives at least an
+// eighth more blocks than tiles.  Both schemes need the blocks co-resident
+// (*cooperative) and `flags_per_block` flags per block.
+int64_t plan_simt(SimtParams &prm, const GemmProblem &p, int BM, int BN, int BK, int64_t slots,
+                  int flags_per_block, bool *cooperative) {
+  const int64_t tiles_m = (p.M + BM - 1) / BM;
+  const int64_t tiles_n = (p.N + BN - 1) / BN;
+  const int64_t tiles = tiles_m * tiles_n;
+  const int slices = int((p.K + BK - 1) / BK);
+  prm.M = int(p.M); prm.N = int(p.N); prm.K = int(p.K);
+  prm.A = p.A; prm.lda = p.lda; prm.B = p.B; prm.ldb = p.ldb; prm.C = p.C; prm.ldc = p.ldc;
+  prm.tiles_m = int(tiles_m); prm.tiles_n = int(tiles_n);
+  prm.vec_store = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0 &&
+                   p.N % 4 == 0) ? 1 : 0;
+  prm.slices = slices;
+  prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  prm.drop_signal_block = g_drop_signal_block.load(std::memory_order_relaxed);
+  const bool flags_fit = slots > 0 && slots * flags_per_block <= kMaxPersistentBlocks;
+  const int64_t rem = slots > 0 ? tiles % slots : 0;
+  const bool stream_k = flags_fit && tiles > slots && rem != 0 && rem * 10 < slots * 9 &&
+                        slices >= 4;
+  int64_t small_blocks = 0;
+  if (!stream_k && flags_fit && tiles < slots) {
+    const int64_t iters = tiles * slices;
+    int64_t share = (iters + slots - 1) / slots;
+    share = share > (slices + 3) / 4 ? share : (slices + 3) / 4;
+    share = share > 4 ? share : 4;
+    const int64_t g = (iters + share - 1) / share;
+    if (g * 8 >= tiles * 9) small_blocks = g;
+  }
+  *cooperative = stream_k || small_blocks > 0;
+  if (*cooperative) {
+    const int64_t sk_tiles = stream_k ? rem + slots : tiles;
+    prm.dp_tiles = int(tiles - sk_tiles);
+    prm.sk_iters = sk_tiles * slices;
+    unsigned int e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    prm.epoch = e;
+    return stream_k ? slots : small_blocks;
+  }
+  prm.dp_tiles = int(tiles);
+  prm.sk_iters = 0;
+  prm.epoch = 0;
+  return tiles;
+}
+
 template <class Cf, int kACopy, int kBCopy>
 cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
   static LaunchState state;
   auto kernel = gemm_simt_kernel<Cf, kACopy, kBCopy>;
-  constexpr int kSmemBytes = Cf::template smem_bytes<kBCopy>();
+  constexpr int kSmemBytes = Cf::template smem_bytes<kACopy, kBCopy>();
   const uint64_t bit = uint64_t(1) << (dev.id & 63);
   if (!(state.configured.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -630,65 +835,34 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStre
     state.configured.fetch_or(bit, std::memory_order_release);
   }
   const int blocks_per_sm = state.blocks_per_sm[dev.id & 63].load(std::memory_order_relaxed);
-
-  const int64_t tiles_m = (p.M + Cf::BM - 1) / Cf::BM;
-  const int64_t tiles_n = (p.N + Cf::BN - 1) / Cf::BN;
-  const int64_t tiles = tiles_m * tiles_n;
+  const int64_t tiles = ((p.M + Cf::BM - 1) / Cf::BM) * ((p.N + Cf::BN - 1) / Cf::BN);
   if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  const int slices = int((p.K + Cf::BK - 1) / Cf::BK);
 
+  CUtensorMap a_map = {}, b_map = {};
+  cudaError_t e = cudaSuccess;
+  if (kACopy == kCopyTma)       // A stored K x M: boxes of BM columns x BK rows, a[k][m]
+    e = encode_f32_2d(&a_map, p.A, p.K, p.M, p.lda, Cf::BM, Cf::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  if (kBCopy == kCopyTma)       // B stored K x N: boxes of BN columns x BK rows, b[k][n]
+    e = encode_f32_2d(&b_map, p.B, p.K, p.N, p.ldb, Cf::BN, Cf::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
   SimtParams prm = {};
-  prm.M = int(p.M); prm.N = int(p.N); prm.K = int(p.K);
-  prm.A = p.A; prm.lda = p.lda; prm.B = p.B; prm.ldb = p.ldb; prm.C = p.C; prm.ldc = p.ldc;
-  prm.tiles_m = int(tiles_m); prm.tiles_n = int(tiles_n);
-  prm.vec_store = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0 &&
-                   p.N % 4 == 0) ? 1 : 0;
-  prm.slices = slices;
-  prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-  prm.drop_signal_block = g_drop_signal_block.load(std::memory_order_relaxed);
-
-  // Stream-K when the last wave would be partly empty: one block per resident
-  // slot, the last full wave plus the remainder split over K.
-  const int64_t slots = int64_t(blocks_per_sm) * dev.sm_count;
-  const int64_t rem = slots > 0 ? tiles % slots : 0;
-  const bool stream_k = slots > 0 && slots <= kMaxPersistentBlocks && tiles > slots &&
-                        rem != 0 && rem * 10 < slots * 9 && slices >= 4;
-  // Fewer tiles than slots: every tile's K-slices are shared by up to about
-  // five consecutive blocks (a share is at least a quarter of a tile and four
-  // slices), when that gives at least an eighth more blocks than tiles.
-  int64_t small_blocks = 0;
-  if (!stream_k && slots > 0 && slots <= kMaxPersistentBlocks && tiles < slots) {
-    const int64_t iters = tiles * slices;
-    int64_t share = (iters + slots - 1) / slots;
-    share = share > (slices + 3) / 4 ? share : (slices + 3) / 4;
-    share = share > 4 ? share : 4;
-    const int64_t g = (iters + share - 1) / share;
-    if (g * 8 >= tiles * 9) small_blocks = g;
-  }
+  bool coop = false;
+  const int64_t grid = plan_simt(prm, p, Cf::BM, Cf::BN, Cf::BK,
+                                 int64_t(blocks_per_sm) * dev.sm_count, 1, &coop);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(Cf::kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  if (stream_k || small_blocks > 0) {
-    const int64_t sk_tiles = stream_k ? rem + slots : tiles;
-    prm.dp_tiles = int(tiles - sk_tiles);
-    prm.sk_iters = sk_tiles * slices;
-    unsigned int e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
-    if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
-    prm.epoch = e;
-    cfg.gridDim = dim3(unsigned(stream_k ? slots : small_blocks), 1, 1);
+  cfg.gridDim = dim3(unsigned(grid), 1, 1);
+  if (coop) {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-  } else {
-    prm.dp_tiles = int(tiles);
-    prm.sk_iters = 0;
-    prm.epoch = 0;
-    cfg.gridDim = dim3(unsigned(tiles), 1, 1);
   }
-  return cudaLaunchKernelEx(&cfg, kernel, prm);
+  return cudaLaunchKernelEx(&cfg, kernel, a_map, b_map, prm);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -701,6 +875,10 @@ cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_
   // in 16-byte vectors when aligned; the other two layouts by transposing copies.
   const bool vec_a = aligned16(p.A) && p.lda % 4 == 0 && p.M % 4 == 0;
   const bool vec_b = aligned16(p.B) && p.ldb % 4 == 0 && p.N % 4 == 0;
+  // Operands whose rows all start on 16-byte boundaries are copied by TMA
+  // (the tensor-map rules: 16-byte aligned base, row stride a multiple of 16 bytes).
+  const bool tma_a = aligned16(p.A) && p.lda % 4 == 0;
+  const bool tma_b = aligned16(p.B) && p.ldb % 4 == 0;
   // Unaligned B takes the 128 x 256 tile unless its tiles would leave SMs
   // idle; the default tile then gives twice the blocks (1024 x 1023 x 1024:
   // 21.2 against 15.8 TFLOP/s; 512 x 511 x 2048: 10.0 against 5.9).
@@ -709,19 +887,20 @@ cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_
   if (!p.transa) {
     if (p.transb)
       return launch_variant<SquareConfig, kCopyTransposing, kCopyTransposing>(p, dev, stream);
-    if (vec_b) return launch_variant<Cf, kCopyTransposing, kCopyVec>(p, dev, stream);
+    if (tma_b)
+      return launch_variant<Cf, kCopyTransposing, kCopyTma>(p, dev, stream);
     return wide_b ? launch_variant<UB, kCopyTransposing, kCopyScalar>(p, dev, stream)
                   : launch_variant<Cf, kCopyTransposing, kCopyScalar>(p, dev, stream);
   }
   if (p.transb)
     return vec_a ? launch_variant<WideMConfig, kCopyVec, kCopyTransposing>(p, dev, stream)
                  : launch_variant<WideMConfig, kCopyScalar, kCopyTransposing>(p, dev, stream);
-  if (vec_a) {
-    if (vec_b) return launch_variant<Cf, kCopyVec, kCopyVec>(p, dev, stream);
+  if (tma_b)
+    return tma_a ? launch_variant<Cf, kCopyTma, kCopyTma>(p, dev, stream)
+                 : launch_variant<Cf, kCopyScalar, kCopyTma>(p, dev, stream);
+  if (vec_a)
     return wide_b ? launch_variant<UB, kCopyVec, kCopyScalar>(p, dev, stream)
                   : launch_variant<Cf, kCopyVec, kCopyScalar>(p, dev, stream);
-  }
-  if (vec_b) return launch_variant<Cf, kCopyScalar, kCopyVec>(p, dev, stream);
   return wide_b ? launch_variant<UB, kCopyScalar, kCopyScalar>(p, dev, stream)
                 : launch_variant<Cf, kCopyScalar, kCopyScalar>(p, dev, stream);
 }

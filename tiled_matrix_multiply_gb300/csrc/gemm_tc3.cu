@@ -57,12 +57,10 @@
 // bit 1 in its device status word, stops issuing work, waits (bounded) for its
 // copies in flight, frees its tensor memory and exits.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
-#include <mutex>
 
 #include "tmm_internal.h"
 
@@ -966,36 +964,12 @@ gemm_tc3_pair_kernel(const __grid_constant__ CUtensorMap map_ahi,
 int64_t pad_k(int64_t K) { return (K + kKPad - 1) / kKPad * kKPad; }
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-cudaError_t g_encode_status = cudaSuccess;
-
-cudaError_t get_encoder() {
-  std::call_once(g_encode_once, [] {
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    g_encode_status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                       cudaEnableDefault, &q);
-    if (g_encode_status == cudaSuccess && (q != cudaDriverEntryPointSuccess || fn == nullptr))
-      g_encode_status = cudaErrorNotSupported;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  return g_encode_status;
-}
-
 // K-major operand: `rows` rows of `kdim` floats, `ld` floats apart; box of
 // kTcBK x box_rows, 64-byte swizzle.  Reads past kdim or rows return zeros.
 cudaError_t encode_operand(CUtensorMap *map, const float *base, int64_t rows, int64_t kdim,
                            int64_t ld, uint32_t box_rows) {
-  const cuuint64_t dims[2] = {cuuint64_t(kdim), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(ld) * 4};
-  const cuuint32_t box[2] = {cuuint32_t(kTcBK), box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base),
-                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  return encode_f32_2d(map, base, rows, kdim, ld, uint32_t(kTcBK), box_rows,
+                       CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 std::atomic<uint64_t> g_tc3_configured{0};
@@ -1116,7 +1090,7 @@ size_t tc3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 
 cudaError_t launch_tc3(const GemmProblem &p, const DeviceInfo &dev, void *workspace,
                        cudaStream_t stream) {
-  cudaError_t e = get_encoder();
+  cudaError_t e = tensor_map_encoder_ready();
   if (e != cudaSuccess) return e;
   const int64_t Kp = pad_k(p.K);
   char *ws = static_cast<char *>(workspace);

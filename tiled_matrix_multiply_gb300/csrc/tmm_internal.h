@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace tmm {
@@ -29,6 +30,15 @@ struct DeviceInfo {
   int cc_major, cc_minor;
   int max_smem_optin;  // bytes of shared memory a block may opt in to
 };
+
+// A 2-D FP32 tensor map (TMA descriptor): `rows` rows of `cols` floats, `ld`
+// floats apart, copied in boxes of box_cols x box_rows; reads outside the
+// matrix return zeros.  The base must be 16-byte aligned and ld a multiple of
+// 4 (the tensor-map rules); cudaErrorInvalidValue otherwise.
+cudaError_t tensor_map_encoder_ready();
+cudaError_t encode_f32_2d(CUtensorMap *map, const float *base, int64_t rows, int64_t cols,
+                          int64_t ld, uint32_t box_cols, uint32_t box_rows,
+                          CUtensorMapSwizzle swizzle);
 
 // Each launcher enqueues its kernel(s) on `stream` and returns the launch
 // status.  Problems reaching a launcher have M, N, K > 0.
