@@ -243,7 +243,8 @@ int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K,
 /*
  * tmm_check_device -- synchronise `stream`, then read and clear the current
  * device's status words.  Returns TMM_OK, or TMM_ERR_DEVICE_TIMEOUT when a
- * bounded wait inside gemm_f32 (between the blocks sharing a split tile),
+ * bounded wait inside gemm_f32 (between the blocks sharing a split tile, or
+ * for a K-slice's TMA copy),
  * gemm_f32_tc3 (between the copy, tensor-core and epilogue roles of a block
  * or block pair), window_sum_f32 (for a tile's bulk copy) or softmax_rows_f32
  * (between the blocks sharing a row of more than 65536 columns) ran out of time
@@ -258,7 +259,9 @@ int tmm_check_device(tmm_stream_t stream);
  * drop_signal_block >= 0 makes that block of later split-tile launches of
  * gemm_f32 (and that split unit -- the K-part of a tile, numbered across the
  * call's split tiles -- of gemm_f32_tc3) skip raising its flags, so the one
- * waiting on it runs into the time limit, and makes that block of later window_sum_f32
+ * waiting on it runs into the time limit; makes that block of later gemm_f32
+ * launches whose operands are staged by TMA (rows on 16-byte boundaries) wait
+ * for 16 bytes more than the first copy of each tile brings; makes that block of later window_sum_f32
  * launches (16-byte-aligned x) wait for 16 bytes more than its first tile
  * copy brings, and that block of later softmax_rows_f32 launches on rows of
  * more than 65536 columns skip counting itself in;

@@ -98,3 +98,41 @@ def test_stream_k_wait_timeout_is_reported_and_recovers(shape):
     C = _run("gemm_f32", A, B, check_canaries=False)
     parity.assert_bit_exact(C, oracle.gemm(A, B), "after timeout")
     assert lib.tmm_check_device(stream) == _abi.TMM_OK
+
+
+@pytest.mark.parametrize("transa", [0, 1])
+def test_tma_wait_timeout_is_reported_and_recovers(transa):
+    # 1216 x 4096 tiles exactly into 304 blocks of 64 x 256 (two per SM): one
+    # plain wave, no split tiles, so only the TMA wait of block 1 -- armed for
+    # 16 bytes its copy never brings -- can run out of time.  transa = 1 stages
+    # both operands by TMA (A stored K x M), transa = 0 only B.
+    lib = _abi.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    M, N, K = 1216, 4096, 512
+    rng = np.random.default_rng(43)
+    A = rng.integers(-4, 5, (M, K)).astype(np.float32)
+    B = rng.integers(-4, 5, (K, N)).astype(np.float32)
+    dA = torch.from_numpy(np.ascontiguousarray(A.T) if transa else A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    lda = M if transa else K
+
+    def call():
+        C = torch.full((M, N), float("nan"), device="cuda")
+        rc = lib.gemm_f32_ex(transa, 0, M, N, K, dA.data_ptr(), lda, dB.data_ptr(), N,
+                             C.data_ptr(), N, stream)
+        assert rc == _abi.TMM_OK, _abi.last_error()
+        return C
+
+    assert lib.tmm_check_device(stream) == _abi.TMM_OK      # clean slate
+    try:
+        assert lib.tmm_testing_set_wait_hooks(1, 2_000_000) == _abi.TMM_OK
+        call()
+        rc = lib.tmm_check_device(stream)
+        assert rc == _abi.TMM_ERR_DEVICE_TIMEOUT, rc
+    finally:
+        lib.tmm_testing_set_wait_hooks(-1, 0)
+    assert lib.tmm_check_device(stream) == _abi.TMM_OK
+    C = call()
+    torch.cuda.synchronize()
+    parity.assert_bit_exact(C.cpu().numpy(), oracle.gemm(A, B), f"after TMA timeout, transa={transa}")
+    assert lib.tmm_check_device(stream) == _abi.TMM_OK

@@ -389,7 +389,9 @@ struct SimtBlock {
       b_dst0 = smem_addr(smem) + 4u * (kASlab + b_k * kBsLd + b_n);
     }
 
-    auto issue_slice = [&](int s, int stage) {
+    // extra_tx: bytes the stage's barrier expects beyond the copies (testing
+    // hook: a barrier that never completes).
+    auto issue_slice = [&](int s, int stage, uint32_t extra_tx) {
       const int k0 = s * BK;
       const uint32_t st_off = 4u * stage * kStageFloats;
       if (kACopy == kCopyTransposing) {
@@ -455,7 +457,7 @@ struct SimtBlock {
       }
       if (kTma && tid == 0 && !tma_dead) {
         const uint32_t bar = bars + 8u * stage, st = smem_addr(smem) + st_off;
-        mbar_arrive_expect_tx(bar, kTmaBytes);
+        mbar_arrive_expect_tx(bar, kTmaBytes + extra_tx);
         if (kACopy == kCopyTma) tma_load_2d(st, a_map, m0, k0, bar);
         if (kBCopy == kCopyTma) tma_load_2d(st + 4u * kASlab, b_map, n0, k0, bar);
       }
@@ -465,7 +467,9 @@ struct SimtBlock {
 
 #pragma unroll
     for (int s = 0; s < kStages - 1; ++s) {
-      if (s_begin + s < s_end) issue_slice(s_begin + s, s);
+      if (s_begin + s < s_end)
+        issue_slice(s_begin + s, s,
+                    (s == 0 && int(blockIdx.x) == p.drop_signal_block) ? 16u : 0u);
       cp_async_commit();
     }
 
@@ -486,7 +490,7 @@ struct SimtBlock {
         const int sn = s + kStages - 1;
         int stage_n = stage + kStages - 1;
         if (stage_n >= kStages) stage_n -= kStages;
-        if (sn < s_end) issue_slice(sn, stage_n);
+        if (sn < s_end) issue_slice(sn, stage_n, 0u);
         cp_async_commit();
       }
       const float *st = smem + stage * kStageFloats;
