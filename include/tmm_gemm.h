@@ -78,6 +78,12 @@ typedef struct CUstream_st *tmm_stream_t;
 /* Reported by tmm_check_device: a bounded wait inside a kernel ran out of
  * time, and results written since the last check are not valid. */
 #define TMM_ERR_DEVICE_TIMEOUT (-5)
+/* Reported by tmm_check_device of the bounds-checked debug build only (the
+ * library compiled with -DTMM_BOUNDS_CHECK): a product kernel computed a
+ * global address outside its matrix (or in a row gap) or a shared-memory
+ * offset outside its slab; the access was skipped, and results written since
+ * the last check are not valid.  The normal build never returns it. */
+#define TMM_ERR_BOUNDS (-6)
 
 /* The same status codes under the names of the product's boundary contract
  * (GEMM_ERR_*); each equals its TMM_ERR_* counterpart. */
@@ -87,6 +93,7 @@ typedef struct CUstream_st *tmm_stream_t;
 #define GEMM_ERR_UNSUPPORTED_DEVICE TMM_ERR_UNSUPPORTED_DEVICE
 #define GEMM_ERR_CUDA TMM_ERR_CUDA
 #define GEMM_ERR_DEVICE_TIMEOUT TMM_ERR_DEVICE_TIMEOUT
+#define GEMM_ERR_BOUNDS TMM_ERR_BOUNDS
 
 /*
  * gemm_f32 -- the tiled FP32 product on the CUDA cores (FFMA, IEEE single
@@ -251,6 +258,8 @@ int gemm_f32_tc3_noalloc(int64_t M, int64_t N, int64_t K,
  * since the last check; results written since then are not valid.  The pages have no counterpart: this is the library's failure
  * detection ("CMU DLSys Lecture 12" section 2 only asks that API and launch
  * errors be checked).  TMM_ERR_CUDA if the synchronisation itself failed.
+ * In the bounds-checked build, TMM_ERR_BOUNDS (which takes precedence) when a
+ * range check of gemm_f32, gemm_f32_naive or gemm_f32_tc3 failed.
  */
 int tmm_check_device(tmm_stream_t stream);
 

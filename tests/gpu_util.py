@@ -52,29 +52,45 @@ class DevMatrix:
 
 def run_entry(entry: str, A: np.ndarray, B: np.ndarray, *, lda=None, ldb=None, ldc=None,
               a_off=0, b_off=0, c_off=0, stream=None, check_canaries=True,
-              check_status=True) -> np.ndarray:
-    """C = A x B through the C ABI on device buffers laid out as requested."""
-    M, K = A.shape
-    K2, N = B.shape
+              check_status=True, lib=None, trans=(0, 0)) -> np.ndarray:
+    """C = op(A) x op(B) through the C ABI on device buffers laid out as requested.
+
+    A and B are the stored matrices: with trans = (1, *) A is stored K x M, with
+    (*, 1) B is stored N x K (the layouts of gemm_f32_ex / gemm_f32_tc3_ex).
+    `lib` selects another build of the library (default: the normal one)."""
+    ta, tb = trans
+    M, K = (A.shape[1], A.shape[0]) if ta else A.shape
+    N, K2 = (B.shape[0], B.shape[1]) if tb else (B.shape[1], B.shape[0])
     assert K == K2
-    dA = DevMatrix(A, M, K, lda, a_off)
-    dB = DevMatrix(B, K, N, ldb, b_off)
+    lib = lib if lib is not None else _abi.load()
+    dA = DevMatrix(A, A.shape[0], A.shape[1], lda, a_off)
+    dB = DevMatrix(B, B.shape[0], B.shape[1], ldb, b_off)
     dC = DevMatrix(None, M, N, ldc, c_off)
     s = stream if stream is not None else torch.cuda.current_stream()
-    if entry == "gemm_f32_tc3":
-        lib = _abi.load()
+    if entry in ("gemm_f32_tc3", "gemm_f32_tc3_ex"):
         need = int(lib.gemm_f32_tc3_workspace_size(M, N, K))
         ws = torch.empty(max(need, 1) + 256, dtype=torch.uint8, device=dC.buf.device)
         wptr = (ws.data_ptr() + 255) // 256 * 256
-        rc = lib.gemm_f32_tc3(M, N, K, dA.ptr, dA.ld, dB.ptr, dB.ld, dC.ptr, dC.ld, wptr, need,
-                              s.cuda_stream)
+        if entry == "gemm_f32_tc3":
+            assert trans == (0, 0)
+            rc = lib.gemm_f32_tc3(M, N, K, dA.ptr, dA.ld, dB.ptr, dB.ld, dC.ptr, dC.ld, wptr,
+                                  need, s.cuda_stream)
+        else:
+            rc = lib.gemm_f32_tc3_ex(ta, tb, M, N, K, dA.ptr, dA.ld, dB.ptr, dB.ld, dC.ptr,
+                                     dC.ld, wptr, need, s.cuda_stream)
+    elif entry == "gemm_f32_ex":
+        rc = lib.gemm_f32_ex(ta, tb, M, N, K, dA.ptr, dA.ld, dB.ptr, dB.ld, dC.ptr, dC.ld,
+                             s.cuda_stream)
     else:
-        rc = _abi.call(entry, M, N, K, dA.ptr, dA.ld, dB.ptr, dB.ld, dC.ptr, dC.ld,
-                       s.cuda_stream)
-    assert rc == _abi.TMM_OK, f"{entry} returned {rc}: {_abi.last_error()}"
+        assert trans == (0, 0)
+        rc = int(getattr(lib, entry)(M, N, K, dA.ptr, dA.ld, dB.ptr, dB.ld, dC.ptr, dC.ld,
+                                     s.cuda_stream))
+    msg = lib.tmm_last_error_string().decode(errors="replace")
+    assert rc == _abi.TMM_OK, f"{entry} returned {rc}: {msg}"
     torch.cuda.synchronize()
     if check_status:
-        assert _abi.load().tmm_check_device(s.cuda_stream) == _abi.TMM_OK, _abi.last_error()
+        st = lib.tmm_check_device(s.cuda_stream)
+        assert st == _abi.TMM_OK, (st, lib.tmm_last_error_string().decode(errors="replace"))
     if check_canaries:
         assert dC.outside_window_untouched(), f"{entry} wrote outside C's M x N window"
     return dC.window()

@@ -171,7 +171,7 @@ def test_boundary_contract_names_alias_the_library_names(lib):
     # Status codes: GEMM_ERR_* in the header equal the TMM_ERR_* codes, and the
     # binding carries both names.
     macros = _header_macros()
-    for suffix in ("INVALID_ARG", "ALIAS", "UNSUPPORTED_DEVICE", "CUDA", "DEVICE_TIMEOUT"):
+    for suffix in ("INVALID_ARG", "ALIAS", "UNSUPPORTED_DEVICE", "CUDA", "DEVICE_TIMEOUT", "BOUNDS"):
         g, t = _macro_value(macros, "GEMM_ERR_" + suffix), _macro_value(macros, "TMM_ERR_" + suffix)
         assert g == t == getattr(_abi, "GEMM_ERR_" + suffix) == getattr(_abi, "TMM_ERR_" + suffix)
     assert _macro_value(macros, "GEMM_OK") == _abi.TMM_OK == 0

@@ -18,6 +18,7 @@ TMM_ERR_ALIAS = -2
 TMM_ERR_UNSUPPORTED_DEVICE = -3
 TMM_ERR_CUDA = -4
 TMM_ERR_DEVICE_TIMEOUT = -5
+TMM_ERR_BOUNDS = -6          # the bounds-checked debug build only
 # The boundary contract's names for the same codes (GEMM_ERR_* in the header).
 GEMM_OK = TMM_OK
 GEMM_ERR_INVALID_ARG = TMM_ERR_INVALID_ARG
@@ -25,6 +26,7 @@ GEMM_ERR_ALIAS = TMM_ERR_ALIAS
 GEMM_ERR_UNSUPPORTED_DEVICE = TMM_ERR_UNSUPPORTED_DEVICE
 GEMM_ERR_CUDA = TMM_ERR_CUDA
 GEMM_ERR_DEVICE_TIMEOUT = TMM_ERR_DEVICE_TIMEOUT
+GEMM_ERR_BOUNDS = TMM_ERR_BOUNDS
 
 STATUS_NAMES = {
     TMM_OK: "TMM_OK",
@@ -33,6 +35,7 @@ STATUS_NAMES = {
     TMM_ERR_UNSUPPORTED_DEVICE: "TMM_ERR_UNSUPPORTED_DEVICE",
     TMM_ERR_CUDA: "TMM_ERR_CUDA",
     TMM_ERR_DEVICE_TIMEOUT: "TMM_ERR_DEVICE_TIMEOUT",
+    TMM_ERR_BOUNDS: "TMM_ERR_BOUNDS",
 }
 
 # Entry points with the common product signature

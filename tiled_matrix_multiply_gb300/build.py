@@ -18,6 +18,12 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libtmm_gemm.so")
+# The bounds-checked debug build (every global address and shared-memory offset
+# of the product kernels range-checked, see csrc/bounds_check.cuh): its own
+# objects and library, beside the normal ones.
+CHECKED_FLAGS = ["-DTMM_BOUNDS_CHECK"]
+CHECKED_BUILD_DIR = os.path.join(PKG, "_build_checked")
+CHECKED_LIB_PATH = os.path.join(LIB_DIR, "libtmm_gemm_checked.so")
 
 SOURCES = ["gemm_abi.cpp", "gemm_naive.cu", "gemm_simt.cu", "gemm_tc3.cu",
            "gemm_tc3_noalloc.cu", "window_sum.cu", "reduce_softmax.cu", "tensor_map.cpp"]
@@ -64,15 +70,15 @@ def source_digest(names: list[str] | None = None) -> str:
     return h.hexdigest()[:16]
 
 
-def is_fresh() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_fresh(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+def _compile(src: str, extra: list[str], build_dir: str) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [nvcc(), *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
@@ -80,20 +86,31 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(force: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Build libtmm_gemm.so unless an up-to-date copy exists; return its path."""
-    if not force and not extra_flags and is_fresh():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def _build(lib_path: str, build_dir: str, extra: list[str]) -> str:
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
-    extra = list(extra_flags or [])
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     with ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, extra, build_dir), srcs))
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc(), "-shared", *ARCH, "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{res.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+def build(force: bool = False, extra_flags: list[str] | None = None) -> str:
+    """Build libtmm_gemm.so unless an up-to-date copy exists; return its path."""
+    if not force and not extra_flags and is_fresh():
+        return LIB_PATH
+    return _build(LIB_PATH, BUILD_DIR, list(extra_flags or []))
+
+
+def build_checked(force: bool = False) -> str:
+    """Build the bounds-checked libtmm_gemm_checked.so (a debug build for the tests) unless
+    an up-to-date copy exists; return its path."""
+    if not force and is_fresh(CHECKED_LIB_PATH):
+        return CHECKED_LIB_PATH
+    return _build(CHECKED_LIB_PATH, CHECKED_BUILD_DIR, CHECKED_FLAGS)

@@ -9,9 +9,15 @@
 // ceil(N/16) x ceil(M/16) blocks, extra threads in the last blocks do nothing.
 //
 // It is the contrast kernel: its L1/L2 load traffic, not the FMA pipe, bounds it.
+#include "bounds_check.cuh"
 #include "tmm_internal.h"
 
 namespace tmm {
+
+// Status word of the naive kernel: bit 2 (kStatusBounds) when a range check of
+// the bounds-checked build failed.
+__device__ unsigned int g_naive_status;
+
 namespace {
 
 constexpr int kNaiveTile = 16;
@@ -30,12 +36,24 @@ gemm_naive_kernel(int64_t M, int64_t N, int64_t K,
     const float *a = A + i * lda;
     const float *b = B + j;
     float acc = 0.0f;
-    for (int64_t k = 0; k < K; ++k) acc = fmaf(a[k], b[k * ldb], acc);
-    C[i * ldc + j] = acc;
+    for (int64_t k = 0; k < K; ++k) {
+      if (TMM_IN_BOUNDS(in_matrix(a + k, A, M, K, lda) && in_matrix(b + k * ldb, B, K, N, ldb),
+                        &g_naive_status))
+        acc = fmaf(a[k], b[k * ldb], acc);
+    }
+    if (TMM_IN_BOUNDS(in_matrix(C + i * ldc + j, C, M, N, ldc), &g_naive_status))
+      C[i * ldc + j] = acc;
   }
 }
 
 }  // namespace
+
+cudaError_t naive_device_status(unsigned int *status, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, g_naive_status, sizeof(unsigned int));
+  if (e != cudaSuccess || !clear) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_naive_status, &zero, sizeof(unsigned int));
+}
 
 cudaError_t launch_naive(const GemmProblem &p, const DeviceInfo &, cudaStream_t stream) {
   const int64_t gx = (p.N + kNaiveTile - 1) / kNaiveTile;

@@ -60,6 +60,7 @@
 #include <atomic>
 #include <cstdint>
 
+#include "bounds_check.cuh"
 #include "tmm_internal.h"
 
 namespace tmm {
@@ -71,7 +72,8 @@ namespace tmm {
 constexpr int kFlagRegions = 16;
 constexpr int kMaxPersistentBlocks = 4096;
 __device__ unsigned int g_simt_flags[kFlagRegions * kMaxPersistentBlocks];
-// Device status word (bit 0: a stream-K wait ran out of time).
+// Device status word (bit 0: a stream-K wait ran out of time; bit 1: a TMA
+// wait did; bit 2: a range check of the bounds-checked build failed).
 __device__ unsigned int g_simt_status;
 
 namespace {
@@ -391,17 +393,38 @@ struct SimtBlock {
 
     // extra_tx: bytes the stage's barrier expects beyond the copies (testing
     // hook: a barrier that never completes).
+    // Stored shapes of A and B (for the range checks of the debug build).
+    constexpr bool kAStoredMK = kACopy == kCopyTransposing, kBStoredNK = kBCopy == kCopyTransposing;
+    const int64_t a_rows = kAStoredMK ? p.M : p.K, a_cols = kAStoredMK ? p.K : p.M;
+    const int64_t b_rows = kBStoredNK ? p.N : p.K, b_cols = kBStoredNK ? p.K : p.N;
+    (void)a_rows; (void)a_cols; (void)b_rows; (void)b_cols;
     auto issue_slice = [&](int s, int stage, uint32_t extra_tx) {
       const int k0 = s * BK;
       const uint32_t st_off = 4u * stage * kStageFloats;
+      const int64_t st_base = int64_t(smem_addr(smem) + st_off);
+      (void)st_base;
+      // A copy of `n` floats from src to shared address dst stays inside its
+      // matrix and its slab (debug build only).
+      auto a_ok = [&](uint32_t dst, const float *src, int n) {
+        return TMM_IN_BOUNDS(in_matrix(src, p.A, a_rows, a_cols, p.lda, n) &&
+                                 in_region(int64_t(dst) - st_base, kASlab, n),
+                             &g_simt_status);
+      };
+      auto b_ok = [&](uint32_t dst, const float *src, int n) {
+        return TMM_IN_BOUNDS(in_matrix(src, p.B, b_rows, b_cols, p.ldb, n) &&
+                                 in_region(int64_t(dst) - st_base - 4 * kASlab, BK * kBsLd, n),
+                             &g_simt_status);
+      };
+      (void)a_ok; (void)b_ok;
       if (kACopy == kCopyTransposing) {
         const float *a = a_src + k0;
 #pragma unroll
         for (int it = 0; it < Cf::kACopies; ++it) {
           const int r = it % Cf::kARowGroupsPerWarp, h = it / Cf::kARowGroupsPerWarp;
+          const uint32_t dst = a_dst0 + st_off + 4u * (8 * h * kAsLd + 4 * Cf::kWarps * r);
+          const float *src = a + r * a_step + 8 * h;
           const bool ok = ((a_rows_ok >> r) & 1u) && (k0 + t_k + 8 * h < p.K);
-          cp_async_4(a_dst0 + st_off + 4u * (8 * h * kAsLd + 4 * Cf::kWarps * r),
-                     a + r * a_step + 8 * h, ok, p.A);
+          cp_async_4(dst, src, ok && a_ok(dst, src, 1), p.A);
         }
       } else if (kACopy == kCopyVec) {
         constexpr int kRowsPerPass = Cf::kThreads / (Cf::BM / 4);
@@ -410,8 +433,10 @@ struct SimtBlock {
 #pragma unroll
         for (int v = 0; v < BK * Cf::BM / 4 / Cf::kThreads; ++v) {
           const int kr = a_k + kRowsPerPass * v;
-          cp_async_16(a_dst0 + st_off + 4u * (kRowsPerPass * v * kAsLd),
-                      a + int64_t(kRowsPerPass * v) * a_step, col_ok && (k0 + kr < p.K), p.A);
+          const uint32_t dst = a_dst0 + st_off + 4u * (kRowsPerPass * v * kAsLd);
+          const float *src = a + int64_t(kRowsPerPass * v) * a_step;
+          const bool ok = col_ok && (k0 + kr < p.K);
+          cp_async_16(dst, src, ok && a_ok(dst, src, 4), p.A);
         }
       } else if (kACopy == kCopyScalar) {
         constexpr int kColPasses = Cf::BM / 32;
@@ -420,8 +445,9 @@ struct SimtBlock {
         for (int it = 0; it < BK * Cf::BM / Cf::kThreads; ++it) {
           const int kr = Cf::kWarps * (it / kColPasses), c = it % kColPasses;
           const bool ok = (m0 + a_m + 32 * c < p.M) && (k0 + a_k + kr < p.K);
-          cp_async_4(a_dst0 + st_off + 4u * (kr * kAsLd + 32 * c),
-                     a + int64_t(kr) * a_step + 32 * c, ok, p.A);
+          const uint32_t dst = a_dst0 + st_off + 4u * (kr * kAsLd + 32 * c);
+          const float *src = a + int64_t(kr) * a_step + 32 * c;
+          cp_async_4(dst, src, ok && a_ok(dst, src, 1), p.A);
         }
       }
       if (kBCopy == kCopyTransposing) {
@@ -430,8 +456,9 @@ struct SimtBlock {
         for (int it = 0; it < Cf::BN / 4 / Cf::kWarps * (BK / 8); ++it) {
           const int r = it % (Cf::BN / 4 / Cf::kWarps), h = it / (Cf::BN / 4 / Cf::kWarps);
           const bool ok = ((b_rows_ok >> r) & 1u) && (k0 + t_k + 8 * h < p.K);
-          cp_async_4(b_dst0 + st_off + 4u * (8 * h * kBsLd + 4 * Cf::kWarps * r),
-                     b + r * b_step + 8 * h, ok, p.B);
+          const uint32_t dst = b_dst0 + st_off + 4u * (8 * h * kBsLd + 4 * Cf::kWarps * r);
+          const float *src = b + r * b_step + 8 * h;
+          cp_async_4(dst, src, ok && b_ok(dst, src, 1), p.B);
         }
       } else if (kBCopy == kCopyVec) {
         constexpr int kBRowsPerPass = Cf::kThreads / Cf::kBVecPerRow;
@@ -441,8 +468,9 @@ struct SimtBlock {
         for (int v = 0; v < Cf::kBVecCopies; ++v) {
           const int kr = b_k + kBRowsPerPass * v;
           const bool ok = col_ok && (k0 + kr < p.K);
-          cp_async_16(b_dst0 + st_off + 4u * (kBRowsPerPass * v * kBsLd),
-                      b + int64_t(kBRowsPerPass * v) * b_step, ok, p.B);
+          const uint32_t dst = b_dst0 + st_off + 4u * (kBRowsPerPass * v * kBsLd);
+          const float *src = b + int64_t(kBRowsPerPass * v) * b_step;
+          cp_async_16(dst, src, ok && b_ok(dst, src, 4), p.B);
         }
       } else if (kBCopy == kCopyScalar) {
         constexpr int kColPasses = Cf::BN / 32;
@@ -451,11 +479,16 @@ struct SimtBlock {
         for (int it = 0; it < Cf::kBScalarCopies; ++it) {
           const int kr = Cf::kWarps * (it / kColPasses), c = it % kColPasses;
           const bool ok = (n0 + b_n + 32 * c < p.N) && (k0 + b_k + kr < p.K);
-          cp_async_4(b_dst0 + st_off + 4u * (kr * kBsLd + 32 * c),
-                     b + int64_t(kr) * b_step + 32 * c, ok, p.B);
+          const uint32_t dst = b_dst0 + st_off + 4u * (kr * kBsLd + 32 * c);
+          const float *src = b + int64_t(kr) * b_step + 32 * c;
+          cp_async_4(dst, src, ok && b_ok(dst, src, 1), p.B);
         }
       }
       if (kTma && tid == 0 && !tma_dead) {
+        // The box origins lie inside the matrices (the copy fills the rest with zeros).
+        (void)TMM_IN_BOUNDS(k0 < p.K && (kBCopy != kCopyTma || n0 < p.N) &&
+                                (kACopy != kCopyTma || m0 < p.M),
+                            &g_simt_status);
         const uint32_t bar = bars + 8u * stage, st = smem_addr(smem) + st_off;
         mbar_arrive_expect_tx(bar, kTmaBytes + extra_tx);
         if (kACopy == kCopyTma) tma_load_2d(st, a_map, m0, k0, bar);
@@ -536,12 +569,19 @@ struct SimtBlock {
     const float *b = bs + k * kBsLd + b_off;
 #pragma unroll
     for (int t = 0; t < Cf::TM / 4; ++t) {
-      const float4 v = *reinterpret_cast<const float4 *>(a + 4 * Cf::LM * t);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (TMM_IN_BOUNDS(in_region(4 * (a + 4 * Cf::LM * t - as),
+                                  Cf::template a_slab_floats<kACopy>(), 4),
+                        &g_simt_status))
+        v = *reinterpret_cast<const float4 *>(a + 4 * Cf::LM * t);
       af[4 * t + 0] = v.x; af[4 * t + 1] = v.y; af[4 * t + 2] = v.z; af[4 * t + 3] = v.w;
     }
 #pragma unroll
     for (int c = 0; c < Cf::TN / 4; ++c) {
-      const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(b + 4 * Cf::LN * c);
+      ulonglong2 v = make_ulonglong2(0, 0);
+      if (TMM_IN_BOUNDS(in_region(4 * (b + 4 * Cf::LN * c - bs), Cf::BK * kBsLd, 4),
+                        &g_simt_status))
+        v = *reinterpret_cast<const ulonglong2 *>(b + 4 * Cf::LN * c);
       bf[2 * c + 0] = v.x; bf[2 * c + 1] = v.y;
     }
   }
@@ -601,7 +641,9 @@ struct SimtBlock {
           const float *c_row = c_base + int64_t(dr) * p.ldc;
 #pragma unroll
           for (int c = 0; c < Cf::TN / 4; ++c)
-            if (col0 + 4 * Cf::LN * c < p.N)
+            if (col0 + 4 * Cf::LN * c < p.N &&
+                TMM_IN_BOUNDS(in_matrix(c_row + 4 * Cf::LN * c, p.C, p.M, p.N, p.ldc, 4),
+                              &g_simt_status))
               w[i][c] = __ldcg(reinterpret_cast<const float4 *>(c_row + 4 * Cf::LN * c));
         }
       } else if (kAdd) {
@@ -615,10 +657,15 @@ struct SimtBlock {
           for (int c = 0; c < Cf::TN / 4; ++c) {
             const int dc = 4 * Cf::LN * c;
             const int left = p.N - (col0 + dc);
-            w[i][c].x = left > 0 ? __ldcg(c_row + dc + 0) : 0.f;
-            w[i][c].y = left > 1 ? __ldcg(c_row + dc + 1) : 0.f;
-            w[i][c].z = left > 2 ? __ldcg(c_row + dc + 2) : 0.f;
-            w[i][c].w = left > 3 ? __ldcg(c_row + dc + 3) : 0.f;
+            auto ld = [&](int j) {
+              return left > j && TMM_IN_BOUNDS(in_matrix(c_row + dc + j, p.C, p.M, p.N, p.ldc),
+                                               &g_simt_status)
+                         ? __ldcg(c_row + dc + j) : 0.f;
+            };
+            w[i][c].x = ld(0);
+            w[i][c].y = ld(1);
+            w[i][c].z = ld(2);
+            w[i][c].w = ld(3);
           }
         }
       }
@@ -641,13 +688,16 @@ struct SimtBlock {
                 v.x = w[i][c].x + v.x; v.y = w[i][c].y + v.y;
                 v.z = w[i][c].z + v.z; v.w = w[i][c].w + v.w;
               }
-              *reinterpret_cast<float4 *>(c_row + dc) = v;
+              if (TMM_IN_BOUNDS(in_matrix(c_row + dc, p.C, p.M, p.N, p.ldc, 4), &g_simt_status))
+                *reinterpret_cast<float4 *>(c_row + dc) = v;
             }
           } else {
             const float wv[4] = {w[i][c].x, w[i][c].y, w[i][c].z, w[i][c].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              if (col0 + dc + j < p.N) {
+              if (col0 + dc + j < p.N &&
+                  TMM_IN_BOUNDS(in_matrix(c_row + dc + j, p.C, p.M, p.N, p.ldc),
+                                &g_simt_status)) {
                 float v = a[4 * c + j];
                 if (kAdd) v = wv[j] + v;
                 c_row[dc + j] = v;

@@ -62,11 +62,14 @@
 #include <atomic>
 #include <cstdint>
 
+#include "bounds_check.cuh"
 #include "tmm_internal.h"
 
 namespace tmm {
 
-__device__ unsigned int g_tc3_status;   // bit 1: a bounded wait ran out of time
+// Status word: bit 1 when a bounded wait ran out of time, bit 2 when a range
+// check of the bounds-checked build failed.
+__device__ unsigned int g_tc3_status;
 // Split-tile flags, one per (tail block, accumulate warp): kTc3FlagRegions
 // rings; a call uses region epoch % kTc3FlagRegions and raises flags to its epoch.
 constexpr int kTc3FlagRegions = 16;
@@ -214,18 +217,24 @@ __global__ void tc3_split_a_kernel(int M, int K, int Kp, const float *__restrict
     const float *a = A + int64_t(m) * lda;
     float x[4];
     if (vec_load && k + 4 <= K) {
-      const float4 v = *reinterpret_cast<const float4 *>(a + k);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (TMM_IN_BOUNDS(in_matrix(a + k, A, M, K, lda, 4), &g_tc3_status))
+        v = *reinterpret_cast<const float4 *>(a + k);
       x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
     } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) x[j] = k + j < K ? a[k + j] : 0.0f;
+      for (int j = 0; j < 4; ++j)
+        x[j] = k + j < K && TMM_IN_BOUNDS(in_matrix(a + k + j, A, M, K, lda), &g_tc3_status)
+                   ? a[k + j] : 0.0f;
     }
     float h[4], l[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) split_tf32(x[j], h[j], l[j]);
     const int64_t o = int64_t(m) * Kp + k;
-    if (write_hi) *reinterpret_cast<float4 *>(hi + o) = make_float4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<float4 *>(lo + o) = make_float4(l[0], l[1], l[2], l[3]);
+    if (write_hi && TMM_IN_BOUNDS(in_matrix(hi + o, hi, M, Kp, Kp, 4), &g_tc3_status))
+      *reinterpret_cast<float4 *>(hi + o) = make_float4(h[0], h[1], h[2], h[3]);
+    if (TMM_IN_BOUNDS(in_matrix(lo + o, lo, M, Kp, Kp, 4), &g_tc3_status))
+      *reinterpret_cast<float4 *>(lo + o) = make_float4(l[0], l[1], l[2], l[3]);
   }
 }
 
@@ -242,7 +251,10 @@ __global__ void tc3_split_bt_kernel(int K, int N, int Kp, const float *__restric
 #pragma unroll
   for (int j = 0; j < 32; j += 8) {
     const int k = k0 + ty + j, n = n0 + tx;
-    tile[ty + j][tx] = (k < K && n < N) ? B[int64_t(k) * ldb + n] : 0.0f;
+    tile[ty + j][tx] = (k < K && n < N && TMM_IN_BOUNDS(in_matrix(B + int64_t(k) * ldb + n, B,
+                                                                   K, N, ldb),
+                                                         &g_tc3_status))
+                           ? B[int64_t(k) * ldb + n] : 0.0f;
   }
   __syncthreads();
 #pragma unroll
@@ -251,8 +263,12 @@ __global__ void tc3_split_bt_kernel(int K, int N, int Kp, const float *__restric
     if (n < N && k < Kp) {
       float h, l;
       split_tf32(tile[tx][ty + j], h, l);
-      hi[int64_t(n) * Kp + k] = h;
-      lo[int64_t(n) * Kp + k] = l;
+      if (TMM_IN_BOUNDS(in_matrix(hi + int64_t(n) * Kp + k, hi, N, Kp, Kp) &&
+                            in_matrix(lo + int64_t(n) * Kp + k, lo, N, Kp, Kp),
+                        &g_tc3_status)) {
+        hi[int64_t(n) * Kp + k] = h;
+        lo[int64_t(n) * Kp + k] = l;
+      }
     }
   }
 }
@@ -369,8 +385,9 @@ __device__ __forceinline__ void store_c_block(const Tc3Params &p, const float (&
     __syncwarp();   // the previous part's transposed reads are done
 #pragma unroll
     for (int q = 0; q < 8; ++q)
-      st_shared_v4(stg + uint32_t(lane * 128 + ((q ^ (lane & 7)) << 4)), acc[32 * b + 4 * q],
-                   acc[32 * b + 4 * q + 1], acc[32 * b + 4 * q + 2], acc[32 * b + 4 * q + 3]);
+      if (TMM_IN_BOUNDS(in_region(lane * 128 + ((q ^ (lane & 7)) << 4), 1024, 4), &g_tc3_status))
+        st_shared_v4(stg + uint32_t(lane * 128 + ((q ^ (lane & 7)) << 4)), acc[32 * b + 4 * q],
+                     acc[32 * b + 4 * q + 1], acc[32 * b + 4 * q + 2], acc[32 * b + 4 * q + 3]);
     __syncwarp();
     const int col = col0 + 32 * b + 4 * cq;
     const bool vec = p.vec_store && col + 4 <= p.N;
@@ -380,14 +397,18 @@ __device__ __forceinline__ void store_c_block(const Tc3Params &p, const float (&
 #pragma unroll
       for (int u = 0; u < kStoreBatch; ++u) {
         const int r = 4 * (kStoreBatch * h + u) + rsub;
-        v[u] = ld_shared_v4(stg + uint32_t(r * 128 + ((cq ^ (r & 7)) << 4)));
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (TMM_IN_BOUNDS(in_region(r * 128 + ((cq ^ (r & 7)) << 4), 1024, 4), &g_tc3_status))
+          v[u] = ld_shared_v4(stg + uint32_t(r * 128 + ((cq ^ (r & 7)) << 4)));
         w[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
       if (adds_prev && vec) {
 #pragma unroll
         for (int u = 0; u < kStoreBatch; ++u) {
           const int row = row_base + 4 * (kStoreBatch * h + u) + rsub;
-          if (row < p.M)
+          if (row < p.M && TMM_IN_BOUNDS(in_matrix(p.C + int64_t(row) * p.ldc + col, p.C, p.M,
+                                                   p.N, p.ldc, 4),
+                                         &g_tc3_status))
             w[u] = __ldcg(reinterpret_cast<const float4 *>(p.C + int64_t(row) * p.ldc + col));
         }
       }
@@ -401,11 +422,13 @@ __device__ __forceinline__ void store_c_block(const Tc3Params &p, const float (&
           if (adds_prev) {
             o.x = w[u].x + o.x; o.y = w[u].y + o.y; o.z = w[u].z + o.z; o.w = w[u].w + o.w;
           }
-          *reinterpret_cast<float4 *>(c_row + col) = o;
+          if (TMM_IN_BOUNDS(in_matrix(c_row + col, p.C, p.M, p.N, p.ldc, 4), &g_tc3_status))
+            *reinterpret_cast<float4 *>(c_row + col) = o;
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (col + j < p.N) {
+            if (col + j < p.N &&
+                TMM_IN_BOUNDS(in_matrix(c_row + col + j, p.C, p.M, p.N, p.ldc), &g_tc3_status)) {
               float o = f4_get(v[u], j);
               if (adds_prev) o = __ldcg(c_row + col + j) + o;
               c_row[col + j] = o;

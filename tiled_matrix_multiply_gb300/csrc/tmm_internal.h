@@ -43,6 +43,9 @@ cudaError_t encode_f32_2d(CUtensorMap *map, const float *base, int64_t rows, int
 // Each launcher enqueues its kernel(s) on `stream` and returns the launch
 // status.  Problems reaching a launcher have M, N, K > 0.
 cudaError_t launch_naive(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream);
+// Status word of the naive kernel (bit 2: a range check of the bounds-checked
+// build failed), read from the current device, optionally cleared.
+cudaError_t naive_device_status(unsigned int *status, bool clear);
 cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream);
 
 // Split-TF32 tensor-core path: workspace bytes for an M x N x K product
