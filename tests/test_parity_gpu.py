@@ -247,3 +247,20 @@ def test_repeat_calls_are_bit_identical():
     C1 = _run("gemm_f32", A, B)
     C2 = _run("gemm_f32", A, B)
     assert np.array_equal(C1.view(np.uint32), C2.view(np.uint32))
+
+
+# Shapes large enough for the 64 x 512 tiles of aligned A x B (their tiles fill two
+# waves of SMs), with tails in M, N and K: N a multiple of 4, and N odd with a
+# padded, aligned leading dimension (B staged by TMA either way).
+@pytest.mark.parametrize("M,N,K,ldb", [(4000, 2996, 1001, 2996), (4000, 3001, 1001, 3004),
+                                        (2500, 4100, 517, 4100)])
+def test_wide_tile_path_tails(M, N, K, ldb):
+    rng = np.random.default_rng(36)
+    A = rng.random((M, K), dtype=np.float32) * 2 - 1
+    B = rng.random((K, N), dtype=np.float32) * 2 - 1
+    C = _run("gemm_f32", A, B, ldb=ldb, check_canaries=False)
+    parity.assert_close(C, oracle.gemm(A, B), K, f"wide {M}x{N}x{K}")
+    Ai = rng.integers(-4, 5, (M, K)).astype(np.float32)
+    Bi = rng.integers(-4, 5, (K, N)).astype(np.float32)
+    Ci = _run("gemm_f32", Ai, Bi, ldb=ldb, ldc=N + 3)
+    parity.assert_bit_exact(Ci, oracle.gemm(Ai, Bi), f"wide int {M}x{N}x{K}")

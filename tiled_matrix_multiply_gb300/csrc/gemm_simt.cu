@@ -113,17 +113,26 @@ struct SimtConfig {
   __host__ __device__ static constexpr int as_ld() {
     return kACopy == kCopyTma ? BM : BM + 4;
   }
+  // A TMA copy moves boxes of at most 256 columns; a wider B slab is held as
+  // consecutive sub-slabs of kBBox columns.
+  static constexpr int kBBox = BN < 256 ? BN : 256;
   template <int kBCopy>
   __host__ __device__ static constexpr int bs_ld() {
-    return kBCopy == kCopyTransposing ? BN + 4 : BN;
+    return kBCopy == kCopyTransposing ? BN + 4 : kBCopy == kCopyTma ? kBBox : BN;
   }
   template <int kACopy>
   __host__ __device__ static constexpr int a_slab_floats() {
     return BK * as_ld<kACopy>();
   }
+  // The B slab: BK rows of pitch bs_ld (TMA copies of more than 256 columns land
+  // as consecutive sub-slabs of 256, so the slab is BK x BN either way).
+  template <int kBCopy>
+  __host__ __device__ static constexpr int b_slab_floats() {
+    return kBCopy == kCopyTransposing ? BK * (BN + 4) : BK * BN;
+  }
   template <int kACopy, int kBCopy>
   __host__ __device__ static constexpr int stage_floats() {
-    return a_slab_floats<kACopy>() + BK * bs_ld<kBCopy>();
+    return a_slab_floats<kACopy>() + b_slab_floats<kBCopy>();
   }
   template <int kACopy, int kBCopy>
   __host__ __device__ static constexpr bool uses_tma() {
@@ -301,7 +310,8 @@ struct SimtBlock {
   // Accumulators in pairs along N: acc[i][jp] holds columns 2 jp (lo), 2 jp + 1 (hi).
   uint64_t acc[Cf::TM][Cf::TN / 2];
   int lane, warp, tid;
-  int a_off, b_off;
+  int a_off, b_off;   // this thread's first row and column of the tile
+  int b_frag;         // offset of its first B column in the B slab
 
   __device__ __forceinline__ void init_lanes() {
     tid = threadIdx.x;
@@ -315,7 +325,11 @@ struct SimtBlock {
     const int wm = warp / Cf::kWarpsN, wn = warp % Cf::kWarpsN;
     a_off = wm * (Cf::LM * Cf::TM) + lm * 4;
     b_off = wn * (Cf::LN * Cf::TN) + ln * 4;
+    // A warp's columns lie in one sub-slab (checked below).
+    b_frag = kBCopy == kCopyTma ? (b_off / Cf::kBBox) * (Cf::BK * Cf::kBBox) + b_off % Cf::kBBox
+                                : b_off;
   }
+  static_assert(Cf::kBBox % (Cf::LN * Cf::TN) == 0, "a warp's B columns in one TMA box");
 
   // Row of C (relative to the block tile's a_off) of accumulator row r.
   __device__ __forceinline__ static constexpr int row_of(int r) {
@@ -412,7 +426,8 @@ struct SimtBlock {
       };
       auto b_ok = [&](uint32_t dst, const float *src, int n) {
         return TMM_IN_BOUNDS(in_matrix(src, p.B, b_rows, b_cols, p.ldb, n) &&
-                                 in_region(int64_t(dst) - st_base - 4 * kASlab, BK * kBsLd, n),
+                                 in_region(int64_t(dst) - st_base - 4 * kASlab,
+                                           Cf::template b_slab_floats<kBCopy>(), n),
                              &g_simt_status);
       };
       (void)a_ok; (void)b_ok;
@@ -492,7 +507,11 @@ struct SimtBlock {
         const uint32_t bar = bars + 8u * stage, st = smem_addr(smem) + st_off;
         mbar_arrive_expect_tx(bar, kTmaBytes + extra_tx);
         if (kACopy == kCopyTma) tma_load_2d(st, a_map, m0, k0, bar);
-        if (kBCopy == kCopyTma) tma_load_2d(st + 4u * kASlab, b_map, n0, k0, bar);
+        if (kBCopy == kCopyTma)
+#pragma unroll
+          for (int j = 0; j < Cf::BN / Cf::kBBox; ++j)
+            tma_load_2d(st + 4u * (kASlab + j * BK * Cf::kBBox), b_map, n0 + j * Cf::kBBox, k0,
+                        bar);
       }
     };
 
@@ -566,7 +585,7 @@ struct SimtBlock {
   __device__ __forceinline__ void load_frag(const float *as, const float *bs, int k,
                                             float (&af)[Cf::TM], uint64_t (&bf)[Cf::TN / 2]) {
     const float *a = as + k * kAsLd + a_off;
-    const float *b = bs + k * kBsLd + b_off;
+    const float *b = bs + k * kBsLd + b_frag;
 #pragma unroll
     for (int t = 0; t < Cf::TM / 4; ++t) {
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -579,7 +598,8 @@ struct SimtBlock {
 #pragma unroll
     for (int c = 0; c < Cf::TN / 4; ++c) {
       ulonglong2 v = make_ulonglong2(0, 0);
-      if (TMM_IN_BOUNDS(in_region(4 * (b + 4 * Cf::LN * c - bs), Cf::BK * kBsLd, 4),
+      if (TMM_IN_BOUNDS(in_region(4 * (b + 4 * Cf::LN * c - bs),
+                                  Cf::template b_slab_floats<kBCopy>(), 4),
                         &g_simt_status))
         v = *reinterpret_cast<const ulonglong2 *>(b + 4 * Cf::LN * c);
       bf[2 * c + 0] = v.x; bf[2 * c + 1] = v.y;
@@ -808,6 +828,11 @@ using SquareConfig = SimtConfig<8, 16, 2, 2, 16, 4, 2>;
 // SM, and 3 stages measured best (4000 x 3001 x 2047: 48.4 TFLOP/s against
 // 45.6; 4096 x 4095 x 4096: 54.5 against 50.0).
 using UnalignedBConfig = SimtConfig<8, 16, 2, 4, 16, 3, 1>;
+// B staged by TMA leaves A's transposing copies as the only per-thread ones;
+// a 64 x 512 tile on 8 warps (one block per SM, B in two 256-column boxes)
+// halves them per thread: 4096^3 64.5 against 63.9 TFLOP/s, 8192 x 8192 x 1024
+// 63.3 against 63.1.  Used when its tiles fill two waves of SMs.
+using WideNConfig = SimtConfig<8, 16, 1, 8, 16, 4, 1>;
 
 struct LaunchState {
   std::atomic<uint64_t> configured{0};   // bit per device: smem opt-in done
@@ -898,7 +923,8 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStre
     e = encode_f32_2d(&a_map, p.A, p.K, p.M, p.lda, Cf::BM, Cf::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   if (kBCopy == kCopyTma)       // B stored K x N: boxes of BN columns x BK rows, b[k][n]
-    e = encode_f32_2d(&b_map, p.B, p.K, p.N, p.ldb, Cf::BN, Cf::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+    e = encode_f32_2d(&b_map, p.B, p.K, p.N, p.ldb, Cf::kBBox, Cf::BK,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   SimtParams prm = {};
   bool coop = false;
@@ -941,8 +967,13 @@ cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_
   if (!p.transa) {
     if (p.transb)
       return launch_variant<SquareConfig, kCopyTransposing, kCopyTransposing>(p, dev, stream);
-    if (tma_b)
-      return launch_variant<Cf, kCopyTransposing, kCopyTma>(p, dev, stream);
+    if (tma_b) {
+      using W = WideNConfig;
+      const int64_t wide_tiles = (p.M + W::BM - 1) / W::BM * ((p.N + W::BN - 1) / W::BN);
+      return wide_tiles >= 2 * int64_t(dev.sm_count)
+                 ? launch_variant<W, kCopyTransposing, kCopyTma>(p, dev, stream)
+                 : launch_variant<Cf, kCopyTransposing, kCopyTma>(p, dev, stream);
+    }
     return wide_b ? launch_variant<UB, kCopyTransposing, kCopyScalar>(p, dev, stream)
                   : launch_variant<Cf, kCopyTransposing, kCopyScalar>(p, dev, stream);
   }
