@@ -48,3 +48,18 @@ def assert_bit_exact(C: np.ndarray, ref: np.ndarray, what: str = ""):
     bad = np.flatnonzero(C.view(np.uint32) != want.view(np.uint32))
     assert bad.size == 0, (f"{what}: {bad.size} entries differ, first at "
                            f"{np.unravel_index(bad[0], C.shape)}: {C.flat[bad[0]]} vs {want.flat[bad[0]]}")
+
+
+def assert_close_few_outputs(C: np.ndarray, A: np.ndarray, B: np.ndarray, what: str = ""):
+    """For products with only a handful of outputs, where the normwise ratio is a
+    single entry's relative error and cancellation (an entry far smaller than its
+    terms) can put any FP32 summation order above 1e-5: every entry within the
+    elementwise bar 1e-4 sqrt(K) and within the classical bound of an FP32 dot
+    product summed in any order, K 2^-24 sum_k |A_ik B_kj|."""
+    K = A.shape[1]
+    ref = A.astype(np.float64) @ B.astype(np.float64)
+    mag = np.abs(A.astype(np.float64)) @ np.abs(B.astype(np.float64))
+    assert np.all(np.isfinite(C)), f"{what}: non-finite entries"
+    err = np.abs(C.astype(np.float64) - ref)
+    assert np.all(err <= elementwise_tol(K)), f"{what}: max abs error {err.max():.3e}"
+    assert np.all(err <= K * 2.0 ** -24 * mag), f"{what}: beyond the FP32 dot-product bound"

@@ -55,7 +55,12 @@ def test_stream_k_shapes_float(shape):
     A = rng.random((M, K), dtype=np.float32) * 2 - 1
     B = rng.random((K, N), dtype=np.float32) * 2 - 1
     C = _run("gemm_f32", A, B, check_canaries=False)
-    parity.assert_close(C, oracle.gemm(A, B), K, f"stream-K {shape}")
+    ref = oracle.gemm(A, B)
+    if M * N < 16:   # a single output: its own error bound, not a normwise ratio
+        parity.assert_close_few_outputs(C, A, B, f"stream-K {shape}")
+        assert np.max(np.abs(C - ref)) <= parity.elementwise_tol(K)
+    else:
+        parity.assert_close(C, ref, K, f"stream-K {shape}")
     assert _abi.load().tmm_check_device(torch.cuda.current_stream().cuda_stream) == _abi.TMM_OK
 
 

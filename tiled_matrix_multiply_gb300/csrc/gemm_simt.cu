@@ -300,7 +300,18 @@ struct SimtParams {
   unsigned int epoch;    // this call's flag value (never 0)
   int64_t wait_limit_ns; // bound on a stream-K wait
   int drop_signal_block; // testing hook: this block never raises its flag (-1: none)
+  // Small problems split per tile (parts > 0): tile t's K-slices go to blocks
+  // t * parts .. t * parts + parts - 1 in unequal parts; part q holds
+  // part_base + (parts - 1 - q) * part_step slices (part 0 also the remainder).
+  int parts, part_base, part_step, part_rem;
 };
+
+// First K-slice of part q of a tile split per tile (q == parts: the tile's end).
+__device__ __forceinline__ int part_begin(const SimtParams &p, int q) {
+  if (q >= p.parts) return p.slices;
+  return q * p.part_base + p.part_step * (q * (p.parts - 1) - q * (q - 1) / 2) +
+         (q > 0 ? p.part_rem : 0);
+}
 
 // One block's work on tile `tile`, K-slices [s_begin, s_end).  kACopy, kBCopy:
 // how the A and B slabs are copied (kCopyTransposing for A stored M x K and B
@@ -761,11 +772,18 @@ gemm_simt_kernel(const __grid_constant__ CUtensorMap a_map,
   }
   if (p.sk_iters == 0) return;
 
-  // This block's share of the split tiles' K-slices.
+  // This block's share of the split tiles' K-slices: an even share of all of
+  // them, or one part of one tile.
   const int64_t g = gridDim.x, b = blockIdx.x;
-  const int64_t it_end = (b + 1) * p.sk_iters / g;
+  int64_t it_start = b * p.sk_iters / g, it_end = (b + 1) * p.sk_iters / g;
+  if (p.parts > 0) {
+    const int64_t t = b / p.parts;
+    const int q = int(b - t * p.parts);
+    it_start = t * p.slices + part_begin(p, q);
+    it_end = t * p.slices + part_begin(p, q + 1);
+  }
   unsigned int *flags = g_simt_flags + (p.epoch % kFlagRegions) * kMaxPersistentBlocks;
-  for (int64_t it = b * p.sk_iters / g; it < it_end;) {
+  for (int64_t it = it_start; it < it_end;) {
     const int tile = p.dp_tiles + int(it / p.slices);
     const int s_begin = int(it % p.slices);
     const int64_t rest = it_end - it;
@@ -851,6 +869,12 @@ std::atomic<int> g_drop_signal_block{-1};
 // least a quarter of a tile and four slices), when that gives at least an
 // eighth more blocks than tiles.  Both schemes need the blocks co-resident
 // (*cooperative) and `flags_per_block` flags per block.
+// Slices by which each part of a tile split per tile is longer than the next
+// (measured, TFLOP/s for steps 0 / 1 / 2 / 3: 1024^3 34.6 / 35.8 / 35.8 / 32.4;
+// 1000 x 1000 x 2990 44.0 / 44.7 / 42.7 / 42.7; the even split across tile
+// boundaries before: 35.2 and 41.5).
+constexpr int kChainStep = 1;
+
 int64_t plan_simt(SimtParams &prm, const GemmProblem &p, int BM, int BN, int BK, int64_t slots,
                   int flags_per_block, bool *cooperative) {
   const int64_t tiles_m = (p.M + BM - 1) / BM;
@@ -870,13 +894,31 @@ int64_t plan_simt(SimtParams &prm, const GemmProblem &p, int BM, int BN, int BK,
   const bool stream_k = flags_fit && tiles > slots && rem != 0 && rem * 10 < slots * 9 &&
                         slices >= 4;
   int64_t small_blocks = 0;
+  prm.parts = 0;
   if (!stream_k && flags_fit && tiles < slots) {
-    const int64_t iters = tiles * slices;
-    int64_t share = (iters + slots - 1) / slots;
-    share = share > (slices + 3) / 4 ? share : (slices + 3) / 4;
-    share = share > 4 ? share : 4;
-    const int64_t g = (iters + share - 1) / share;
-    if (g * 8 >= tiles * 9) small_blocks = g;
+    // With room for at least two blocks per tile: each tile in `parts` parts
+    // (up to four, of at least four slices), the part holding the end of K --
+    // the first of the tile's chain to store its sum -- the smallest, and each
+    // earlier part kChainStep slices longer, so the sum handed down the chain
+    // arrives while the part receiving it still computes.
+    const int64_t parts = std::min<int64_t>({4, slots / tiles, slices / 4});
+    if (parts >= 2) {
+      int step = kChainStep;
+      while (step > 0 && slices - step * parts * (parts - 1) / 2 < 4 * parts) --step;
+      const int base = int((slices - step * parts * (parts - 1) / 2) / parts);
+      prm.parts = int(parts);
+      prm.part_step = step;
+      prm.part_base = base;
+      prm.part_rem = int(slices - step * parts * (parts - 1) / 2 - base * parts);
+      small_blocks = tiles * parts;
+    } else {
+      const int64_t iters = tiles * slices;
+      int64_t share = (iters + slots - 1) / slots;
+      share = share > (slices + 3) / 4 ? share : (slices + 3) / 4;
+      share = share > 4 ? share : 4;
+      const int64_t g = (iters + share - 1) / share;
+      if (g * 8 >= tiles * 9) small_blocks = g;
+    }
   }
   *cooperative = stream_k || small_blocks > 0;
   if (*cooperative) {
