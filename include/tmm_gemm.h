@@ -26,12 +26,13 @@
  *                Caller-owned; read only.  Pointers must be 4-byte aligned
  *                (natural float alignment).  Rows that all start on 16-byte
  *                boundaries (16-byte aligned base, leading dimension a
- *                multiple of 4) are faster: on the FFMA path B stored K x N
- *                (and A stored K x M) is then read in 16-byte vectors, else
- *                element by element, which costs gemm_f32 a noticeable part
- *                of its throughput when B's rows are unaligned; on the
- *                tensor-core path an operand stored K-major is then read in
- *                place as its own TF32 high part.
+ *                multiple of 4) save a copy: on the FFMA path B stored K x N
+ *                (and A stored K x M) is then read in place by TMA, where
+ *                any other B (stored N x K, or with unaligned rows) and A
+ *                stored K x M with unaligned rows are first restaged into a
+ *                scratch copy with 16-byte rows (one more read and write of
+ *                the operand); on the tensor-core path an operand stored
+ *                K-major is then read in place as its own TF32 high part.
  *   lda, ldb     leading dimensions in elements: lda >= max(1, K),
  *                ldb >= max(1, N).
  *   C            DEVICE pointer to the FP32 row-major result, caller-owned,
@@ -41,13 +42,21 @@
  *                the legacy default stream.  Every call is asynchronous: it
  *                returns once the kernel is enqueued; the caller synchronises.
  *
- * The library allocates no device or host memory per call.  All entry points
+ * Memory: gemm_f32 and gemm_f32_ex take the scratch of a restaged operand
+ * (K x N rounded up to a multiple of 4 floats for B, K x M likewise for A)
+ * from a stream-ordered memory pool the library creates per device: it is
+ * allocated on `stream` before the copy and freed on `stream` after the
+ * product, so calls on different streams never share it, and the pool keeps
+ * the freed memory for later calls (for the life of the process).  No other
+ * entry point allocates device or host memory per call.  All entry points
  * use the current CUDA device (cudaSetDevice) and are thread-safe.
  *
  * Return value: TMM_OK (0) when the work was enqueued, otherwise one of the
- * negative TMM_ERR_* codes below, in which case nothing was launched.  No
- * exception crosses the ABI and nothing is printed; tmm_last_error_string()
- * gives a one-line description of the calling thread's last failure.
+ * negative TMM_ERR_* codes below (TMM_ERR_CUDA also when the scratch of a
+ * restaged operand cannot be allocated); argument errors are found before
+ * anything is launched.  No exception crosses the ABI and nothing is
+ * printed; tmm_last_error_string() gives a one-line description of the
+ * calling thread's last failure.
  */
 #ifndef TMM_GEMM_H
 #define TMM_GEMM_H
@@ -130,9 +139,10 @@ int gemm_f32(int64_t M, int64_t N, int64_t K,
  *                         op(B) = B   (transb = 0, B stored K x N, ldb >= max(1, N))
  *                                 B^T (transb = 1, B stored N x K, ldb >= max(1, K)).
  * transa = 1, transb = 0 is the layout of "CMU DLSys Lecture 12" section 4,
- * C_ij = sum_k A_ki B_kj.  Only the copy of the slabs into shared memory
- * changes with the layout (the shared-memory slabs are k-major in every
- * case); the register tiles, scheduling and contract are gemm_f32's.
+ * C_ij = sum_k A_ki B_kj.  Only the way the operands reach the k-major
+ * shared-memory slabs changes with the layout: A stored K x M is copied by
+ * TMA, B stored N x K is first transposed into a K x N scratch copy (see
+ * Memory above); the register tiles, scheduling and contract are gemm_f32's.
  * TMM_ERR_INVALID_ARG also for transa or transb not 0 or 1.
  */
 int gemm_f32_ex(int transa, int transb,

@@ -26,7 +26,8 @@ CHECKED_BUILD_DIR = os.path.join(PKG, "_build_checked")
 CHECKED_LIB_PATH = os.path.join(LIB_DIR, "libtmm_gemm_checked.so")
 
 SOURCES = ["gemm_abi.cpp", "gemm_naive.cu", "gemm_simt.cu", "gemm_tc3.cu",
-           "gemm_tc3_noalloc.cu", "window_sum.cu", "reduce_softmax.cu", "tensor_map.cpp"]
+           "gemm_tc3_noalloc.cu", "window_sum.cu", "reduce_softmax.cu", "tensor_map.cpp",
+           "operand_stage.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC] + ARCH

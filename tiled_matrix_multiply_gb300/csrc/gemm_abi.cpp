@@ -184,19 +184,22 @@ int tmm_check_device(tmm_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return fail(TMM_ERR_CUDA, "tmm_check_device: cudaStreamSynchronize: %s", cudaGetErrorString(e));
-  unsigned int simt = 0, tc3 = 0, win = 0, sm = 0, naive = 0;
+  unsigned int simt = 0, tc3 = 0, win = 0, sm = 0, naive = 0, stage = 0;
   e = tmm::simt_device_status(&simt, true);
   if (e == cudaSuccess) e = tmm::tc3_device_status(&tc3, true);
   if (e == cudaSuccess) e = tmm::window_device_status(&win, true);
   if (e == cudaSuccess) e = tmm::softmax_device_status(&sm, true);
   if (e == cudaSuccess) e = tmm::naive_device_status(&naive, true);
+  if (e == cudaSuccess) e = tmm::stage_device_status(&stage, true);
   if (e != cudaSuccess)
     return fail(TMM_ERR_CUDA, "tmm_check_device: status read: %s", cudaGetErrorString(e));
-  if ((simt | tc3 | naive) & tmm::kStatusBounds)
+  if ((simt | tc3 | naive | stage) & tmm::kStatusBounds)
     return fail(TMM_ERR_BOUNDS,
                 "tmm_check_device: a range check of the bounds-checked build failed inside %s",
-                (simt & tmm::kStatusBounds) ? "gemm_f32"
-                : (tc3 & tmm::kStatusBounds) ? "gemm_f32_tc3" : "gemm_f32_naive");
+                (simt & tmm::kStatusBounds)    ? "gemm_f32"
+                : (stage & tmm::kStatusBounds) ? "gemm_f32 (operand restaging)"
+                : (tc3 & tmm::kStatusBounds)   ? "gemm_f32_tc3"
+                                               : "gemm_f32_naive");
   if (simt | tc3 | win | sm)
     return fail(TMM_ERR_DEVICE_TIMEOUT,
                 "tmm_check_device: a bounded wait inside %s ran out of time; the affected "

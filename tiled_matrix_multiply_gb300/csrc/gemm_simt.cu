@@ -4,25 +4,27 @@
 //   * block tile: each block owns a BM x BN tile of C (64 x 256 with 1 x 4
 //     warps in the default configuration; two blocks resident per SM);
 //   * K-slices of BK flow through a ring of kStages shared-memory stages
-//     filled by asynchronous copies (cp.async).  This generalises the double
-//     buffer of "Tiling Strategies" section 3: the copies of the next
+//     filled by asynchronous copies (TMA and cp.async).  This generalises the
+//     double buffer of "Tiling Strategies" section 3: the copies of the next
 //     kStages - 1 slices are in flight while one slice is consumed, and no
 //     register holds staged data;
 //   * thread tile: each thread owns a TM x TN tile of C in registers and
 //     performs one outer product per k (TM + TN operands, TM*TN FFMA), with
-//     the operands of step k+1 loaded from shared memory while step k's FFMAs
-//     issue ("Tiling Hierarchy on GPUs", "Register Tiling", "Register
-//     prefetching", "Reducing Overhead Slots").
+//     the operands of step k+2 (k+1 when A is copied by TMA) loaded from
+//     shared memory while step k's FFMAs issue ("Tiling Hierarchy on GPUs",
+//     "Register Tiling", "Register prefetching", "Reducing Overhead Slots").
 //
 // Shared-memory layout.  The A slab is stored transposed, a[k][m], so a
 // thread's rows of A at one k are 16-byte vectors; from A stored M x K it is
 // filled by 4-byte copies, each warp copying 4 rows x 8 consecutive k (four
-// 32-byte global sectors) into 32 distinct banks (row length BM + 4 floats).
-// The B slab keeps B's layout b[k][n] and is filled by 16-byte copies of
-// whole row segments when every row of B starts on a 16-byte boundary
-// (4-byte copies otherwise).  The layouts that read A stored K x M or B
-// stored N x K use the same copies with the roles exchanged (see the copy
-// kinds below).
+// 32-byte global sectors) into 32 distinct banks (row length BM + 4 floats);
+// from A stored K x M (the A^T B layouts) by one TMA copy per K-slice.  The B
+// slab keeps the layout b[k][n] and is always filled by TMA, one copy of the
+// whole slab per K-slice issued by one thread: B stored K x N with rows on
+// 16-byte boundaries is read in place, any other B (stored N x K, or rows of
+// a pitch that is not a multiple of 4 floats) is first restaged into that
+// layout by a copy kernel (operand_stage.cu).  A stored K x M without
+// 16-byte rows is restaged the same way.
 //
 // Warp tiling ("Tiling Hierarchy on GPUs", "Warp Tiling"): the 32 lanes of a
 // warp form an LM x LN grid (4 x 8 or 8 x 4); lane (lm, ln) owns rows
@@ -80,18 +82,15 @@ namespace {
 
 constexpr int kGroupM = 16;
 
-// How an operand slab reaches its k-major shared-memory layout:
-//   kCopyTransposing  -- the stored rows run along m (A) or n (B) with k contiguous,
-//                        so each element is placed by a 4-byte copy (4 rows x 8 k per
-//                        warp instruction, into 32 distinct banks);
-//   kCopyVec          -- the stored rows run along k, contiguous in m or n, 16-byte
-//                        aligned: whole 16-byte vectors;
-//   kCopyScalar       -- as kCopyVec without the alignment: 4-byte copies;
-//   kCopyTma          -- as kCopyVec, by TMA: one copy of the whole slab per
-//                        K-slice (B stored K x N, A stored K x M), issued by one
-//                        thread and counted on the stage's mbarrier; no
-//                        per-thread copy instructions.
-constexpr int kCopyTransposing = 0, kCopyVec = 1, kCopyScalar = 2, kCopyTma = 3;
+// How the A slab reaches its k-major shared-memory layout:
+//   kCopyTransposing  -- A stored M x K (k contiguous): each element is placed
+//                        by a 4-byte copy (4 rows x 8 k per warp instruction,
+//                        into 32 distinct banks);
+//   kCopyTma          -- A stored K x M with 16-byte rows: one TMA copy of the
+//                        whole slab per K-slice, issued by one thread and
+//                        counted on the stage's mbarrier with B's copy.
+// The B slab is always copied by TMA.
+constexpr int kCopyTransposing = 0, kCopyTma = 3;
 
 template <int TM_, int TN_, int kWarpsM_, int kWarpsN_, int BK_, int kStages_, int kMinBlocks_>
 struct SimtConfig {
@@ -106,67 +105,45 @@ struct SimtConfig {
   static constexpr int kThreads = 32 * kWarpsM * kWarpsN;
   static constexpr int kWarps = kWarpsM * kWarpsN;
   static constexpr int kMinBlocks = kMinBlocks_;
-  // Row pitches of the k-major slabs; both are 4 mod 32 floats when filled by
-  // transposing copies, which spreads a warp's 4 rows x 8 k over 32 banks.
-  // A TMA copy writes its box densely.
+  // Row pitch of the k-major A slab: 4 mod 32 floats when filled by
+  // transposing copies, which spreads a warp's 4 rows x 8 k over 32 banks; a
+  // TMA copy writes its box densely.
   template <int kACopy>
   __host__ __device__ static constexpr int as_ld() {
     return kACopy == kCopyTma ? BM : BM + 4;
   }
   // A TMA copy moves boxes of at most 256 columns; a wider B slab is held as
-  // consecutive sub-slabs of kBBox columns.
+  // consecutive sub-slabs of kBBox columns (BK x BN floats either way).
   static constexpr int kBBox = BN < 256 ? BN : 256;
-  template <int kBCopy>
-  __host__ __device__ static constexpr int bs_ld() {
-    return kBCopy == kCopyTransposing ? BN + 4 : kBCopy == kCopyTma ? kBBox : BN;
-  }
+  static constexpr int kBsLd = kBBox;
   template <int kACopy>
   __host__ __device__ static constexpr int a_slab_floats() {
     return BK * as_ld<kACopy>();
   }
-  // The B slab: BK rows of pitch bs_ld (TMA copies of more than 256 columns land
-  // as consecutive sub-slabs of 256, so the slab is BK x BN either way).
-  template <int kBCopy>
-  __host__ __device__ static constexpr int b_slab_floats() {
-    return kBCopy == kCopyTransposing ? BK * (BN + 4) : BK * BN;
-  }
-  template <int kACopy, int kBCopy>
+  static constexpr int kBSlabFloats = BK * BN;
+  template <int kACopy>
   __host__ __device__ static constexpr int stage_floats() {
-    return a_slab_floats<kACopy>() + b_slab_floats<kBCopy>();
+    return a_slab_floats<kACopy>() + kBSlabFloats;
   }
-  template <int kACopy, int kBCopy>
-  __host__ __device__ static constexpr bool uses_tma() {
-    return kACopy == kCopyTma || kBCopy == kCopyTma;
-  }
-  // With TMA copies the ring starts on a 128-byte boundary (the TMA
-  // destination rule), and is followed by one mbarrier per stage.
-  template <int kACopy, int kBCopy>
+  // The ring starts on a 128-byte boundary (the TMA destination rule) and is
+  // followed by one mbarrier per stage.
+  template <int kACopy>
   __host__ __device__ static constexpr int smem_bytes() {
-    return kStages * stage_floats<kACopy, kBCopy>() * 4 +
-           (uses_tma<kACopy, kBCopy>() ? 128 + 8 * kStages : 0);
+    return kStages * stage_floats<kACopy>() * 4 + 128 + 8 * kStages;
   }
   // A copies: groups of 4 rows x 8 k per warp instruction.
   static constexpr int kARowGroups = BM / 4;
   static constexpr int kARowGroupsPerWarp = kARowGroups / kWarps;
   static constexpr int kACopies = kARowGroupsPerWarp * (BK / 8);
-  // B copies.
-  static constexpr int kBVecPerRow = BN / 4;
-  static constexpr int kBVecCopies = BK * BN / 4 / kThreads;
-  static constexpr int kBScalarCopies = BK * BN / kThreads;
-  static constexpr int kKUnroll = BK;   // the whole slice unrolled (fits the instruction cache)
 
   static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tiles are made of 4 x 4 quadrants");
-  static_assert(BK % 8 == 0 && BK % kKUnroll == 0, "slice depth");
+  static_assert(BK % 8 == 0, "slice depth");
   static_assert(kARowGroups % kWarps == 0, "A copy groups divide among warps");
-  static_assert((BN / 4) % kWarps == 0, "transposing B copy groups divide among warps");
-  static_assert(kThreads % (BM / 4) == 0 && (BK * BM) % (4 * kThreads) == 0 &&
-                (BK * BM) % kThreads == 0 && BM % 32 == 0, "direct A copies");
-  static_assert((BM + 4) % 32 == 4 && (BN + 4) % 32 == 4, "pitches for transposing copies");
-  static_assert(kThreads % kBVecPerRow == 0, "B vector copies cover whole rows");
-  static_assert((BK * BN) % (4 * kThreads) == 0 && (BK * BN) % kThreads == 0, "B copies");
-  static_assert(BN % 32 == 0, "scalar B copies: a warp copies 32 consecutive columns");
+  static_assert((BM + 4) % 32 == 4, "pitch for transposing copies");
+  static_assert(BN % kBBox == 0, "whole TMA boxes of B");
   static_assert((BK * (BM + 4) * 4) % 128 == 0 && (BK * BM * 4) % 128 == 0 &&
-                (BK * BN * 4) % 128 == 0, "TMA destinations on 128-byte boundaries");
+                (BK * BN * 4) % 128 == 0 && (BK * kBBox * 4) % 128 == 0,
+                "TMA destinations on 128-byte boundaries");
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -293,7 +270,6 @@ struct SimtParams {
   float *C;
   int64_t ldc;
   int tiles_m, tiles_n;
-  int vec_store;         // C 16-byte aligned and ldc, N multiples of 4
   int slices;            // K-slices per tile
   int dp_tiles;          // tiles [0, dp_tiles) are processed whole, striding by gridDim.x
   int64_t sk_iters;      // (tiles - dp_tiles) * slices, divided evenly among the blocks
@@ -313,10 +289,11 @@ __device__ __forceinline__ int part_begin(const SimtParams &p, int q) {
          (q > 0 ? p.part_rem : 0);
 }
 
-// One block's work on tile `tile`, K-slices [s_begin, s_end).  kACopy, kBCopy:
-// how the A and B slabs are copied (kCopyTransposing for A stored M x K and B
-// stored N x K; kCopyVec / kCopyScalar for A stored K x M and B stored K x N).
-template <class Cf, int kACopy, int kBCopy>
+// One block's work on tile `tile`, K-slices [s_begin, s_end).  kACopy: how
+// the A slab is copied (kCopyTransposing for A stored M x K, kCopyTma for A
+// stored K x M).  kVecC: C takes 16-byte stores (C 16-byte aligned, ldc and N
+// multiples of 4), decided per call; element-wise stores otherwise.
+template <class Cf, int kACopy, bool kVecC>
 struct SimtBlock {
   // Accumulators in pairs along N: acc[i][jp] holds columns 2 jp (lo), 2 jp + 1 (hi).
   uint64_t acc[Cf::TM][Cf::TN / 2];
@@ -337,8 +314,7 @@ struct SimtBlock {
     a_off = wm * (Cf::LM * Cf::TM) + lm * 4;
     b_off = wn * (Cf::LN * Cf::TN) + ln * 4;
     // A warp's columns lie in one sub-slab (checked below).
-    b_frag = kBCopy == kCopyTma ? (b_off / Cf::kBBox) * (Cf::BK * Cf::kBBox) + b_off % Cf::kBBox
-                                : b_off;
+    b_frag = (b_off / Cf::kBBox) * (Cf::BK * Cf::kBBox) + b_off % Cf::kBBox;
   }
   static_assert(Cf::kBBox % (Cf::LN * Cf::TN) == 0, "a warp's B columns in one TMA box");
 
@@ -360,89 +336,38 @@ struct SimtBlock {
                                            const CUtensorMap *b_map, uint32_t bars,
                                            uint32_t &phases) {
     constexpr int BK = Cf::BK, kAsLd = Cf::template as_ld<kACopy>();
-    constexpr int kBsLd = Cf::template bs_ld<kBCopy>();
+    constexpr int kBsLd = Cf::kBsLd;
     constexpr int kASlab = Cf::template a_slab_floats<kACopy>();
-    constexpr int kStageFloats = Cf::template stage_floats<kACopy, kBCopy>();
+    constexpr int kStageFloats = Cf::template stage_floats<kACopy>();
     constexpr int kStages = Cf::kStages;
-    constexpr bool kTma = Cf::template uses_tma<kACopy, kBCopy>();
     constexpr bool kTmaA = kACopy == kCopyTma;
-    constexpr uint32_t kTmaBytes =
-        (kTmaA ? kASlab * 4 : 0) + (kBCopy == kCopyTma ? BK * Cf::BN * 4 : 0);
+    constexpr uint32_t kTmaBytes = (kTmaA ? kASlab * 4 : 0) + Cf::kBSlabFloats * 4;
 
-    // Transposing copies (A stored M x K, B stored N x K): warp instruction
-    // (r, h) copies rows 4 (warp + kWarps r) + lane/8 of the tile, k 8 h + lane % 8.
+    // Transposing copies of A (stored M x K): warp instruction (r, h) copies
+    // rows 4 (warp + kWarps r) + lane/8 of the tile, k 8 h + lane % 8.
     const int t_row = (lane >> 3) + 4 * warp;
     const int t_k = lane & 7;
-    // Direct copies (A stored K x M, B stored K x N): vector v is k row
-    // tid / (E/4) + v (threads / (E/4)) of the slab, columns 4 (tid % (E/4));
-    // scalar it is k row warp + kWarps (it / (E/32)), column lane + 32 (it % (E/32)),
-    // E = BM or BN.
-    const float *a_src;
-    int64_t a_step;            // between copy groups (transposing) or slab rows (direct)
-    uint32_t a_rows_ok = 0;    // transposing: bit r: row t_row + 4 kWarps r inside M
-    int a_k = 0, a_m = 0;      // direct: this thread's k row and column in the slab
-    uint32_t a_dst0;
-    if (kACopy == kCopyTransposing) {
+    const float *a_src = p.A;
+    int64_t a_step = 0;        // between copy groups
+    uint32_t a_rows_ok = 0;    // bit r: row t_row + 4 kWarps r inside M
+    uint32_t a_dst0 = 0;
+    if (!kTmaA) {
 #pragma unroll
       for (int r = 0; r < Cf::kARowGroupsPerWarp; ++r)
         a_rows_ok |= uint32_t(m0 + t_row + 4 * Cf::kWarps * r < p.M) << r;
       a_src = p.A + int64_t(min(m0 + t_row, p.M - 1)) * p.lda + t_k;
       a_step = int64_t(4 * Cf::kWarps) * p.lda;
       a_dst0 = smem_addr(smem) + 4u * (t_k * kAsLd + t_row);
-    } else {
-      a_k = kACopy == kCopyVec ? tid / (Cf::BM / 4) : warp;
-      a_m = kACopy == kCopyVec ? (tid % (Cf::BM / 4)) * 4 : lane;
-      a_src = p.A + int64_t(a_k) * p.lda + min(m0 + a_m, p.M - 1);
-      a_step = p.lda;
-      a_dst0 = smem_addr(smem) + 4u * (a_k * kAsLd + a_m);
-    }
-    const float *b_src;
-    int64_t b_step;
-    uint32_t b_rows_ok = 0;
-    int b_k = 0, b_n = 0;
-    uint32_t b_dst0;
-    if (kBCopy == kCopyTransposing) {
-#pragma unroll
-      for (int r = 0; r < Cf::BN / 4 / Cf::kWarps; ++r)
-        b_rows_ok |= uint32_t(n0 + t_row + 4 * Cf::kWarps * r < p.N) << r;
-      b_src = p.B + int64_t(min(n0 + t_row, p.N - 1)) * p.ldb + t_k;
-      b_step = int64_t(4 * Cf::kWarps) * p.ldb;
-      b_dst0 = smem_addr(smem) + 4u * (kASlab + t_k * kBsLd + t_row);
-    } else {
-      b_k = kBCopy == kCopyVec ? tid / Cf::kBVecPerRow : warp;
-      b_n = kBCopy == kCopyVec ? (tid % Cf::kBVecPerRow) * 4 : lane;
-      b_src = p.B + int64_t(b_k) * p.ldb + min(n0 + b_n, p.N - 1);
-      b_step = p.ldb;
-      b_dst0 = smem_addr(smem) + 4u * (kASlab + b_k * kBsLd + b_n);
     }
 
     // extra_tx: bytes the stage's barrier expects beyond the copies (testing
     // hook: a barrier that never completes).
-    // Stored shapes of A and B (for the range checks of the debug build).
-    constexpr bool kAStoredMK = kACopy == kCopyTransposing, kBStoredNK = kBCopy == kCopyTransposing;
-    const int64_t a_rows = kAStoredMK ? p.M : p.K, a_cols = kAStoredMK ? p.K : p.M;
-    const int64_t b_rows = kBStoredNK ? p.N : p.K, b_cols = kBStoredNK ? p.K : p.N;
-    (void)a_rows; (void)a_cols; (void)b_rows; (void)b_cols;
     auto issue_slice = [&](int s, int stage, uint32_t extra_tx) {
       const int k0 = s * BK;
       const uint32_t st_off = 4u * stage * kStageFloats;
-      const int64_t st_base = int64_t(smem_addr(smem) + st_off);
-      (void)st_base;
-      // A copy of `n` floats from src to shared address dst stays inside its
-      // matrix and its slab (debug build only).
-      auto a_ok = [&](uint32_t dst, const float *src, int n) {
-        return TMM_IN_BOUNDS(in_matrix(src, p.A, a_rows, a_cols, p.lda, n) &&
-                                 in_region(int64_t(dst) - st_base, kASlab, n),
-                             &g_simt_status);
-      };
-      auto b_ok = [&](uint32_t dst, const float *src, int n) {
-        return TMM_IN_BOUNDS(in_matrix(src, p.B, b_rows, b_cols, p.ldb, n) &&
-                                 in_region(int64_t(dst) - st_base - 4 * kASlab,
-                                           Cf::template b_slab_floats<kBCopy>(), n),
-                             &g_simt_status);
-      };
-      (void)a_ok; (void)b_ok;
-      if (kACopy == kCopyTransposing) {
+      if (!kTmaA) {
+        const int64_t st_base = int64_t(smem_addr(smem) + st_off);
+        (void)st_base;
         const float *a = a_src + k0;
 #pragma unroll
         for (int it = 0; it < Cf::kACopies; ++it) {
@@ -450,79 +375,24 @@ struct SimtBlock {
           const uint32_t dst = a_dst0 + st_off + 4u * (8 * h * kAsLd + 4 * Cf::kWarps * r);
           const float *src = a + r * a_step + 8 * h;
           const bool ok = ((a_rows_ok >> r) & 1u) && (k0 + t_k + 8 * h < p.K);
-          cp_async_4(dst, src, ok && a_ok(dst, src, 1), p.A);
-        }
-      } else if (kACopy == kCopyVec) {
-        constexpr int kRowsPerPass = Cf::kThreads / (Cf::BM / 4);
-        const float *a = a_src + int64_t(k0) * a_step;
-        const bool col_ok = m0 + a_m < p.M;
-#pragma unroll
-        for (int v = 0; v < BK * Cf::BM / 4 / Cf::kThreads; ++v) {
-          const int kr = a_k + kRowsPerPass * v;
-          const uint32_t dst = a_dst0 + st_off + 4u * (kRowsPerPass * v * kAsLd);
-          const float *src = a + int64_t(kRowsPerPass * v) * a_step;
-          const bool ok = col_ok && (k0 + kr < p.K);
-          cp_async_16(dst, src, ok && a_ok(dst, src, 4), p.A);
-        }
-      } else if (kACopy == kCopyScalar) {
-        constexpr int kColPasses = Cf::BM / 32;
-        const float *a = a_src + int64_t(k0) * a_step;
-#pragma unroll
-        for (int it = 0; it < BK * Cf::BM / Cf::kThreads; ++it) {
-          const int kr = Cf::kWarps * (it / kColPasses), c = it % kColPasses;
-          const bool ok = (m0 + a_m + 32 * c < p.M) && (k0 + a_k + kr < p.K);
-          const uint32_t dst = a_dst0 + st_off + 4u * (kr * kAsLd + 32 * c);
-          const float *src = a + int64_t(kr) * a_step + 32 * c;
-          cp_async_4(dst, src, ok && a_ok(dst, src, 1), p.A);
+          // The copy stays inside A and the A slab (debug build only).
+          cp_async_4(dst, src,
+                     ok && TMM_IN_BOUNDS(in_matrix(src, p.A, p.M, p.K, p.lda) &&
+                                             in_region(int64_t(dst) - st_base, kASlab),
+                                         &g_simt_status),
+                     p.A);
         }
       }
-      if (kBCopy == kCopyTransposing) {
-        const float *b = b_src + k0;
-#pragma unroll
-        for (int it = 0; it < Cf::BN / 4 / Cf::kWarps * (BK / 8); ++it) {
-          const int r = it % (Cf::BN / 4 / Cf::kWarps), h = it / (Cf::BN / 4 / Cf::kWarps);
-          const bool ok = ((b_rows_ok >> r) & 1u) && (k0 + t_k + 8 * h < p.K);
-          const uint32_t dst = b_dst0 + st_off + 4u * (8 * h * kBsLd + 4 * Cf::kWarps * r);
-          const float *src = b + r * b_step + 8 * h;
-          cp_async_4(dst, src, ok && b_ok(dst, src, 1), p.B);
-        }
-      } else if (kBCopy == kCopyVec) {
-        constexpr int kBRowsPerPass = Cf::kThreads / Cf::kBVecPerRow;
-        const float *b = b_src + int64_t(k0) * b_step;
-        const bool col_ok = n0 + b_n < p.N;
-#pragma unroll
-        for (int v = 0; v < Cf::kBVecCopies; ++v) {
-          const int kr = b_k + kBRowsPerPass * v;
-          const bool ok = col_ok && (k0 + kr < p.K);
-          const uint32_t dst = b_dst0 + st_off + 4u * (kBRowsPerPass * v * kBsLd);
-          const float *src = b + int64_t(kBRowsPerPass * v) * b_step;
-          cp_async_16(dst, src, ok && b_ok(dst, src, 4), p.B);
-        }
-      } else if (kBCopy == kCopyScalar) {
-        constexpr int kColPasses = Cf::BN / 32;
-        const float *b = b_src + int64_t(k0) * b_step;
-#pragma unroll
-        for (int it = 0; it < Cf::kBScalarCopies; ++it) {
-          const int kr = Cf::kWarps * (it / kColPasses), c = it % kColPasses;
-          const bool ok = (n0 + b_n + 32 * c < p.N) && (k0 + b_k + kr < p.K);
-          const uint32_t dst = b_dst0 + st_off + 4u * (kr * kBsLd + 32 * c);
-          const float *src = b + int64_t(kr) * b_step + 32 * c;
-          cp_async_4(dst, src, ok && b_ok(dst, src, 1), p.B);
-        }
-      }
-      if (kTma && tid == 0 && !tma_dead) {
+      if (tid == 0 && !tma_dead) {
         // The box origins lie inside the matrices (the copy fills the rest with zeros).
-        (void)TMM_IN_BOUNDS(k0 < p.K && (kBCopy != kCopyTma || n0 < p.N) &&
-                                (kACopy != kCopyTma || m0 < p.M),
-                            &g_simt_status);
+        (void)TMM_IN_BOUNDS(k0 < p.K && n0 < p.N && (!kTmaA || m0 < p.M), &g_simt_status);
         const uint32_t bar = bars + 8u * stage, st = smem_addr(smem) + st_off;
         mbar_arrive_expect_tx(bar, kTmaBytes + extra_tx);
-        if (kACopy == kCopyTma) tma_load_2d(st, a_map, m0, k0, bar);
-        if (kBCopy == kCopyTma)
+        if (kTmaA) tma_load_2d(st, a_map, m0, k0, bar);
 #pragma unroll
-          for (int j = 0; j < Cf::BN / Cf::kBBox; ++j)
-            tma_load_2d(st + 4u * (kASlab + j * BK * Cf::kBBox), b_map, n0 + j * Cf::kBBox, k0,
-                        bar);
+        for (int j = 0; j < Cf::BN / Cf::kBBox; ++j)
+          tma_load_2d(st + 4u * (kASlab + j * BK * Cf::kBBox), b_map, n0 + j * Cf::kBBox, k0,
+                      bar);
       }
     };
 
@@ -539,16 +409,12 @@ struct SimtBlock {
     int stage = 0;
     for (int s = s_begin; s < s_end; ++s) {
       cp_async_wait<kStages - 2>();   // slice s has landed (this thread's copies) ...
-      if (kTma) {
-        // ... and its TMA copies ...
-        if (!mbar_wait_unless(bars + 8u * stage, (phases >> stage) & 1u, p.wait_limit_ns,
-                              tma_dead))
-          tma_wait_failed(p, bars, phases, stage, s, s_end);
-        phases ^= 1u << stage;
-        __syncthreads();              // ... and everyone's; slice s-1's stage is free
-      } else {
-        __syncthreads();              // ... and everyone's; slice s-1's stage is free
-      }
+      // ... and its TMA copies ...
+      if (!mbar_wait_unless(bars + 8u * stage, (phases >> stage) & 1u, p.wait_limit_ns,
+                            tma_dead))
+        tma_wait_failed(p, bars, phases, stage, s, s_end);
+      phases ^= 1u << stage;
+      __syncthreads();                // ... and everyone's; slice s-1's stage is free
       {
         const int sn = s + kStages - 1;
         int stage_n = stage + kStages - 1;
@@ -610,95 +476,180 @@ struct SimtBlock {
     for (int c = 0; c < Cf::TN / 4; ++c) {
       ulonglong2 v = make_ulonglong2(0, 0);
       if (TMM_IN_BOUNDS(in_region(4 * (b + 4 * Cf::LN * c - bs),
-                                  Cf::template b_slab_floats<kBCopy>(), 4),
+                                  Cf::kBSlabFloats, 4),
                         &g_simt_status))
         v = *reinterpret_cast<const ulonglong2 *>(b + 4 * Cf::LN * c);
       bf[2 * c + 0] = v.x; bf[2 * c + 1] = v.y;
     }
   }
 
-  // The BK outer products of one staged slice, the fragments of step k + 1
-  // loaded while step k's packed FMAs issue.
+  // The BK outer products of one staged slice (the whole slice unrolled; the
+  // packed code fits the instruction cache), the fragments of step k + kPrefetch
+  // loaded while step k's packed FMAs issue.  Two steps ahead with A copied by
+  // transposing copies (4096^3 66.1 against 64.8 TFLOP/s one step ahead;
+  // 4000 x 3001 x 2047 58.8 against 57.6), one with A copied by TMA (4096^3
+  // 66.7 against 65.8 two steps ahead).
+  static constexpr int kPrefetch = kACopy == kCopyTma ? 1 : 2;
   template <int kAsLd, int kBsLd>
   __device__ __forceinline__ void slice_products(const float *as, const float *bs) {
-    constexpr int BK = Cf::BK;
-    float af[2][Cf::TM];
-    uint64_t bf[2][Cf::TN / 2];
-    load_frag<kAsLd, kBsLd>(as, bs, 0, af[0], bf[0]);
-#pragma unroll 1
-    for (int kk = 0; kk < BK; kk += Cf::kKUnroll) {
+    constexpr int BK = Cf::BK, D = kPrefetch, kBufs = kPrefetch + 1;
+    float af[kBufs][Cf::TM];
+    uint64_t bf[kBufs][Cf::TN / 2];
 #pragma unroll
-      for (int u = 0; u < Cf::kKUnroll; ++u) {
-        const int k = kk + u;
-        if (u + 1 < Cf::kKUnroll || k + 1 < BK)
-          load_frag<kAsLd, kBsLd>(as, bs, k + 1, af[(u + 1) & 1], bf[(u + 1) & 1]);
-        // Outer product: acc[i][j] += a[i] * b[j], two columns per instruction.
+    for (int d = 0; d < D; ++d) load_frag<kAsLd, kBsLd>(as, bs, d, af[d], bf[d]);
 #pragma unroll
-        for (int i = 0; i < Cf::TM; ++i) {
-          const uint64_t ai = pack2(af[u & 1][i], af[u & 1][i]);
+    for (int k = 0; k < BK; ++k) {
+      if (k + D < BK)
+        load_frag<kAsLd, kBsLd>(as, bs, k + D, af[(k + D) % kBufs], bf[(k + D) % kBufs]);
+      // Outer product: acc[i][j] += a[i] * b[j], two columns per instruction.
 #pragma unroll
-          for (int j = 0; j < Cf::TN / 2; ++j) acc[i][j] = ffma2(ai, bf[u & 1][j], acc[i][j]);
-        }
+      for (int i = 0; i < Cf::TM; ++i) {
+        const uint64_t ai = pack2(af[k % kBufs][i], af[k % kBufs][i]);
+#pragma unroll
+        for (int j = 0; j < Cf::TN / 2; ++j)
+          acc[i][j] = ffma2(ai, bf[k % kBufs][j], acc[i][j]);
       }
     }
   }
 
   // Accumulator (r, 4c + j) is C[m0 + a_off + row_of(r)][n0 + b_off + 4 LN c + j].
-  // kAdd: add the partial sums already in C (loaded through L2) before storing,
-  // kAddRows rows of them loaded together.
-  template <bool kAdd, int kAddRows = 4>
-  __device__ __forceinline__ void epilogue(const SimtParams &p, int m0, int n0) {
+  // Stores this thread's part of the tile; kAdd: the running sum of the later
+  // K-slices, already in C, is added first (partial + own, in that order).
+  template <bool kAdd>
+  __device__ __forceinline__ void epilogue(const SimtParams &p, int m0, int n0, float *smem) {
+    if (kAdd && kVecC)
+      add_staged(p, m0, n0, smem);
+    else if (kAdd)
+      add_elementwise(p, m0, n0);
+    else
+      store(p, m0, n0);
+  }
+
+  __device__ __forceinline__ void store(const SimtParams &p, int m0, int n0) {
     const int row0 = m0 + a_off;
     const int col0 = n0 + b_off;
     float *c_base = p.C + int64_t(row0) * p.ldc + col0;
-    // kAdd: the partial sums of kAddRows rows are all loaded before the first
-    // store, so the loads are in flight together (a store before a load of the
-    // same array would order them one after another) -- element by element
-    // when C takes no 16-byte stores.
+#pragma unroll
+    for (int r = 0; r < Cf::TM; ++r) {
+      const int dr = row_of(r);
+      if (row0 + dr >= p.M) continue;
+      float *c_row = c_base + int64_t(dr) * p.ldc;
+      float a[Cf::TN];
+#pragma unroll
+      for (int j = 0; j < Cf::TN / 2; ++j) unpack2(acc[r][j], a[2 * j], a[2 * j + 1]);
+#pragma unroll
+      for (int c = 0; c < Cf::TN / 4; ++c) {
+        const int dc = 4 * Cf::LN * c;
+        if (kVecC) {
+          if (col0 + dc < p.N &&
+              TMM_IN_BOUNDS(in_matrix(c_row + dc, p.C, p.M, p.N, p.ldc, 4), &g_simt_status))
+            *reinterpret_cast<float4 *>(c_row + dc) =
+                make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (col0 + dc + j < p.N &&
+                TMM_IN_BOUNDS(in_matrix(c_row + dc + j, p.C, p.M, p.N, p.ldc), &g_simt_status))
+              c_row[dc + j] = a[4 * c + j];
+        }
+      }
+    }
+  }
+
+  // The add when C takes 16-byte stores: this thread's part of the running
+  // sum is copied by 16-byte cp.async (through L2) into the stage ring, free
+  // once the mainloop has ended, every row in flight at once, then added and
+  // stored -- one round trip to L2, where loads into registers (the
+  // accumulators leave room for a few rows at a time) took one per row group.
+  // Vector (i, c) of a round of kRows rows sits at float4 slot
+  // (i TN/4 + c) kThreads + tid: a warp's copies and reads cover 512
+  // contiguous bytes, and a thread reads back only what it copied (visible to
+  // it once its own copies are waited for).
+  __device__ __forceinline__ void add_staged(const SimtParams &p, int m0, int n0, float *smem) {
+    constexpr int kRingFloats = Cf::kStages * Cf::template stage_floats<kACopy>();
+    constexpr int kVecs = Cf::TN / 4;
+    constexpr int kFit = kRingFloats / (Cf::kThreads * Cf::TN);
+    constexpr int kRows = kFit >= Cf::TM ? Cf::TM : kFit >= 4 ? 4 : kFit >= 2 ? 2 : 1;
+    static_assert(kFit >= 1 && Cf::TM % kRows == 0, "a round of rows fits the ring");
+    const int row0 = m0 + a_off;
+    const int col0 = n0 + b_off;
+    float *c_base = p.C + int64_t(row0) * p.ldc + col0;
+    const uint32_t ring = smem_addr(smem);
+#pragma unroll
+    for (int r0 = 0; r0 < Cf::TM; r0 += kRows) {
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        const int dr = row_of(r0 + i);
+        const bool row_ok = row0 + dr < p.M;
+        const float *c_row = c_base + int64_t(dr) * p.ldc;
+#pragma unroll
+        for (int c = 0; c < kVecs; ++c) {
+          const int slot = (i * kVecs + c) * Cf::kThreads + tid;
+          const float *src = c_row + 4 * Cf::LN * c;
+          const bool ok = row_ok && col0 + 4 * Cf::LN * c < p.N;
+          cp_async_16(ring + 16u * slot, src,
+                      ok && TMM_IN_BOUNDS(in_matrix(src, p.C, p.M, p.N, p.ldc, 4) &&
+                                              in_region(16 * int64_t(slot), kRingFloats, 4),
+                                          &g_simt_status),
+                      p.C);
+        }
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        const int r = r0 + i;
+        const int dr = row_of(r);
+        if (row0 + dr >= p.M) continue;
+        float *c_row = c_base + int64_t(dr) * p.ldc;
+        float a[Cf::TN];
+#pragma unroll
+        for (int j = 0; j < Cf::TN / 2; ++j) unpack2(acc[r][j], a[2 * j], a[2 * j + 1]);
+#pragma unroll
+        for (int c = 0; c < kVecs; ++c) {
+          const int dc = 4 * Cf::LN * c;
+          if (col0 + dc >= p.N) continue;
+          const int slot = (i * kVecs + c) * Cf::kThreads + tid;
+          const float4 w = *reinterpret_cast<const float4 *>(smem + 4 * slot);
+          float4 v = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+          v.x = w.x + v.x; v.y = w.y + v.y; v.z = w.z + v.z; v.w = w.w + v.w;
+          if (TMM_IN_BOUNDS(in_matrix(c_row + dc, p.C, p.M, p.N, p.ldc, 4), &g_simt_status))
+            *reinterpret_cast<float4 *>(c_row + dc) = v;
+        }
+      }
+    }
+    __syncthreads();   // the next tile's copies may overwrite the ring
+  }
+
+  // The add when C takes element-wise stores: the running sum is loaded
+  // element by element through L2 (a 4-byte copy into shared memory would go
+  // through L1, which may hold an older sum of the same lines), kAddRows rows
+  // of it before the first store, so the loads are in flight together (a
+  // store before a load of the same array would order them one after another).
+  __device__ __forceinline__ void add_elementwise(const SimtParams &p, int m0, int n0) {
+    constexpr int kAddRows = 4;
     static_assert(Cf::TM % kAddRows == 0, "whole row groups");
+    const int row0 = m0 + a_off;
+    const int col0 = n0 + b_off;
+    float *c_base = p.C + int64_t(row0) * p.ldc + col0;
 #pragma unroll
     for (int r0 = 0; r0 < Cf::TM; r0 += kAddRows) {
-      float4 w[kAddRows][Cf::TN / 4];
+      float w[kAddRows][Cf::TN];
 #pragma unroll
-      for (int i = 0; i < kAddRows; ++i)
+      for (int i = 0; i < kAddRows; ++i) {
+        const int dr = row_of(r0 + i);
+        const bool row_ok = row0 + dr < p.M;
+        const float *c_row = c_base + int64_t(dr) * p.ldc;
 #pragma unroll
-        for (int c = 0; c < Cf::TN / 4; ++c) w[i][c] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (kAdd && p.vec_store) {
+        for (int c = 0; c < Cf::TN / 4; ++c)
 #pragma unroll
-        for (int i = 0; i < kAddRows; ++i) {
-          const int r = r0 + i;
-          const int dr = row_of(r);
-          if (row0 + dr >= p.M) continue;
-          const float *c_row = c_base + int64_t(dr) * p.ldc;
-#pragma unroll
-          for (int c = 0; c < Cf::TN / 4; ++c)
-            if (col0 + 4 * Cf::LN * c < p.N &&
-                TMM_IN_BOUNDS(in_matrix(c_row + 4 * Cf::LN * c, p.C, p.M, p.N, p.ldc, 4),
-                              &g_simt_status))
-              w[i][c] = __ldcg(reinterpret_cast<const float4 *>(c_row + 4 * Cf::LN * c));
-        }
-      } else if (kAdd) {
-#pragma unroll
-        for (int i = 0; i < kAddRows; ++i) {
-          const int r = r0 + i;
-          const int dr = row_of(r);
-          if (row0 + dr >= p.M) continue;
-          const float *c_row = c_base + int64_t(dr) * p.ldc;
-#pragma unroll
-          for (int c = 0; c < Cf::TN / 4; ++c) {
-            const int dc = 4 * Cf::LN * c;
-            const int left = p.N - (col0 + dc);
-            auto ld = [&](int j) {
-              return left > j && TMM_IN_BOUNDS(in_matrix(c_row + dc + j, p.C, p.M, p.N, p.ldc),
-                                               &g_simt_status)
-                         ? __ldcg(c_row + dc + j) : 0.f;
-            };
-            w[i][c].x = ld(0);
-            w[i][c].y = ld(1);
-            w[i][c].z = ld(2);
-            w[i][c].w = ld(3);
+          for (int j = 0; j < 4; ++j) {
+            const int dc = 4 * Cf::LN * c + j;
+            w[i][4 * c + j] =
+                row_ok && col0 + dc < p.N &&
+                        TMM_IN_BOUNDS(in_matrix(c_row + dc, p.C, p.M, p.N, p.ldc), &g_simt_status)
+                    ? __ldcg(c_row + dc) : 0.f;
           }
-        }
       }
 #pragma unroll
       for (int i = 0; i < kAddRows; ++i) {
@@ -710,57 +661,38 @@ struct SimtBlock {
 #pragma unroll
         for (int j = 0; j < Cf::TN / 2; ++j) unpack2(acc[r][j], a[2 * j], a[2 * j + 1]);
 #pragma unroll
-        for (int c = 0; c < Cf::TN / 4; ++c) {
-          const int dc = 4 * Cf::LN * c;
-          if (p.vec_store) {
-            if (col0 + dc < p.N) {
-              float4 v = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
-              if (kAdd) {
-                v.x = w[i][c].x + v.x; v.y = w[i][c].y + v.y;
-                v.z = w[i][c].z + v.z; v.w = w[i][c].w + v.w;
-              }
-              if (TMM_IN_BOUNDS(in_matrix(c_row + dc, p.C, p.M, p.N, p.ldc, 4), &g_simt_status))
-                *reinterpret_cast<float4 *>(c_row + dc) = v;
-            }
-          } else {
-            const float wv[4] = {w[i][c].x, w[i][c].y, w[i][c].z, w[i][c].w};
+        for (int c = 0; c < Cf::TN / 4; ++c)
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (col0 + dc + j < p.N &&
-                  TMM_IN_BOUNDS(in_matrix(c_row + dc + j, p.C, p.M, p.N, p.ldc),
-                                &g_simt_status)) {
-                float v = a[4 * c + j];
-                if (kAdd) v = wv[j] + v;
-                c_row[dc + j] = v;
-              }
+          for (int j = 0; j < 4; ++j) {
+            const int dc = 4 * Cf::LN * c + j;
+            if (col0 + dc < p.N &&
+                TMM_IN_BOUNDS(in_matrix(c_row + dc, p.C, p.M, p.N, p.ldc), &g_simt_status))
+              c_row[dc] = w[i][4 * c + j] + a[4 * c + j];
           }
-        }
       }
     }
   }
 };
 
 // a_map, b_map: the tensor maps of A and B for the TMA copy kinds, else unused.
-template <class Cf, int kACopy, int kBCopy>
+template <class Cf, int kACopy, bool kVecC>
 __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 gemm_simt_kernel(const __grid_constant__ CUtensorMap a_map,
                  const __grid_constant__ CUtensorMap b_map, const SimtParams p) {
   extern __shared__ __align__(16) float smem_raw[];
-  constexpr int kRingFloats = Cf::kStages * Cf::template stage_floats<kACopy, kBCopy>();
-  float *smem = smem_raw;
-  uint32_t bars = 0, phases = 0;
-  if (Cf::template uses_tma<kACopy, kBCopy>()) {
-    const uint32_t raw = smem_addr(smem_raw);
-    const uint32_t base = (raw + 127u) & ~127u;
-    smem = smem_raw + (base - raw) / 4;
-    bars = base + uint32_t(kRingFloats * 4);
-    if (threadIdx.x == 0) {
-      for (int i = 0; i < Cf::kStages; ++i) mbar_init(bars + 8u * i, 1);
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
+  constexpr int kRingFloats = Cf::kStages * Cf::template stage_floats<kACopy>();
+  // The ring on a 128-byte boundary, then one mbarrier per stage.
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 127u) & ~127u;
+  float *smem = smem_raw + (base - raw) / 4;
+  const uint32_t bars = base + uint32_t(kRingFloats * 4);
+  uint32_t phases = 0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Cf::kStages; ++i) mbar_init(bars + 8u * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  SimtBlock<Cf, kACopy, kBCopy> blk;
+  __syncthreads();
+  SimtBlock<Cf, kACopy, kVecC> blk;
   blk.init_lanes();
 
   // Whole tiles.
@@ -768,7 +700,7 @@ gemm_simt_kernel(const __grid_constant__ CUtensorMap a_map,
     int tm, tn;
     tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
     blk.mainloop(p, smem, tm * Cf::BM, tn * Cf::BN, 0, p.slices, &a_map, &b_map, bars, phases);
-    blk.template epilogue<false>(p, tm * Cf::BM, tn * Cf::BN);
+    blk.template epilogue<false>(p, tm * Cf::BM, tn * Cf::BN, smem);
   }
   if (p.sk_iters == 0) return;
 
@@ -793,10 +725,10 @@ gemm_simt_kernel(const __grid_constant__ CUtensorMap a_map,
     const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
     blk.mainloop(p, smem, m0, n0, s_begin, s_end, &a_map, &b_map, bars, phases);
     if (s_begin == 0 && s_end == p.slices) {
-      blk.template epilogue<false>(p, m0, n0);
+      blk.template epilogue<false>(p, m0, n0, smem);
     } else if (s_end == p.slices) {
       // Slices [s_begin, S): store the partial sums, then raise this block's flag.
-      blk.template epilogue<false>(p, m0, n0);
+      blk.template epilogue<false>(p, m0, n0, smem);
       __syncthreads();
       if (threadIdx.x == 0 && int(b) != p.drop_signal_block) {
         __threadfence();
@@ -816,7 +748,7 @@ gemm_simt_kernel(const __grid_constant__ CUtensorMap a_map,
         }
       }
       __syncthreads();
-      blk.template epilogue<true>(p, m0, n0);
+      blk.template epilogue<true>(p, m0, n0, smem);
       if (s_begin > 0) {
         // A middle share (small problems only): C now holds the sum of slices
         // [s_begin, S), which the previous block waits for.
@@ -834,22 +766,12 @@ gemm_simt_kernel(const __grid_constant__ CUtensorMap a_map,
 // ---- host side ------------------------------------------------------------------
 
 using DefaultConfig = SimtConfig<8, 16, 1, 4, 16, 4, 2>;
-// Transposing copies cost one 4-byte copy per element, so a layout that reads
-// B stored N x K keeps the tile narrow in N: 256 x 64 tiles when A is copied
-// directly (A stored K x M), 128 x 128 when both operands are transposed.
-using WideMConfig = SimtConfig<8, 16, 4, 1, 16, 4, 2>;
-using SquareConfig = SimtConfig<8, 16, 2, 2, 16, 4, 2>;
-// B rows that do not start on 16-byte boundaries are copied element by
-// element, and those copies limit the default tile (32 of a thread's 40 copies
-// per K-slice).  A 128 x 256 tile with 2 x 4 warps gives each thread the same
-// products for 8 copies of A and 16 of B; at 232 registers one block fits per
-// SM, and 3 stages measured best (4000 x 3001 x 2047: 48.4 TFLOP/s against
-// 45.6; 4096 x 4095 x 4096: 54.5 against 50.0).
-using UnalignedBConfig = SimtConfig<8, 16, 2, 4, 16, 3, 1>;
-// B staged by TMA leaves A's transposing copies as the only per-thread ones;
+// With B copied by TMA, A's transposing copies are the only per-thread ones;
 // a 64 x 512 tile on 8 warps (one block per SM, B in two 256-column boxes)
 // halves them per thread: 4096^3 64.5 against 63.9 TFLOP/s, 8192 x 8192 x 1024
-// 63.3 against 63.1.  Used when its tiles fill two waves of SMs.
+// 63.3 against 63.1.  Used when its tiles fill two waves of SMs.  (A stored
+// K x M, copied by TMA as well, measured no better on it: 4096^3 67.3 against
+// 66.9 on the default tile, 8192 x 8192 x 1024 66.1 against 66.7.)
 using WideNConfig = SimtConfig<8, 16, 1, 8, 16, 4, 1>;
 
 struct LaunchState {
@@ -884,8 +806,6 @@ int64_t plan_simt(SimtParams &prm, const GemmProblem &p, int BM, int BN, int BK,
   prm.M = int(p.M); prm.N = int(p.N); prm.K = int(p.K);
   prm.A = p.A; prm.lda = p.lda; prm.B = p.B; prm.ldb = p.ldb; prm.C = p.C; prm.ldc = p.ldc;
   prm.tiles_m = int(tiles_m); prm.tiles_n = int(tiles_n);
-  prm.vec_store = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && p.ldc % 4 == 0 &&
-                   p.N % 4 == 0) ? 1 : 0;
   prm.slices = slices;
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   prm.drop_signal_block = g_drop_signal_block.load(std::memory_order_relaxed);
@@ -936,11 +856,11 @@ int64_t plan_simt(SimtParams &prm, const GemmProblem &p, int BM, int BN, int BK,
   return tiles;
 }
 
-template <class Cf, int kACopy, int kBCopy>
+template <class Cf, int kACopy, bool kVecC>
 cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
   static LaunchState state;
-  auto kernel = gemm_simt_kernel<Cf, kACopy, kBCopy>;
-  constexpr int kSmemBytes = Cf::template smem_bytes<kACopy, kBCopy>();
+  auto kernel = gemm_simt_kernel<Cf, kACopy, kVecC>;
+  constexpr int kSmemBytes = Cf::template smem_bytes<kACopy>();
   const uint64_t bit = uint64_t(1) << (dev.id & 63);
   if (!(state.configured.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -964,9 +884,8 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStre
   if (kACopy == kCopyTma)       // A stored K x M: boxes of BM columns x BK rows, a[k][m]
     e = encode_f32_2d(&a_map, p.A, p.K, p.M, p.lda, Cf::BM, Cf::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  if (kBCopy == kCopyTma)       // B stored K x N: boxes of BN columns x BK rows, b[k][n]
-    e = encode_f32_2d(&b_map, p.B, p.K, p.N, p.ldb, Cf::kBBox, Cf::BK,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
+  // B stored K x N: boxes of kBBox columns x BK rows, b[k][n]
+  e = encode_f32_2d(&b_map, p.B, p.K, p.N, p.ldb, Cf::kBBox, Cf::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   SimtParams prm = {};
   bool coop = false;
@@ -989,47 +908,61 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStre
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A (stored M x K, or K x M with 16-byte rows) and B (stored K x N with
+// 16-byte rows) as the kernels read them.
+template <bool kVecC>
+cudaError_t launch_layout(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
+  if (p.transa) return launch_variant<DefaultConfig, kCopyTma, kVecC>(p, dev, stream);
+  using W = WideNConfig;
+  const int64_t wide_tiles = (p.M + W::BM - 1) / W::BM * ((p.N + W::BN - 1) / W::BN);
+  return wide_tiles >= 2 * int64_t(dev.sm_count)
+             ? launch_variant<W, kCopyTransposing, kVecC>(p, dev, stream)
+             : launch_variant<DefaultConfig, kCopyTransposing, kVecC>(p, dev, stream);
+}
+
 }  // namespace
 
+// The product in any layout: an operand the kernels cannot copy by TMA as it
+// is stored -- B stored N x K, B stored K x N or A stored K x M with a row
+// pitch that is not a multiple of 4 floats or a base off a 16-byte boundary --
+// is first restaged into a K x N (K x M) copy with 16-byte rows, in scratch
+// allocated and freed on `stream` (the restaging copies read and write the
+// operand once).  A stored M x K is read as stored, by transposing copies.
 cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
-  using Cf = DefaultConfig;
-  // A stored K x M (transa) or B stored K x N (no transb) are copied directly,
-  // in 16-byte vectors when aligned; the other two layouts by transposing copies.
-  const bool vec_a = aligned16(p.A) && p.lda % 4 == 0 && p.M % 4 == 0;
-  const bool vec_b = aligned16(p.B) && p.ldb % 4 == 0 && p.N % 4 == 0;
-  // Operands whose rows all start on 16-byte boundaries are copied by TMA
-  // (the tensor-map rules: 16-byte aligned base, row stride a multiple of 16 bytes).
-  const bool tma_a = aligned16(p.A) && p.lda % 4 == 0;
-  const bool tma_b = aligned16(p.B) && p.ldb % 4 == 0;
-  // Unaligned B takes the 128 x 256 tile unless its tiles would leave SMs
-  // idle; the default tile then gives twice the blocks (1024 x 1023 x 1024:
-  // 21.2 against 15.8 TFLOP/s; 512 x 511 x 2048: 10.0 against 5.9).
-  using UB = UnalignedBConfig;
-  const bool wide_b = (p.M + UB::BM - 1) / UB::BM * ((p.N + UB::BN - 1) / UB::BN) >= dev.sm_count;
-  if (!p.transa) {
-    if (p.transb)
-      return launch_variant<SquareConfig, kCopyTransposing, kCopyTransposing>(p, dev, stream);
-    if (tma_b) {
-      using W = WideNConfig;
-      const int64_t wide_tiles = (p.M + W::BM - 1) / W::BM * ((p.N + W::BN - 1) / W::BN);
-      return wide_tiles >= 2 * int64_t(dev.sm_count)
-                 ? launch_variant<W, kCopyTransposing, kCopyTma>(p, dev, stream)
-                 : launch_variant<Cf, kCopyTransposing, kCopyTma>(p, dev, stream);
-    }
-    return wide_b ? launch_variant<UB, kCopyTransposing, kCopyScalar>(p, dev, stream)
-                  : launch_variant<Cf, kCopyTransposing, kCopyScalar>(p, dev, stream);
+  // Rows on 16-byte boundaries: 16-byte aligned base, pitch a multiple of 4 floats.
+  const bool tma_b = !p.transb && aligned16(p.B) && p.ldb % 4 == 0;
+  const bool tma_a = !p.transa || (aligned16(p.A) && p.lda % 4 == 0);
+  GemmProblem q = p;
+  const int64_t ld_b = (p.N + 3) / 4 * 4, ld_a = (p.M + 3) / 4 * 4;
+  const size_t b_bytes = tma_b ? 0 : size_t(p.K) * size_t(ld_b) * sizeof(float);
+  const size_t b_span = (b_bytes + 255) / 256 * 256;
+  const size_t a_bytes = tma_a ? 0 : size_t(p.K) * size_t(ld_a) * sizeof(float);
+  void *scratch = nullptr;
+  cudaError_t e = cudaSuccess;
+  if (b_bytes + a_bytes > 0) {
+    e = scratch_alloc(&scratch, b_span + a_bytes, dev, stream);
+    if (e != cudaSuccess) return e;
   }
-  if (p.transb)
-    return vec_a ? launch_variant<WideMConfig, kCopyVec, kCopyTransposing>(p, dev, stream)
-                 : launch_variant<WideMConfig, kCopyScalar, kCopyTransposing>(p, dev, stream);
-  if (tma_b)
-    return tma_a ? launch_variant<Cf, kCopyTma, kCopyTma>(p, dev, stream)
-                 : launch_variant<Cf, kCopyScalar, kCopyTma>(p, dev, stream);
-  if (vec_a)
-    return wide_b ? launch_variant<UB, kCopyVec, kCopyScalar>(p, dev, stream)
-                  : launch_variant<Cf, kCopyVec, kCopyScalar>(p, dev, stream);
-  return wide_b ? launch_variant<UB, kCopyScalar, kCopyScalar>(p, dev, stream)
-                : launch_variant<Cf, kCopyScalar, kCopyScalar>(p, dev, stream);
+  if (!tma_b) {
+    float *b = static_cast<float *>(scratch);
+    e = p.transb ? stage_transpose(p.B, p.ldb, p.N, p.K, b, ld_b, dev, stream)
+                 : stage_rows(p.B, p.ldb, p.K, p.N, b, ld_b, dev, stream);
+    q.B = b;
+    q.ldb = ld_b;
+    q.transb = 0;
+  }
+  if (e == cudaSuccess && !tma_a) {
+    float *a = reinterpret_cast<float *>(static_cast<char *>(scratch) + b_span);
+    e = stage_rows(p.A, p.lda, p.K, p.M, a, ld_a, dev, stream);
+    q.A = a;
+    q.lda = ld_a;
+  }
+  const bool vec_c = aligned16(p.C) && p.ldc % 4 == 0 && p.N % 4 == 0;
+  if (e == cudaSuccess)
+    e = vec_c ? launch_layout<true>(q, dev, stream) : launch_layout<false>(q, dev, stream);
+  // Freed in stream order, after the product has read the staged copies.
+  const cudaError_t f = scratch_free(scratch, stream);
+  return e != cudaSuccess ? e : f;
 }
 
 cudaError_t simt_device_status(unsigned int *status, bool clear) {

@@ -48,6 +48,24 @@ cudaError_t launch_naive(const GemmProblem &p, const DeviceInfo &dev, cudaStream
 cudaError_t naive_device_status(unsigned int *status, bool clear);
 cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream);
 
+// Operand restaging for the tiled product's TMA copies (operand_stage.cu):
+// dst[r][c] = src[r][c] (stage_rows) or dst[c][r] = src[r][c]
+// (stage_transpose) for r < rows, c < cols, with any source pitch and a
+// destination pitch ld_dst; launched on `stream`.
+cudaError_t stage_rows(const float *src, int64_t ld_src, int64_t rows, int64_t cols, float *dst,
+                       int64_t ld_dst, const DeviceInfo &dev, cudaStream_t stream);
+cudaError_t stage_transpose(const float *src, int64_t ld_src, int64_t rows, int64_t cols,
+                            float *dst, int64_t ld_dst, const DeviceInfo &dev,
+                            cudaStream_t stream);
+// Stream-ordered scratch from the library's memory pool of the device (kept
+// for reuse after it is freed); a failed allocation leaves no pending CUDA
+// error behind.
+cudaError_t scratch_alloc(void **ptr, size_t bytes, const DeviceInfo &dev, cudaStream_t stream);
+cudaError_t scratch_free(void *ptr, cudaStream_t stream);
+// Status word of the restaging copies (bit 2: a range check of the
+// bounds-checked build failed), optionally cleared.
+cudaError_t stage_device_status(unsigned int *status, bool clear);
+
 // Split-TF32 tensor-core path: workspace bytes for an M x N x K product
 // (SIZE_MAX when the count does not fit in size_t), and the launch (split
 // pre-pass + product kernel); `workspace` is 256-byte aligned.
