@@ -5,7 +5,10 @@ last wave on a 152-SM GB300 with two resident blocks per SM, which sends
 gemm_f32 down the persistent stream-K path: split tiles are summed by two
 blocks that meet through a flag.  The small shapes have fewer tiles than
 resident blocks: every tile is split over several consecutive blocks, each
-adding the next block's running sum (a chain of up to five).  The timeout
+adding the next block's running sum (a chain of up to five), or -- with few
+tiles, or C without 16-byte rows -- every block takes an equal share and the
+blocks sharing a tile reduce it together from their partial sums (up to one
+contributor per resident block).  The timeout
 tests make one block skip its flag (a testing hook of the library) with a
 2 ms limit: the waiting block must give up, the library must report
 TMM_ERR_DEVICE_TIMEOUT through tmm_check_device, and the next call must be
@@ -39,13 +42,16 @@ def _run(*a, **k):
 
 # (M, N, K): all tiles split (400 tiles); data-parallel waves plus split tiles
 # (1122 tiles); ragged K; ragged M and N with odd leading dimensions.  Then
-# fewer tiles than resident blocks: 64 tiles in four equal shares each; 64
-# tiles of 187 slices in shares that straddle tiles; one tile over four
-# blocks; single rows and columns; 4 tiles of 16 slices; 200 tiles (shares of
-# two thirds of a tile).
+# fewer tiles than resident blocks, chained: 64 tiles in four unequal parts
+# each; 64 tiles of 187 slices; 200 tiles (shares of two thirds of a tile).
+# Reduced together: one tile over 64 blocks; single rows and columns; 4
+# tiles of 125 slices; 4 tiles of 16 slices; 16 tiles of 256 slices (19
+# contributors each); C rows of 1023 floats (no 16-byte stores); one tile of
+# 4096 slices over all 304 resident blocks.
 SK_SHAPES = [(2560, 2560, 1000), (4224, 4224, 256), (2600, 2700, 1001), (3001, 2999, 777),
              (1024, 1024, 1024), (1000, 1000, 2990), (64, 256, 4096), (1, 1, 1024),
-             (37, 1000, 2000), (256, 256, 256), (1280, 2560, 1024)]
+             (37, 1000, 2000), (256, 256, 256), (1280, 2560, 1024), (512, 512, 4096),
+             (1024, 1023, 1024), (64, 256, 65536)]
 
 
 @pytest.mark.parametrize("shape", SK_SHAPES)
@@ -79,10 +85,12 @@ def test_stream_k_shapes_integer_exact_and_deterministic(shape):
     assert np.array_equal(D1.view(np.uint32), D2.view(np.uint32))
 
 
-@pytest.mark.parametrize("shape", [(2560, 2560, 256), (1024, 1024, 1024)])
+@pytest.mark.parametrize("shape", [(2560, 2560, 256), (1024, 1024, 1024), (512, 512, 4096)])
 def test_stream_k_wait_timeout_is_reported_and_recovers(shape):
     # 2560^2 x 256: block 1 holds the tail of a two-block tile.  1024^3: block 1
     # holds the second of four shares of tile 0, so block 0 waits for it.
+    # 512^2 x 4096 (reduced together): block 1 never raises the flags of its
+    # partial sums, so every block sharing its tiles waits for them.
     lib = _abi.load()
     stream = torch.cuda.current_stream().cuda_stream
     M, N, K = shape

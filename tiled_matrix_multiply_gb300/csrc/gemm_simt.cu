@@ -200,6 +200,19 @@ __device__ __forceinline__ unsigned int load_acquire(const unsigned int *p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Wait until *flag == value, an acquire load every 128 ns (a chain's
+// hand-over is on its critical path: a sleep doubling up to 1 us between
+// relaxed polls measured slower, 1000 x 1000 x 2990 44.1 against 45.4
+// TFLOP/s).  False when limit_ns passes first.
+__device__ __forceinline__ bool wait_flag(const unsigned int *flag, unsigned int value,
+                                          int64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (load_acquire(flag) != value) {
+    if (int64_t(global_timer_ns() - t0) > limit_ns) return false;
+    __nanosleep(128);
+  }
+  return true;
+}
 __device__ __forceinline__ void store_release(unsigned int *p, unsigned int v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -276,9 +289,11 @@ struct SimtParams {
   unsigned int epoch;    // this call's flag value (never 0)
   int64_t wait_limit_ns; // bound on a stream-K wait
   int drop_signal_block; // testing hook: this block never raises its flag (-1: none)
-  // Small problems split per tile (parts > 0): tile t's K-slices go to blocks
-  // t * parts .. t * parts + parts - 1 in unequal parts; part q holds
-  // part_base + (parts - 1 - q) * part_step slices (part 0 also the remainder).
+  // Small problems (fewer tiles than resident blocks) chained through C:
+  // with parts > 0, tile t's K-slices go to blocks t parts .. t parts +
+  // parts - 1 in unequal parts, part q holding part_base + (parts - 1 - q)
+  // part_step slices (part 0 also the remainder); with parts == 0, every
+  // block an equal share of all tiles' K-slices, at least a quarter of a tile.
   int parts, part_base, part_step, part_rem;
 };
 
@@ -287,6 +302,19 @@ __device__ __forceinline__ int part_begin(const SimtParams &p, int q) {
   if (q >= p.parts) return p.slices;
   return q * p.part_base + p.part_step * (q * (p.parts - 1) - q * (q - 1) / 2) +
          (q > 0 ? p.part_rem : 0);
+}
+
+// First K-slice unit (tile t, slice s is unit t S + s) of block b's equal
+// share of T units over G blocks.
+__device__ __forceinline__ int64_t share_begin(int64_t T, int64_t G, int64_t b) {
+  return b * T / G;
+}
+// The block whose share holds unit u.
+__device__ __forceinline__ int64_t share_owner(int64_t T, int64_t G, int64_t u) {
+  int64_t c = u * G / T;
+  while (c + 1 < G && share_begin(T, G, c + 1) <= u) ++c;
+  while (c > 0 && share_begin(T, G, c) > u) --c;
+  return c;
 }
 
 // One block's work on tile `tile`, K-slices [s_begin, s_end).  kACopy: how
@@ -512,6 +540,126 @@ struct SimtBlock {
     }
   }
 
+  // This thread's partial sums into a BM x BN row-major slot (16-byte stores).
+  __device__ __forceinline__ void store_partial(float *slot) {
+#pragma unroll
+    for (int r = 0; r < Cf::TM; ++r) {
+      float *row = slot + (a_off + row_of(r)) * Cf::BN + b_off;
+      float a[Cf::TN];
+#pragma unroll
+      for (int j = 0; j < Cf::TN / 2; ++j) unpack2(acc[r][j], a[2 * j], a[2 * j + 1]);
+#pragma unroll
+      for (int c = 0; c < Cf::TN / 4; ++c)
+        if (TMM_IN_BOUNDS(in_region(4 * (row + 4 * Cf::LN * c - slot), Cf::BM * Cf::BN, 4),
+                          &g_simt_status))
+          *reinterpret_cast<float4 *>(row + 4 * Cf::LN * c) =
+              make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+    }
+  }
+
+  // Tile t of a small problem split in equal shares over all G blocks: every
+  // block whose share meets the tile has stored its partial sums into its
+  // slot and raised the slot's flag.  Once all n flags are up (bounded
+  // waits), contributor j (this block) adds rows [j BM / n, (j + 1) BM / n)
+  // of the n partials, in contributor order, and stores them into C: the n
+  // contributors reduce the tile together, each reading a 1/n-th of every
+  // partial.  The first contributor's share may begin in the tile before,
+  // which makes tile t its second segment.
+  __device__ __forceinline__ void reduce_split_tile(const SimtParams &p, const float *partials,
+                                                    int t, int64_t G, int64_t b,
+                                                    const unsigned int *flags) {
+    const int64_t T = p.sk_iters;
+    const int64_t u0 = int64_t(t) * p.slices, u1 = u0 + p.slices;
+    const int64_t c_lo = share_owner(T, G, u0), c_hi = share_owner(T, G, u1 - 1);
+    const int64_t first_slot = 2 * c_lo + (share_begin(T, G, c_lo) < u0 ? 1 : 0);
+    auto slot_of = [&](int64_t c) { return c == c_lo ? first_slot : 2 * c; };
+    if (tid == 0) {
+      for (int64_t c = c_lo; c <= c_hi; ++c)
+        if (!wait_flag(&flags[slot_of(c)], p.epoch, p.wait_limit_ns))
+          atomicOr(&g_simt_status, 1u);
+    }
+    __syncthreads();
+    int tm, tn;
+    tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
+    const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
+    const int n = int(c_hi - c_lo + 1), j = int(b - c_lo);
+    const int r0 = j * Cf::BM / n, r1 = (j + 1) * Cf::BM / n;
+    // 16 loads of 16 bytes in flight per thread: positions x contributors.
+    if (n <= 2)
+      reduce_rows<8, 2>(p, partials, m0, n0, r0, r1, c_lo, c_hi, first_slot, G);
+    else if (n <= 4)
+      reduce_rows<4, 4>(p, partials, m0, n0, r0, r1, c_lo, c_hi, first_slot, G);
+    else
+      reduce_rows<2, 8>(p, partials, m0, n0, r0, r1, c_lo, c_hi, first_slot, G);
+  }
+
+  // Rows [r0, r1) of a split tile: the partial sums of contributors c_lo ..
+  // c_hi (slot first_slot for c_lo, 2 c for the others) added in contributor
+  // order and stored into C.  Each thread takes P 16-byte positions at a time
+  // and loads them from Q contributors at a time, all P Q loads in flight.
+  template <int P, int Q>
+  __device__ __forceinline__ void reduce_rows(const SimtParams &p, const float *partials, int m0,
+                                              int n0, int r0, int r1, int64_t c_lo, int64_t c_hi,
+                                              int64_t first_slot, int64_t G) {
+    constexpr int kRowVecs = Cf::BN / 4;
+    constexpr int64_t kSlotFloats = int64_t(Cf::BM) * Cf::BN;
+    const int nvec = (r1 - r0) * kRowVecs;
+    for (int base = tid; base < nvec; base += P * Cf::kThreads) {
+      float4 v[P];
+      for (int64_t cc = c_lo; cc <= c_hi; cc += Q) {
+        float4 w[P][Q];
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+          const int idx = base + i * Cf::kThreads;
+          const int64_t off = int64_t(r0 + idx / kRowVecs) * Cf::BN + 4 * (idx % kRowVecs);
+#pragma unroll
+          for (int q = 0; q < Q; ++q) {
+            const int64_t c = cc + q;
+            const int64_t slot = c == c_lo ? first_slot : 2 * c;
+            w[i][q] = (idx < nvec && c <= c_hi &&
+                       TMM_IN_BOUNDS(in_region(4 * (slot * kSlotFloats + off),
+                                               2 * G * kSlotFloats, 4),
+                                     &g_simt_status))
+                          ? __ldcg(reinterpret_cast<const float4 *>(partials +
+                                                                    slot * kSlotFloats + off))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < P; ++i)
+#pragma unroll
+          for (int q = 0; q < Q; ++q) {
+            if (cc + q > c_hi) break;
+            if (cc + q == c_lo) {
+              v[i] = w[i][q];
+            } else {
+              v[i].x = v[i].x + w[i][q].x; v[i].y = v[i].y + w[i][q].y;
+              v[i].z = v[i].z + w[i][q].z; v[i].w = v[i].w + w[i][q].w;
+            }
+          }
+      }
+#pragma unroll
+      for (int i = 0; i < P; ++i) {
+        const int idx = base + i * Cf::kThreads;
+        if (idx >= nvec) break;
+        const int gr = m0 + r0 + idx / kRowVecs, gc = n0 + 4 * (idx % kRowVecs);
+        if (gr >= p.M) continue;
+        float *dst = p.C + int64_t(gr) * p.ldc + gc;
+        if (kVecC) {
+          if (gc < p.N && TMM_IN_BOUNDS(in_matrix(dst, p.C, p.M, p.N, p.ldc, 4), &g_simt_status))
+            *reinterpret_cast<float4 *>(dst) = v[i];
+        } else {
+          const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (gc + e < p.N &&
+                TMM_IN_BOUNDS(in_matrix(dst + e, p.C, p.M, p.N, p.ldc), &g_simt_status))
+              dst[e] = vv[e];
+        }
+      }
+    }
+  }
+
   // Accumulator (r, 4c + j) is C[m0 + a_off + row_of(r)][n0 + b_off + 4 LN c + j].
   // Stores this thread's part of the tile; kAdd: the running sum of the later
   // K-slices, already in C, is added first (partial + own, in that order).
@@ -675,6 +823,7 @@ struct SimtBlock {
 };
 
 // a_map, b_map: the tensor maps of A and B for the TMA copy kinds, else unused.
+// a_map, b_map: the tensor maps of A and B for the TMA copy kinds, else unused.
 template <class Cf, int kACopy, bool kVecC>
 __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 gemm_simt_kernel(const __grid_constant__ CUtensorMap a_map,
@@ -763,6 +912,77 @@ gemm_simt_kernel(const __grid_constant__ CUtensorMap a_map,
   }
 }
 
+// The small-problem split whose blocks reduce the split tiles together: every
+// block takes an equal share of all tiles' K-slices -- at most two segments,
+// the end of one tile and the start of the next -- and stores the partial
+// sums of a segment that is not a whole tile into its slot of `partials`
+// (slot 2 b + segment, BM x BN floats, row-major); the blocks sharing a tile
+// then reduce it together.  A kernel of its own, so that the code of the
+// other kernels is compiled exactly as without it.
+template <class Cf, int kACopy, bool kVecC>
+__global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
+gemm_simt_reduce_kernel(const __grid_constant__ CUtensorMap a_map,
+                        const __grid_constant__ CUtensorMap b_map, const SimtParams p,
+                        float *partials) {
+  extern __shared__ __align__(16) float smem_raw[];
+  constexpr int kRingFloats = Cf::kStages * Cf::template stage_floats<kACopy>();
+  // The ring on a 128-byte boundary, then one mbarrier per stage.
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 127u) & ~127u;
+  float *smem = smem_raw + (base - raw) / 4;
+  const uint32_t bars = base + uint32_t(kRingFloats * 4);
+  uint32_t phases = 0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Cf::kStages; ++i) mbar_init(bars + 8u * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  SimtBlock<Cf, kACopy, kVecC> blk;
+  blk.init_lanes();
+
+  // Small problems reduced together: this block's equal share of all
+  // tiles' K-slices, at most two segments, each leaving its partial sums in
+  // its slot and raising the slot's flag; only then does the block wait, to
+  // reduce its split tiles with the other blocks sharing them, so every
+  // flag is raised before any block waits.  One run-time loop keeps one
+  // copy of the mainloop.
+  const int64_t g = gridDim.x, b = blockIdx.x;
+  unsigned int *flags = g_simt_flags + (p.epoch % kFlagRegions) * kMaxPersistentBlocks;
+  constexpr int64_t kSlotFloats = int64_t(Cf::BM) * Cf::BN;
+  const int64_t it_begin = share_begin(p.sk_iters, g, b);
+  const int64_t it_end = share_begin(p.sk_iters, g, b + 1);
+  for (int64_t it = it_begin; it < it_end;) {
+    const int tile = int(it / p.slices), s_begin = int(it % p.slices);
+    const int64_t rest = it_end - it;
+    const int s_end = rest < int64_t(p.slices - s_begin) ? s_begin + int(rest) : p.slices;
+    const int seg = it == it_begin ? 0 : 1;
+    it += s_end - s_begin;
+    int tm, tn;
+    tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+    const int m0 = tm * Cf::BM, n0 = tn * Cf::BN;
+    blk.mainloop(p, smem, m0, n0, s_begin, s_end, &a_map, &b_map, bars, phases);
+    if (s_begin == 0 && s_end == p.slices) {
+      blk.template epilogue<false>(p, m0, n0, smem);
+      continue;
+    }
+    blk.store_partial(partials + (2 * b + seg) * kSlotFloats);
+    __syncthreads();
+    if (threadIdx.x == 0 && int(b) != p.drop_signal_block) {
+      __threadfence();
+      store_release(&flags[2 * b + seg], p.epoch);
+    }
+  }
+  for (int64_t u = it_begin; u < it_end;) {
+    const int tile = int(u / p.slices), s_begin = int(u % p.slices);
+    const int64_t rest = it_end - u;
+    const int s_end = rest < int64_t(p.slices - s_begin) ? s_begin + int(rest) : p.slices;
+    u += s_end - s_begin;
+    if (s_begin == 0 && s_end == p.slices) continue;
+    blk.reduce_split_tile(p, partials, tile, g, b, flags);
+    __syncthreads();
+  }
+}
+
 // ---- host side ------------------------------------------------------------------
 
 using DefaultConfig = SimtConfig<8, 16, 1, 4, 16, 4, 2>;
@@ -783,22 +1003,36 @@ std::atomic<unsigned int> g_epoch{0};
 std::atomic<int64_t> g_wait_limit_ns{int64_t(10) * 1000 * 1000 * 1000};
 std::atomic<int> g_drop_signal_block{-1};
 
-// Tiling and work split shared by both kernels: fills prm and returns the
-// grid size.  When the tile count leaves the last wave of `slots` resident
-// blocks partly empty, one block per slot, the last full wave plus the
-// remainder split over K (stream-K); with fewer tiles than slots, every
-// tile's K-slices shared by up to about five consecutive blocks (a share is at
-// least a quarter of a tile and four slices), when that gives at least an
-// eighth more blocks than tiles.  Both schemes need the blocks co-resident
-// (*cooperative) and `flags_per_block` flags per block.
 // Slices by which each part of a tile split per tile is longer than the next
 // (measured, TFLOP/s for steps 0 / 1 / 2 / 3: 1024^3 34.6 / 35.8 / 35.8 / 32.4;
 // 1000 x 1000 x 2990 44.0 / 44.7 / 42.7 / 42.7; the even split across tile
 // boundaries before: 35.2 and 41.5).
 constexpr int kChainStep = 1;
 
-int64_t plan_simt(SimtParams &prm, const GemmProblem &p, int BM, int BN, int BK, int64_t slots,
-                  int flags_per_block, bool *cooperative) {
+// Tiling and work split: fills prm and returns the grid size.
+//   * When the tile count leaves the last wave of `slots` resident blocks
+//     partly empty: one block per slot, the last full wave plus the remainder
+//     split over K (stream-K, two blocks per split tile, one flag per block).
+//   * With fewer tiles than slots, the blocks sharing a tile chain their sums
+//     through C: each tile in up to four unequal parts when there is room for
+//     two blocks per tile (the part holding the end of K -- the first of the
+//     chain to store its sum -- the smallest, each earlier part kChainStep
+//     slices longer, so the sum handed down the chain arrives while the part
+//     receiving it still computes), else equal shares of all tiles' K-slices
+//     of at least a quarter of a tile.
+//   * Those chains hand a tile's sum over one contributor after another, and
+//     element by element where C takes no 16-byte stores.  When C takes none,
+//     or when the chains would keep fewer than 2/5 of the slots busy (few
+//     tiles), every block instead takes an equal share (at least four slices)
+//     and the blocks sharing a tile reduce it together from *partial_slots
+//     slots of partial sums (two per block, two flags): 1024 x 1023 x 1024
+//     21.4 -> 30.1 TFLOP/s, 512 x 512 x 4096 21.7 -> 34.0, 256^3 1.33 -> 1.66;
+//     with most slots busy the unequal chains stay ahead (1024^3 37.0 against
+//     32.9, 2048^3 61.5 against 57.9): two blocks sharing an SM progress
+//     unequally, which the chains absorb and equal shares wait for.
+// Every split needs the blocks co-resident (*cooperative).
+int64_t plan_simt(SimtParams &prm, const GemmProblem &p, bool vec_c, bool may_reduce, int BM,
+                  int BN, int BK, int64_t slots, bool *cooperative, int64_t *partial_slots) {
   const int64_t tiles_m = (p.M + BM - 1) / BM;
   const int64_t tiles_n = (p.N + BN - 1) / BN;
   const int64_t tiles = tiles_m * tiles_n;
@@ -809,35 +1043,45 @@ int64_t plan_simt(SimtParams &prm, const GemmProblem &p, int BM, int BN, int BK,
   prm.slices = slices;
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   prm.drop_signal_block = g_drop_signal_block.load(std::memory_order_relaxed);
-  const bool flags_fit = slots > 0 && slots * flags_per_block <= kMaxPersistentBlocks;
+  prm.parts = 0;
+  *partial_slots = 0;
+  const bool flags_fit = slots > 0 && 2 * slots <= kMaxPersistentBlocks;
   const int64_t rem = slots > 0 ? tiles % slots : 0;
   const bool stream_k = flags_fit && tiles > slots && rem != 0 && rem * 10 < slots * 9 &&
                         slices >= 4;
   int64_t small_blocks = 0;
-  prm.parts = 0;
+  bool reduce_split = false;
   if (!stream_k && flags_fit && tiles < slots) {
-    // With room for at least two blocks per tile: each tile in `parts` parts
-    // (up to four, of at least four slices), the part holding the end of K --
-    // the first of the tile's chain to store its sum -- the smallest, and each
-    // earlier part kChainStep slices longer, so the sum handed down the chain
-    // arrives while the part receiving it still computes.
     const int64_t parts = std::min<int64_t>({4, slots / tiles, slices / 4});
+    int64_t chain_blocks = 0;
     if (parts >= 2) {
-      int step = kChainStep;
-      while (step > 0 && slices - step * parts * (parts - 1) / 2 < 4 * parts) --step;
-      const int base = int((slices - step * parts * (parts - 1) / 2) / parts);
-      prm.parts = int(parts);
-      prm.part_step = step;
-      prm.part_base = base;
-      prm.part_rem = int(slices - step * parts * (parts - 1) / 2 - base * parts);
-      small_blocks = tiles * parts;
+      chain_blocks = tiles * parts;
     } else {
       const int64_t iters = tiles * slices;
       int64_t share = (iters + slots - 1) / slots;
       share = share > (slices + 3) / 4 ? share : (slices + 3) / 4;
       share = share > 4 ? share : 4;
       const int64_t g = (iters + share - 1) / share;
-      if (g * 8 >= tiles * 9) small_blocks = g;
+      if (g * 8 >= tiles * 9) chain_blocks = g;
+    }
+    if (may_reduce && (!vec_c || chain_blocks * 5 < slots * 2)) {
+      const int64_t g = std::min<int64_t>(slots, tiles * slices / 4);
+      if (g * 8 >= tiles * 9) {
+        small_blocks = g;
+        reduce_split = true;
+      }
+    }
+    if (!reduce_split && chain_blocks > 0) {
+      small_blocks = chain_blocks;
+      if (parts >= 2) {
+        int step = kChainStep;
+        while (step > 0 && slices - step * parts * (parts - 1) / 2 < 4 * parts) --step;
+        const int base = int((slices - step * parts * (parts - 1) / 2) / parts);
+        prm.parts = int(parts);
+        prm.part_step = step;
+        prm.part_base = base;
+        prm.part_rem = int(slices - step * parts * (parts - 1) / 2 - base * parts);
+      }
     }
   }
   *cooperative = stream_k || small_blocks > 0;
@@ -848,6 +1092,7 @@ int64_t plan_simt(SimtParams &prm, const GemmProblem &p, int BM, int BN, int BK,
     unsigned int e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
     if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
     prm.epoch = e;
+    if (reduce_split) *partial_slots = 2 * small_blocks;
     return stream_k ? slots : small_blocks;
   }
   prm.dp_tiles = int(tiles);
@@ -856,31 +1101,49 @@ int64_t plan_simt(SimtParams &prm, const GemmProblem &p, int BM, int BN, int BK,
   return tiles;
 }
 
-template <class Cf, int kACopy, bool kVecC>
-cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
-  static LaunchState state;
-  auto kernel = gemm_simt_kernel<Cf, kACopy, kVecC>;
-  constexpr int kSmemBytes = Cf::template smem_bytes<kACopy>();
+// Shared-memory opt-in and the resident blocks per SM of one kernel, once per device.
+template <class Kernel>
+cudaError_t configure(Kernel kernel, int threads, int smem_bytes, LaunchState &state,
+                      const DeviceInfo &dev, int *blocks_per_sm) {
   const uint64_t bit = uint64_t(1) << (dev.id & 63);
   if (!(state.configured.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+                                         smem_bytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int nb = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, Cf::kThreads, kSmemBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem_bytes);
     if (e != cudaSuccess) return e;
     state.blocks_per_sm[dev.id & 63].store(nb, std::memory_order_relaxed);
     state.configured.fetch_or(bit, std::memory_order_release);
   }
-  const int blocks_per_sm = state.blocks_per_sm[dev.id & 63].load(std::memory_order_relaxed);
+  *blocks_per_sm = state.blocks_per_sm[dev.id & 63].load(std::memory_order_relaxed);
+  return cudaSuccess;
+}
+
+// kSmall: the tile configuration small problems use, which therefore has a
+// kernel for the reduced split as well (the 64 x 512 tile serves products of
+// at least two waves only).
+template <class Cf, int kACopy, bool kVecC, bool kSmall>
+cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
+  static LaunchState state, state_reduce;
+  auto kernel = gemm_simt_kernel<Cf, kACopy, kVecC>;
+  constexpr int kSmemBytes = Cf::template smem_bytes<kACopy>();
+  int blocks_per_sm = 0, blocks_per_sm_reduce = 0;
+  cudaError_t e = configure(kernel, Cf::kThreads, kSmemBytes, state, dev, &blocks_per_sm);
+  if (e != cudaSuccess) return e;
+  blocks_per_sm_reduce = blocks_per_sm;
+  if constexpr (kSmall) {   // the 64 x 512 tile never takes the reduced split
+    e = configure(gemm_simt_reduce_kernel<Cf, kACopy, kVecC>, Cf::kThreads, kSmemBytes,
+                  state_reduce, dev, &blocks_per_sm_reduce);
+    if (e != cudaSuccess) return e;
+  }
   const int64_t tiles = ((p.M + Cf::BM - 1) / Cf::BM) * ((p.N + Cf::BN - 1) / Cf::BN);
   if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
 
   CUtensorMap a_map = {}, b_map = {};
-  cudaError_t e = cudaSuccess;
   if (kACopy == kCopyTma)       // A stored K x M: boxes of BM columns x BK rows, a[k][m]
     e = encode_f32_2d(&a_map, p.A, p.K, p.M, p.lda, Cf::BM, Cf::BK, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
@@ -889,8 +1152,17 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStre
   if (e != cudaSuccess) return e;
   SimtParams prm = {};
   bool coop = false;
-  const int64_t grid = plan_simt(prm, p, Cf::BM, Cf::BN, Cf::BK,
-                                 int64_t(blocks_per_sm) * dev.sm_count, 1, &coop);
+  int64_t partial_slots = 0;
+  // The slots of the reduced split are those its kernel keeps resident.
+  const int64_t slots = int64_t(std::min(blocks_per_sm, blocks_per_sm_reduce)) * dev.sm_count;
+  const int64_t grid = plan_simt(prm, p, kVecC, kSmall, Cf::BM, Cf::BN, Cf::BK, slots, &coop,
+                                 &partial_slots);
+  void *partials = nullptr;
+  if (partial_slots > 0) {
+    e = scratch_alloc(&partials, size_t(partial_slots) * Cf::BM * Cf::BN * sizeof(float), dev,
+                      stream);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(Cf::kThreads, 1, 1);
@@ -903,7 +1175,18 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStre
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, kernel, a_map, b_map, prm);
+  if constexpr (kSmall) {
+    if (partials)
+      e = cudaLaunchKernelEx(&cfg, gemm_simt_reduce_kernel<Cf, kACopy, kVecC>, a_map, b_map, prm,
+                             static_cast<float *>(partials));
+    else
+      e = cudaLaunchKernelEx(&cfg, kernel, a_map, b_map, prm);
+  } else {
+    e = cudaLaunchKernelEx(&cfg, kernel, a_map, b_map, prm);
+  }
+  // Freed in stream order, after the kernel has read the partial sums.
+  const cudaError_t f = scratch_free(partials, stream);
+  return e != cudaSuccess ? e : f;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -912,12 +1195,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // 16-byte rows) as the kernels read them.
 template <bool kVecC>
 cudaError_t launch_layout(const GemmProblem &p, const DeviceInfo &dev, cudaStream_t stream) {
-  if (p.transa) return launch_variant<DefaultConfig, kCopyTma, kVecC>(p, dev, stream);
+  if (p.transa) return launch_variant<DefaultConfig, kCopyTma, kVecC, true>(p, dev, stream);
   using W = WideNConfig;
   const int64_t wide_tiles = (p.M + W::BM - 1) / W::BM * ((p.N + W::BN - 1) / W::BN);
   return wide_tiles >= 2 * int64_t(dev.sm_count)
-             ? launch_variant<W, kCopyTransposing, kVecC>(p, dev, stream)
-             : launch_variant<DefaultConfig, kCopyTransposing, kVecC>(p, dev, stream);
+             ? launch_variant<W, kCopyTransposing, kVecC, false>(p, dev, stream)
+             : launch_variant<DefaultConfig, kCopyTransposing, kVecC, true>(p, dev, stream);
 }
 
 }  // namespace
