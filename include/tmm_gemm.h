@@ -42,11 +42,13 @@
  *                the legacy default stream.  Every call is asynchronous: it
  *                returns once the kernel is enqueued; the caller synchronises.
  *
- * Memory: gemm_f32 and gemm_f32_ex take the scratch of a restaged operand
- * (K x N rounded up to a multiple of 4 floats for B, K x M likewise for A)
- * from a stream-ordered memory pool the library creates per device: it is
- * allocated on `stream` before the copy and freed on `stream` after the
- * product, so calls on different streams never share it, and the pool keeps
+ * Memory: gemm_f32 and gemm_f32_ex take scratch from a stream-ordered memory
+ * pool the library creates per device -- for a restaged operand (K x N
+ * rounded up to a multiple of 4 floats for B, K x M likewise for A), and for
+ * the partial sums of a small problem whose blocks reduce their tiles
+ * together (two 64 x 256 slots per resident block at most, 40 MiB on GB300).
+ * It is allocated on `stream` and freed on `stream` after the kernels that
+ * read it, so calls on different streams never share it, and the pool keeps
  * the freed memory for later calls (for the life of the process).  No other
  * entry point allocates device or host memory per call.  All entry points
  * use the current CUDA device (cudaSetDevice) and are thread-safe.
@@ -121,10 +123,13 @@ typedef struct CUstream_st *tmm_stream_t;
  * runs persistent and cooperative (one block per resident slot) and splits
  * the K range of the last tiles between pairs of blocks; with fewer tiles
  * than resident blocks, the K range of every tile is split over up to about
- * five consecutive blocks, each adding the next block's running sum.  Blocks
- * meet through flags in library-owned device memory, with a bounded wait
- * (see tmm_check_device).  Up to 16 such calls may be in flight at once (for
- * example on different streams); results are deterministic either way.
+ * five consecutive blocks, each adding the next block's running sum, or --
+ * with few tiles, or C without 16-byte rows -- over equal shares of all
+ * blocks, which then reduce each tile together from their partial sums in a
+ * fixed order.  Blocks meet through flags in library-owned device memory,
+ * with a bounded wait (see tmm_check_device).  Up to 16 such calls may be in
+ * flight at once (for example on different streams); results are
+ * deterministic either way.
  */
 int gemm_f32(int64_t M, int64_t N, int64_t K,
              const float *A, int64_t lda,
