@@ -46,7 +46,9 @@
  * pool the library creates per device -- for a restaged operand (K x N
  * rounded up to a multiple of 4 floats for B, K x M likewise for A), and for
  * the partial sums of a small problem whose blocks reduce their tiles
- * together (two 64 x 256 slots per resident block at most, 40 MiB on GB300).
+ * together (two 64 x 256 slots per resident block at most, 40 MiB on GB300;
+ * when that cannot be allocated the call splits the problem in a way that
+ * needs none).
  * It is allocated on `stream` and freed on `stream` after the kernels that
  * read it, so calls on different streams never share it, and the pool keeps
  * the freed memory for later calls (for the life of the process).  No other

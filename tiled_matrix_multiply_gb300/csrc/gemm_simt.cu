@@ -1155,13 +1155,15 @@ cudaError_t launch_variant(const GemmProblem &p, const DeviceInfo &dev, cudaStre
   int64_t partial_slots = 0;
   // The slots of the reduced split are those its kernel keeps resident.
   const int64_t slots = int64_t(std::min(blocks_per_sm, blocks_per_sm_reduce)) * dev.sm_count;
-  const int64_t grid = plan_simt(prm, p, kVecC, kSmall, Cf::BM, Cf::BN, Cf::BK, slots, &coop,
-                                 &partial_slots);
+  int64_t grid = plan_simt(prm, p, kVecC, kSmall, Cf::BM, Cf::BN, Cf::BK, slots, &coop,
+                           &partial_slots);
   void *partials = nullptr;
-  if (partial_slots > 0) {
-    e = scratch_alloc(&partials, size_t(partial_slots) * Cf::BM * Cf::BN * sizeof(float), dev,
-                      stream);
-    if (e != cudaSuccess) return e;
+  if (partial_slots > 0 &&
+      scratch_alloc(&partials, size_t(partial_slots) * Cf::BM * Cf::BN * sizeof(float), dev,
+                    stream) != cudaSuccess) {
+    // No scratch for the partial sums: the chains through C need none.
+    grid = plan_simt(prm, p, kVecC, false, Cf::BM, Cf::BN, Cf::BK, slots, &coop,
+                     &partial_slots);
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

@@ -106,6 +106,17 @@ int64_t copy_grid(int64_t items, const DeviceInfo &dev) {
   return items < cap ? (items > 0 ? items : 1) : cap;
 }
 
+// The launch's own status (not an error left pending by earlier calls).
+template <class Kernel, class... Args>
+cudaError_t launch_copy(Kernel kernel, int64_t items, const DeviceInfo &dev, cudaStream_t stream,
+                        Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(copy_grid(items, dev)), 1, 1);
+  cfg.blockDim = dim3(kCopyThreads, 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int kMaxDevices = 64;
 std::mutex g_pool_mutex;
 cudaMemPool_t g_pool[kMaxDevices] = {};
@@ -139,18 +150,15 @@ cudaError_t stage_rows(const float *src, int64_t ld_src, int64_t rows, int64_t c
                        int64_t ld_dst, const DeviceInfo &dev, cudaStream_t stream) {
   const int64_t items = (cols + kCopyThreads - 1) / kCopyThreads *
                         ((rows + kCopyUnroll - 1) / kCopyUnroll);
-  stage_rows_kernel<<<unsigned(copy_grid(items, dev)), kCopyThreads, 0, stream>>>(
-      src, ld_src, rows, cols, dst, ld_dst);
-  return cudaGetLastError();
+  return launch_copy(stage_rows_kernel, items, dev, stream, src, ld_src, rows, cols, dst, ld_dst);
 }
 
 cudaError_t stage_transpose(const float *src, int64_t ld_src, int64_t rows, int64_t cols,
                             float *dst, int64_t ld_dst, const DeviceInfo &dev,
                             cudaStream_t stream) {
   const int64_t items = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
-  stage_transpose_kernel<<<unsigned(copy_grid(items, dev)), kCopyThreads, 0, stream>>>(
-      src, ld_src, rows, cols, dst, ld_dst);
-  return cudaGetLastError();
+  return launch_copy(stage_transpose_kernel, items, dev, stream, src, ld_src, rows, cols, dst,
+                     ld_dst);
 }
 
 cudaError_t scratch_alloc(void **ptr, size_t bytes, const DeviceInfo &dev, cudaStream_t stream) {
