@@ -81,8 +81,11 @@ def test_ragged_naive(lib):
 
 @pytest.mark.parametrize("entry", ["gemm_f32_ex", "gemm_f32_tc3_ex"])
 @pytest.mark.parametrize("trans", [(1, 0), (0, 1), (1, 1)])
-@pytest.mark.parametrize("shape", [(300, 257, 129), (1024, 1024, 256)])
+@pytest.mark.parametrize("shape", [(300, 257, 129), (1024, 1024, 256), (301, 1003, 517)])
 def test_transposed_layouts(lib, entry, trans, shape):
+    # (301, 1003, 517): A stored K x M and B stored K x N with rows off 16-byte
+    # boundaries, restaged (re-pitched) before the product; B stored N x K is
+    # restaged (transposed) in every shape.
     M, N, K = shape
     rng = np.random.default_rng(73)
     A = rng.integers(-4, 5, (M, K)).astype(np.float32)
