@@ -51,8 +51,9 @@
  * needs none).
  * It is allocated on `stream` and freed on `stream` after the kernels that
  * read it, so calls on different streams never share it, and the pool keeps
- * the freed memory for later calls (for the life of the process).  No other
- * entry point allocates device or host memory per call.  All entry points
+ * up to 256 MiB of freed memory for later calls (the rest returns to the
+ * device when the stream is synchronised).  No other entry point allocates
+ * device or host memory per call.  All entry points
  * use the current CUDA device (cudaSetDevice) and are thread-safe.
  *
  * Return value: TMM_OK (0) when the work was enqueued, otherwise one of the

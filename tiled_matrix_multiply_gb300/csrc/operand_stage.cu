@@ -15,8 +15,10 @@
 // The scratch comes from a stream-ordered memory pool the library owns (one
 // per device): allocated on the call's stream before the copy, freed on it
 // after the product, so concurrent calls on different streams never share a
-// buffer.  The pool keeps freed memory for later calls (no release
-// threshold), so steady use makes no driver allocation.
+// buffer.  The pool keeps up to kPoolKeepBytes of freed memory for later
+// calls (a 4096 x 4096 operand is 64 MiB), so steady use makes no driver
+// allocation; memory beyond that goes back to the device when the stream is
+// synchronised.
 #include <cstdint>
 #include <mutex>
 
@@ -118,6 +120,7 @@ cudaError_t launch_copy(Kernel kernel, int64_t items, const DeviceInfo &dev, cud
 }
 
 constexpr int kMaxDevices = 64;
+constexpr uint64_t kPoolKeepBytes = uint64_t(256) << 20;
 std::mutex g_pool_mutex;
 cudaMemPool_t g_pool[kMaxDevices] = {};
 
@@ -132,7 +135,7 @@ cudaError_t device_pool(int dev, cudaMemPool_t *pool) {
     cudaMemPool_t p = nullptr;
     cudaError_t e = cudaMemPoolCreate(&p, &props);
     if (e != cudaSuccess) return e;
-    uint64_t keep = UINT64_MAX;
+    uint64_t keep = kPoolKeepBytes;
     e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
     if (e != cudaSuccess) {
       cudaMemPoolDestroy(p);
