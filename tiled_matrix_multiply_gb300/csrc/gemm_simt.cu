@@ -56,9 +56,13 @@
 // over more blocks than tiles, and a tile can have up to about five
 // contributors: each block waits for the next block's flag, adds C (the sum
 // of the slices after its own) to its sums, stores, and raises its own flag
-// for the block before it.  The order of the additions is fixed, so results
-// are deterministic.  The wait is bounded: past the time limit the block
-// records a timeout in the device status word and finishes.
+// for the block before it.  With few tiles, or C without 16-byte rows, a
+// kernel of its own (gemm_simt_reduce_kernel) gives every block an equal
+// share instead; the blocks store their partial sums into scratch slots and
+// then reduce each tile together, each a band of its rows.  The order of the
+// additions is fixed, so results are deterministic.  Every wait is bounded:
+// past the time limit the block records a timeout in the device status word
+// and finishes.
 #include <atomic>
 #include <cstdint>
 
@@ -1026,9 +1030,9 @@ constexpr int kChainStep = 1;
 //     tiles), every block instead takes an equal share (at least four slices)
 //     and the blocks sharing a tile reduce it together from *partial_slots
 //     slots of partial sums (two per block, two flags): 1024 x 1023 x 1024
-//     21.4 -> 30.1 TFLOP/s, 512 x 512 x 4096 21.7 -> 34.0, 256^3 1.33 -> 1.66;
+//     21.5 -> 31.9 TFLOP/s, 512 x 512 x 4096 21.7 -> 39.1, 256^3 1.33 -> 1.67;
 //     with most slots busy the unequal chains stay ahead (1024^3 37.0 against
-//     32.9, 2048^3 61.5 against 57.9): two blocks sharing an SM progress
+//     32.9, 2048^3 61.9 against 57.9): two blocks sharing an SM progress
 //     unequally, which the chains absorb and equal shares wait for.
 // Every split needs the blocks co-resident (*cooperative).
 int64_t plan_simt(SimtParams &prm, const GemmProblem &p, bool vec_c, bool may_reduce, int BM,
