@@ -1223,9 +1223,13 @@ cudaError_t launch_simt(const GemmProblem &p, const DeviceInfo &dev, cudaStream_
   const bool tma_a = !p.transa || (aligned16(p.A) && p.lda % 4 == 0);
   GemmProblem q = p;
   const int64_t ld_b = (p.N + 3) / 4 * 4, ld_a = (p.M + 3) / 4 * 4;
-  const size_t b_bytes = tma_b ? 0 : size_t(p.K) * size_t(ld_b) * sizeof(float);
+  // A restaged copy whose byte count does not fit in size_t cannot be allocated.
+  const unsigned __int128 b_need = tma_b ? 0 : (unsigned __int128)p.K * ld_b * sizeof(float);
+  const unsigned __int128 a_need = tma_a ? 0 : (unsigned __int128)p.K * ld_a * sizeof(float);
+  if (b_need + a_need + 256 > SIZE_MAX) return cudaErrorMemoryAllocation;
+  const size_t b_bytes = size_t(b_need);
   const size_t b_span = (b_bytes + 255) / 256 * 256;
-  const size_t a_bytes = tma_a ? 0 : size_t(p.K) * size_t(ld_a) * sizeof(float);
+  const size_t a_bytes = size_t(a_need);
   void *scratch = nullptr;
   cudaError_t e = cudaSuccess;
   if (b_bytes + a_bytes > 0) {
