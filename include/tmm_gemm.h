@@ -299,6 +299,21 @@ int tmm_check_device(tmm_stream_t stream);
 int tmm_testing_set_wait_hooks(int drop_signal_block, int64_t wait_limit_ns);
 
 /*
+ * tmm_testing_simt_plan -- testing only; no counterpart in the pages.  The work
+ * split gemm_f32 would launch for an M x N x K product (1 <= sizes <= 2^31 - 1)
+ * on 64 x 256 tiles (wide = 0) or 64 x 512 tiles (wide = 1), C taking 16-byte
+ * stores or not (vec_c), the small-problem split reduced together allowed or
+ * not (may_reduce), with `slots` resident blocks; no CUDA call is made.
+ * out: HOST array of 9 values -- grid size, cooperative launch (0/1), partial-
+ * sum slots (0: none), whole tiles processed first, K-slice units split after
+ * them, and the unequal parts of a tile (parts, base, step, remainder; parts
+ * 0 when not split that way).  TMM_ERR_INVALID_ARG for sizes out of range,
+ * slots <= 0 or out NULL.
+ */
+int tmm_testing_simt_plan(int64_t M, int64_t N, int64_t K, int wide, int vec_c, int may_reduce,
+                          int64_t slots, int64_t *out);
+
+/*
  * window_sum_f32 -- valid sliding-window sums, "CMU DLSys Lecture 12: GPU
  * Acceleration" section 3:
  *     y[i] = sum_{d=0}^{W-1} x[i + d],   0 <= i < n,

@@ -1265,6 +1265,26 @@ cudaError_t simt_device_status(unsigned int *status, bool clear) {
   return cudaMemcpyToSymbol(g_simt_status, &zero, sizeof(unsigned int));
 }
 
+void simt_plan_for_testing(int64_t M, int64_t N, int64_t K, int wide, int vec_c, int may_reduce,
+                           int64_t slots, int64_t out[9]) {
+  GemmProblem p = {M, N, K, nullptr, K, nullptr, N, nullptr, N};
+  SimtParams prm = {};
+  bool coop = false;
+  int64_t partial_slots = 0;
+  const int BN = wide ? WideNConfig::BN : DefaultConfig::BN;
+  const int64_t grid = plan_simt(prm, p, vec_c != 0, may_reduce != 0, DefaultConfig::BM, BN,
+                                 DefaultConfig::BK, slots, &coop, &partial_slots);
+  out[0] = grid;
+  out[1] = coop ? 1 : 0;
+  out[2] = partial_slots;
+  out[3] = prm.dp_tiles;
+  out[4] = prm.sk_iters;
+  out[5] = prm.parts;
+  out[6] = prm.part_base;
+  out[7] = prm.part_step;
+  out[8] = prm.part_rem;
+}
+
 void simt_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns) {
   g_drop_signal_block.store(drop_signal_block, std::memory_order_relaxed);
   g_wait_limit_ns.store(wait_limit_ns > 0 ? wait_limit_ns : int64_t(10) * 1000 * 1000 * 1000,

@@ -93,6 +93,9 @@ cudaError_t launch_window_sum(int64_t n, int W, const float *x, float *y,
 cudaError_t simt_device_status(unsigned int *status, bool clear);
 // Testing hooks of the tiled kernel's stream-K waits (see tmm_gemm.h).
 void simt_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns);
+// The tiled kernels' work split, for host tests (see tmm_testing_simt_plan).
+void simt_plan_for_testing(int64_t M, int64_t N, int64_t K, int wide, int vec_c, int may_reduce,
+                           int64_t slots, int64_t out[9]);
 
 // Array sum: a first launch writes one partial per chunk of the input (at most
 // kSumMaxPartials, in a caller-supplied workspace), a second adds them.
