@@ -314,6 +314,19 @@ int tmm_testing_simt_plan(int64_t M, int64_t N, int64_t K, int wide, int vec_c, 
                           int64_t slots, int64_t *out);
 
 /*
+ * tmm_testing_tc3_plan -- testing only; no counterpart in the pages.  The work
+ * list gemm_f32_tc3 would launch for an M x N x K product (1 <= sizes <=
+ * 2^31 - 1) on block pairs with 256 x 256 tiles (pairs = 1) or single blocks
+ * with 128 x 256 tiles (pairs = 0), with `slots` resident pairs or blocks; no
+ * CUDA call is made.  out: HOST array of 6 values -- tiles, work items, whole
+ * tiles listed first, K-parts of each tile after them (1: none split),
+ * 256-value chunks of K, 16-value K-slices.  TMM_ERR_INVALID_ARG for sizes out
+ * of range, slots <= 0 or out NULL.
+ */
+int tmm_testing_tc3_plan(int64_t M, int64_t N, int64_t K, int pairs, int64_t slots,
+                         int64_t *out);
+
+/*
  * window_sum_f32 -- valid sliding-window sums, "CMU DLSys Lecture 12: GPU
  * Acceleration" section 3:
  *     y[i] = sum_{d=0}^{W-1} x[i + d],   0 <= i < n,

@@ -47,7 +47,7 @@ EXPORTED = GEMM_ENTRY_POINTS + ("gemm_f32_ex", "gemm_f32_tc3", "gemm_f32_tc3_ex"
                                  "window_sum_f32", "sum_f32", "sum_f32_workspace_size",
                                  "softmax_rows_f32",
                                  "tmm_check_device", "tmm_testing_set_wait_hooks",
-                                 "tmm_testing_simt_plan",
+                                 "tmm_testing_simt_plan", "tmm_testing_tc3_plan",
                                  "tmm_last_error_string", "tmm_version",
                                  "gemm_last_error_string", "gemm_check_status")
 
@@ -112,6 +112,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.tmm_testing_simt_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_int, i64, ctypes.c_void_p]
         lib.tmm_testing_simt_plan.restype = ctypes.c_int
+        lib.tmm_testing_tc3_plan.argtypes = [i64, i64, i64, ctypes.c_int, i64, ctypes.c_void_p]
+        lib.tmm_testing_tc3_plan.restype = ctypes.c_int
         lib.tmm_last_error_string.argtypes = []
         lib.tmm_last_error_string.restype = ctypes.c_char_p
         lib.tmm_version.argtypes = []

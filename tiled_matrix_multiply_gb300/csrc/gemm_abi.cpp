@@ -218,6 +218,15 @@ int tmm_testing_simt_plan(int64_t M, int64_t N, int64_t K, int wide, int vec_c, 
   return TMM_OK;
 }
 
+int tmm_testing_tc3_plan(int64_t M, int64_t N, int64_t K, int pairs, int64_t slots,
+                         int64_t *out) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX ||
+      slots <= 0 || out == nullptr)
+    return fail(TMM_ERR_INVALID_ARG, "tmm_testing_tc3_plan: bad arguments");
+  tmm::tc3_plan_for_testing(M, N, K, pairs, slots, out);
+  return TMM_OK;
+}
+
 int tmm_testing_set_wait_hooks(int drop_signal_block, int64_t wait_limit_ns) {
   tmm::simt_set_test_hooks(drop_signal_block, wait_limit_ns);
   tmm::tc3_set_test_hooks(drop_signal_block, wait_limit_ns);

@@ -1225,6 +1225,21 @@ cudaError_t tc3_device_status(unsigned int *status, bool clear) {
   return cudaMemcpyToSymbol(g_tc3_status, &zero, sizeof(unsigned int));
 }
 
+void tc3_plan_for_testing(int64_t M, int64_t N, int64_t K, int pairs, int64_t slots,
+                          int64_t out[6]) {
+  const int64_t BM = pairs ? kT2BM : kTcBM, BN = pairs ? kT2BN : kTcBN;
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  Tc3Params prm = {};
+  const int64_t items = plan_tiles(prm, tiles, slots, pairs ? kTc3MaxBlocks / 2 : kTc3MaxBlocks,
+                                   int(pad_k(K) / kTcBK));
+  out[0] = tiles;
+  out[1] = items;
+  out[2] = prm.dp_tiles;
+  out[3] = prm.parts;
+  out[4] = prm.chunks;
+  out[5] = prm.slices;
+}
+
 void tc3_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns) {
   g_tc3_drop_signal_block.store(drop_signal_block, std::memory_order_relaxed);
   g_tc3_wait_limit_ns.store(wait_limit_ns > 0 ? wait_limit_ns : int64_t(10) * 1000 * 1000 * 1000,

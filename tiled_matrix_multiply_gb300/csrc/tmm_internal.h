@@ -78,6 +78,9 @@ cudaError_t tc3_device_status(unsigned int *status, bool clear);
 size_t tc3_noalloc_scratch_bytes();
 cudaError_t tc3_noalloc_scratch(void **ptr);
 void tc3_set_test_hooks(int drop_signal_block, int64_t wait_limit_ns);
+// The tensor-core kernels' work list, for host tests (see tmm_testing_tc3_plan).
+void tc3_plan_for_testing(int64_t M, int64_t N, int64_t K, int pairs, int64_t slots,
+                          int64_t out[6]);
 
 // Sliding-window sums (y_i = sum_{d<W} x_{i+d}, i < n); 1 <= W <= kMaxWindow.
 constexpr int kMaxWindow = 129;
